@@ -1,0 +1,287 @@
+"""Pins of the CPU oracle to things other than itself (no GPU needed).
+
+Each test checks the oracle against a value the pages print, a closed form, an invariant, a
+textbook/library special case, or brute force on tiny inputs.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import CONFIGS, MoEConfig, make_inputs, pack_int4_g64, variant
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def tiny_cfg(**kw):
+    base = dict(name="pin", T=8, d=128, f=64, E=8, G=2, kg=1, ke=2, r=4, dtype="f32", resid="f32",
+                group_map="contiguous", seed=11)
+    base.update(kw)
+    return MoEConfig(**base)
+
+
+# ------------------------------------------------------------------ canonical FP32 router order
+def test_canonical_logits_exact_integer_sums():
+    """Small integers: every partial sum is exact, so the result must equal the integer dot."""
+    rng = np.random.default_rng(0)
+    x = rng.integers(-3, 4, size=(5, 256)).astype(np.float32)
+    w = rng.integers(-3, 4, size=(7, 256)).astype(np.float32)
+    b = rng.integers(-5, 6, size=7).astype(np.float32)
+    got = oracle.canonical_logits(x, w, b)
+    want = x.astype(np.int64) @ w.astype(np.int64).T + b.astype(np.int64)
+    assert np.array_equal(got.astype(np.int64), want)
+
+
+def _one_hot_case(entries, d=256):
+    x = np.zeros((1, d), dtype=np.float32)
+    for i, v in entries.items():
+        x[0, i] = v
+    return x, np.ones((1, d), dtype=np.float32)
+
+
+def test_canonical_logits_butterfly_order():
+    """Hand-derived rounding: partial sums 0..3 hold 2^24, 1, 1, -2^24 (elements 0, 4, 8, 12).
+
+    xor 16/8/4 add zeros; xor 2: s0 = fl(2^24 + 1) = 2^24 (tie to even), s1 = 1 - 2^24 (exact);
+    xor 1: s0 = 2^24 + (1 - 2^24) = 1.  A left-to-right sum gives 0 and the exact sum is 2.
+    """
+    x, w = _one_hot_case({0: 2.0 ** 24, 4: 1.0, 8: 1.0, 12: -2.0 ** 24})
+    assert oracle.canonical_logits(x, w)[0, 0] == 1.0
+
+
+def test_canonical_logits_in_lane_order():
+    """Elements 0, 1 (block 0) and 128, 129 (block 1) all belong to partial sum 0, added in
+    ascending order: 2^24, +1 -> 2^24, +1 -> 2^24, -2^24 -> 0 (descending order would give 2)."""
+    x, w = _one_hot_case({0: 2.0 ** 24, 1: 1.0, 128: 1.0, 129: -2.0 ** 24})
+    assert oracle.canonical_logits(x, w)[0, 0] == 0.0
+    # element 4 is in partial sum 1, so the same values spread over two sums give 2^24+1-2^24+1
+    x, w = _one_hot_case({0: 2.0 ** 24, 4: 1.0, 128: 1.0, 132: -2.0 ** 24})
+    # s0 = 2^24 + 1 -> 2^24 ; s1 = 1 - 2^24 ; s0 + s1 = 1
+    assert oracle.canonical_logits(x, w)[0, 0] == 1.0
+
+
+def test_canonical_logits_fp64_error_bound():
+    rng = np.random.default_rng(1)
+    d = 1024
+    x = rng.standard_normal((64, d)).astype(np.float32)
+    w = (rng.standard_normal((16, d)) / math.sqrt(d)).astype(np.float32)
+    got = oracle.canonical_logits(x, w).astype(np.float64)
+    exact = x.astype(np.float64) @ w.astype(np.float64).T
+    mag = np.abs(x.astype(np.float64)) @ np.abs(w.astype(np.float64)).T
+    n = d // 32 + 5 + 1
+    assert np.all(np.abs(got - exact) <= n * 2.0 ** -24 * mag * 1.01)
+
+
+# ------------------------------------------------------------------ INT4 format
+def test_int4_golden_convention():
+    spec = json.load(open(os.path.join(GOLDEN, "int4_convention.json")))
+    for case in spec["cases"]:
+        b = np.full(32, 0x88, dtype=np.uint8)          # pad the 64-element group with zeros
+        b[:len(case["bytes"])] = case["bytes"]
+        s = np.array([case["scale"]], dtype=np.float16)
+        v = oracle.dequant_int4(b, s)
+        n = len(case["values"])
+        assert np.array_equal(v[:n], np.array(case["values"]))
+        assert np.all(v[n:] == 0)
+
+
+def test_int4_pack_roundtrip_error_bound():
+    g = torch.Generator().manual_seed(5)
+    w = torch.randn(3, 5, 256, generator=g) * 0.02
+    q, s = pack_int4_g64(w)
+    back = oracle.dequant_int4(q.numpy(), s.numpy())
+    step = np.repeat(s.float().numpy().astype(np.float64), 64, axis=-1)
+    err = np.abs(back - w.double().numpy())
+    # symmetric rounding to the nearest code: error <= step/2 (+ fp16 rounding of the scale)
+    assert np.all(err <= 0.5 * step + 7 * step * 2.0 ** -10 + 1e-12)
+    # and the nibble order matters: swapping the nibbles breaks the bound
+    swapped = ((q.numpy() & 0x0F) << 4) | (q.numpy() >> 4)
+    err2 = np.abs(oracle.dequant_int4(swapped, s.numpy()) - w.double().numpy())
+    assert err2.max() > 2 * step.max()
+
+
+# ------------------------------------------------------------------ routing
+def test_gates_sum_to_one_and_group_gate_one():
+    for name in ("tiny_f32",):
+        inp = make_inputs(CONFIGS[name])
+        cfg = inp["cfg"]
+        r = oracle.route(oracle.moe._np(inp["x"]), oracle.moe._np(inp["w_group"]), None,
+                         oracle.moe._np(inp["w_expert"]), inp["group_map"].numpy(), cfg.kg, cfg.ke)
+        assert np.allclose(r["gate"].sum(1), 1.0, atol=1e-12, rtol=0)
+    cfg = tiny_cfg(T=64, G=4, E=16, kg=2, ke=3)
+    inp = make_inputs(cfg)
+    r = oracle.route(oracle.moe._np(inp["x"]), oracle.moe._np(inp["w_group"]), None,
+                     oracle.moe._np(inp["w_expert"]), inp["group_map"].numpy(), cfg.kg, cfg.ke)
+    assert np.allclose(r["gate"].sum(1), 1.0, atol=1e-12, rtol=0)
+    # experts of a slot group belong to that group and are distinct
+    gm = inp["group_map"].numpy()
+    for t in range(cfg.T):
+        for j in range(cfg.kg):
+            es = r["eidx"][t, j * cfg.ke:(j + 1) * cfg.ke]
+            assert np.all(gm[es] == r["gidx"][t, j]) and len(set(es)) == cfg.ke
+
+
+def test_route_matches_torch_topk_when_one_group():
+    """G = 1: level 1 is trivial and level 2 is a plain top-k over all experts, softmax over the
+    selected logits (library topk/softmax)."""
+    cfg = tiny_cfg(T=32, E=8, G=1, kg=1, ke=3)
+    inp = make_inputs(cfg)
+    x = oracle.moe._np(inp["x"])
+    r = oracle.route(x, oracle.moe._np(inp["w_group"]), None, oracle.moe._np(inp["w_expert"]),
+                     inp["group_map"].numpy(), 1, 3)
+    logits = torch.from_numpy(r["expert_logits"]).double()
+    vals, idx = torch.topk(logits, 3, dim=-1)
+    assert np.array_equal(r["eidx"], idx.numpy())
+    assert np.allclose(r["gate"], torch.softmax(vals, -1).numpy(), rtol=0, atol=1e-15)
+
+
+def _expert_ffn_factored(inp, e, xt):
+    """Independent per-expert FFN in factored form W_base x + B (A^T x) (no materialisation)."""
+    g = int(inp["group_map"][e])
+    out = {}
+    for m, base in (("gate", inp["w_gate"]), ("up", inp["w_up"])):
+        At, Bt = oracle.resid_dense({k: v.numpy() for k, v in inp["resid"][m].items()}, e)
+        out[m] = base[g].double().numpy() @ xt + Bt.T @ (At @ xt)
+    h = out["gate"] / (1 + np.exp(-out["gate"])) * out["up"]
+    At, Bt = oracle.resid_dense({k: v.numpy() for k, v in inp["resid"]["down"].items()}, e)
+    return inp["w_down"][g].double().numpy() @ h + Bt.T @ (At @ h)
+
+
+def test_brute_force_routing_and_output():
+    """T=8, G=2, K=4, top-1 group then top-2: enumerate all 2 x 6 choices per token.  The chosen
+    one is the unique choice whose picks beat every unpicked option, and y equals that choice's
+    gated output (all other choices give different outputs)."""
+    cfg = tiny_cfg()
+    inp = make_inputs(cfg)
+    y, r = oracle.forward_tokens(inp)
+    gm = inp["group_map"].numpy()
+    sg, se = r["group_logits"], r["expert_logits"]
+    for t in range(cfg.T):
+        xt = inp["x"][t].double().numpy()
+        winners = []
+        outs = []
+        for g in range(cfg.G):
+            mem = [e for e in range(cfg.E) if gm[e] == g]
+            for pair in itertools.combinations(mem, 2):
+                other_g = [h for h in range(cfg.G) if h != g]
+                beats_g = all((sg[t, g], -g) > (sg[t, h], -h) for h in other_g)
+                beats_e = all((se[t, e], -e) > (se[t, o], -o) for e in pair for o in mem if o not in pair)
+                lv = np.array([se[t, e] for e in pair], dtype=np.float64)
+                q = np.exp(lv - lv.max()); q /= q.sum()
+                out = sum(q[i] * _expert_ffn_factored(inp, pair[i], xt) for i in range(2))
+                outs.append(out)
+                if beats_g and beats_e:
+                    winners.append((g, set(pair), out))
+        assert len(winners) == 1
+        g, pair, out = winners[0]
+        assert r["gidx"][t, 0] == g and set(r["eidx"][t]) == pair
+        scale = np.abs(out).max()
+        assert np.allclose(y[t], out, rtol=0, atol=1e-12 * scale)
+        assert sum(np.allclose(y[t], o, rtol=0, atol=1e-9 * scale) for o in outs) == 1
+
+
+# ------------------------------------------------------------------ permutation
+def test_permute_invariants_and_lexsort():
+    cfg = tiny_cfg(T=200, G=4, E=16, kg=2, ke=2, d=128, f=64, r=0)
+    inp = make_inputs(cfg)
+    r = oracle.route(oracle.moe._np(inp["x"]), oracle.moe._np(inp["w_group"]), None,
+                     oracle.moe._np(inp["w_expert"]), inp["group_map"].numpy(), cfg.kg, cfg.ke)
+    p = oracle.permute(r["eidx"], inp["group_map"].numpy(), cfg.G, cfg.ke)
+    k = cfg.k
+    gm = inp["group_map"].numpy()
+    flat_e = r["eidx"].reshape(-1)
+    perm = p["perm"]
+    # bijection and inverse
+    assert sorted(perm.tolist()) == list(range(cfg.T * k))
+    assert np.array_equal(p["inv_pos"][perm], np.arange(cfg.T * k))
+    keys = [(gm[flat_e[a]], flat_e[a], a // k) for a in perm]
+    assert all(keys[i] < keys[i + 1] for i in range(len(keys) - 1))       # strictly increasing
+    # library sort of the same keys
+    ls = np.lexsort((np.repeat(np.arange(cfg.T), k), flat_e, gm[flat_e]))
+    assert np.array_equal(ls, perm)
+    # offsets
+    assert p["expert_count"].sum() == cfg.T * k
+    for e in range(cfg.E):
+        seg = perm[p["expert_begin"][e]:p["expert_begin"][e] + p["expert_count"][e]]
+        assert np.all(flat_e[seg] == e)
+    assert p["group_begin"][-1] == cfg.T * k
+    # rows (token, group slot) sorted by (group, token)
+    rows = p["row_asg"]
+    rg = gm[r["eidx"][rows // cfg.kg, (rows % cfg.kg) * cfg.ke]]
+    rkeys = list(zip(rg, rows // cfg.kg))
+    assert all(rkeys[i] < rkeys[i + 1] for i in range(len(rkeys) - 1))
+    assert np.array_equal(p["row_of"][rows], np.arange(cfg.T * cfg.kg))
+    assert np.array_equal(np.diff(p["row_begin"]), np.bincount(rg, minlength=cfg.G))
+
+
+# ------------------------------------------------------------------ FFN special cases
+def test_factor_identity():
+    """W~ x == W_base x + B (A^T x) for every matrix of an INT4 expert."""
+    cfg = tiny_cfg(dtype="bf16", resid="int4", d=256, f=128, r=16, resid_std=0.2)
+    inp = make_inputs(cfg)
+    rng = np.random.default_rng(3)
+    xt = rng.standard_normal(256)
+    for e in (0, 5):
+        g = int(inp["group_map"][e])
+        At, Bt = oracle.resid_dense({k: v.numpy() for k, v in inp["resid"]["gate"].items()}, e)
+        W = oracle.materialise(inp["w_gate"][g].float().numpy(), At, Bt)
+        lhs = W @ xt
+        rhs = inp["w_gate"][g].double().numpy() @ xt + Bt.T @ (At @ xt)
+        assert np.allclose(lhs, rhs, rtol=1e-12, atol=1e-12 * np.abs(rhs).max())
+
+
+def test_rank0_is_dense_group_base_moe():
+    """r = 0 and one group per token: y_t = FFN_base^{g(t)}(x_t) whatever the expert choice (gates
+    of the chosen group sum to 1).  Checked against torch FP64 silu/matmul."""
+    cfg = tiny_cfg(T=32, r=0, dtype="bf16", resid="int4", d=256, f=128)
+    inp = make_inputs(cfg)
+    y, r = oracle.forward_tokens(inp)
+    x = inp["x"].double()
+    for t in range(cfg.T):
+        g = int(r["gidx"][t, 0])
+        a = torch.nn.functional.silu(inp["w_gate"][g].double() @ x[t]) * (inp["w_up"][g].double() @ x[t])
+        want = inp["w_down"][g].double() @ a
+        assert torch.allclose(torch.from_numpy(y[t]), want, rtol=1e-11, atol=1e-12)
+
+
+def test_one_expert_per_group_rank0_is_textbook_topk_moe():
+    """K = 1 (G = E), r = 0: the layer is a standard top-k MoE with router w_group and experts the
+    bases, y = sum_i softmax(topk logits)_i FFN_i(x) (per-expert torch loop)."""
+    cfg = tiny_cfg(T=24, E=6, G=6, kg=2, ke=1, r=0)
+    inp = make_inputs(cfg)
+    y, r = oracle.forward_tokens(inp)
+    logits = torch.from_numpy(r["group_logits"]).double()
+    vals, idx = torch.topk(logits, 2, dim=-1)
+    gates = torch.softmax(vals, -1)
+    x = inp["x"].double()
+    for t in range(cfg.T):
+        acc = torch.zeros(cfg.d, dtype=torch.float64)
+        for j in range(2):
+            e = int(idx[t, j])
+            a = torch.nn.functional.silu(inp["w_gate"][e].double() @ x[t]) * (inp["w_up"][e].double() @ x[t])
+            acc += gates[t, j] * (inp["w_down"][e].double() @ a)
+        assert torch.allclose(torch.from_numpy(y[t]), acc, rtol=1e-11, atol=1e-12)
+
+
+def test_residual_is_visible_in_amplified_variant():
+    cfg = tiny_cfg(T=16, dtype="bf16", resid="int4", d=256, f=128, r=16)
+    y_amp, _ = oracle.forward_tokens(make_inputs(variant(cfg, "amplified")))
+    y_r0, _ = oracle.forward_tokens(make_inputs(variant(cfg.replace(resid_std=0.2), "rank0")))
+    diff = np.abs(y_amp - y_r0).sum() / np.abs(y_r0).sum()
+    assert diff > 0.05
+
+
+# ------------------------------------------------------------------ parameter accounting
+def test_compression_ratio_closed_form():
+    spec = json.load(open(os.path.join(GOLDEN, "compression_ratio.json")))
+    cr = oracle.compression_ratio(spec["d_in"], spec["d_out"], spec["K"], spec["r"])
+    assert cr == pytest.approx(spec["formula_value"], rel=1e-12)
+    assert abs(cr - spec["page_printed_value"]) > 0.5      # the printed figure is not the formula's
+    pc = oracle.param_counts(d=4096, f=4096, E=8, G=1, r=16)
+    # one matrix type of one group reproduces CR exactly
+    assert pc["standard"] / pc["clustered"] == pytest.approx(cr, rel=1e-12)
