@@ -1,0 +1,371 @@
+#!/usr/bin/env python
+"""Throughput of the clustered, compressed MoE layer forward pass (tokens/s) on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+One step = one whole forward pass (route, permute, gate/up GEMM with the residual/SwiGLU epilogue,
+down GEMM, combine) over the workload's T tokens, inputs resident in HBM.  Between timed steps the
+L2 is flushed (a 256 MiB write).  Multi-GPU (torchrun): every rank runs an independent replica on
+its own GPU (tokens are independent; no collective on the data path), weak scaling.
+The oracle is only imported by the CPU-baseline leg and by --impl reference.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer fwd tokens/s on 1 B300; % of BF16 tensor or HBM roofline"
+DEFAULT_CONFIG = "small_bf16_int4"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_name(cfg) -> str:
+    return (f"{cfg.name}: T={cfg.T} d_model={cfg.d} d_ff={cfg.f} E={cfg.E} G={cfg.G} "
+            f"top{cfg.kg} group(s) then top{cfg.ke} in group, r={cfg.r} {cfg.resid} residual, "
+            f"{cfg.dtype} base, SwiGLU")
+
+
+# ------------------------------------------------------------------ clocks during the timed region
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        with open(self.file.name) as fh:
+            lines = [ln.strip() for ln in fh if ln.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ CPU oracle timing (rank 0 only)
+def oracle_tokens_per_s(inp, seconds: float, chunk: int):
+    """Runs the oracle (route + FFN of each chunk of tokens) until `seconds` elapsed."""
+    import numpy as np
+
+    import oracle
+    from oracle.moe import _np
+    cfg = inp["cfg"]
+    x = _np(inp["x"]).astype(np.float32)
+    wgp, bgp, wep = _np(inp["w_group"]), _np(inp["b_group"]), _np(inp["w_expert"])
+    gm = _np(inp["group_map"])
+    done, t0 = 0, time.perf_counter()
+    start = 0
+    while True:
+        toks = np.arange(start, min(start + chunk, cfg.T))
+        routing = oracle.route(x[toks], wgp, bgp, wep, gm, cfg.kg, cfg.ke)
+        sub = dict(inp)
+        sub["x"] = inp["x"][toks[0]:toks[-1] + 1]
+        sub["cfg"] = cfg.replace(T=len(toks))
+        oracle.forward_tokens(sub, routing=routing)
+        done += len(toks)
+        start = (start + chunk) % cfg.T
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return done / el, done, el
+
+
+CPU_CHUNK = {"tiny_f32": 256, "small_bf16_int4": 1024, "mixtral_prefill": 16,
+             "finegrained_skewed": 512, "decode": 4}
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from compressed_expert_two_b300 import _lib as L
+    from compressed_expert_two_b300 import workload
+    from compressed_expert_two_b300.layer import DeviceLayer
+    from synth import CONFIGS, make_inputs
+
+    cfg = CONFIGS[args.config]
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    inp = make_inputs(cfg)
+    layer = DeviceLayer(inp, device=dev)
+    out = layer.new_outputs()
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(max(args.warmup, 3)):
+        layer.forward(out=out)
+    torch.cuda.synchronize(dev)
+    if layer.status() != 0:
+        raise RuntimeError("device status after warm-up: %d" % layer.status())
+
+    # kernels of one forward and the groups/experts the workload hits (for the byte count)
+    probe = [torch.cuda.Event(enable_timing=True) for _ in range(64)]
+    for e in probe:
+        e.record(stream)
+    arr = L.moe_hier_profile_begin([e.cuda_event for e in probe])
+    layer.forward(out=out)
+    names = L.moe_hier_profile_end()
+    del arr
+    n_k = len(names)
+    torch.cuda.synchronize(dev)
+    eidx = out["eidx"].cpu()
+    experts_hit = int(torch.unique(eidx).numel())
+    groups_hit = int(torch.unique(out["gidx"].cpu()).numel())
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_k + 1)] for _ in range(K)]
+    for row in ev:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize(dev)
+    gpu_index = local_rank
+    if os.environ.get("CUDA_VISIBLE_DEVICES"):
+        ids = os.environ["CUDA_VISIBLE_DEVICES"].split(",")
+        gpu_index = int(ids[local_rank]) if ids[local_rank].isdigit() else local_rank
+    clocks = Clocks(gpu_index) if rank == 0 else None
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_(i & 0xFF)                      # evict the weights from L2 between steps
+        arr = L.moe_hier_profile_begin([e.cuda_event for e in ev[i]])
+        layer.forward(out=out, routing_out=False)
+        L.moe_hier_profile_end()
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    if layer.status() != 0:
+        raise RuntimeError("device status after timed steps: %d" % layer.status())
+
+    step_ms = [ev[i][0].elapsed_time(ev[i][n_k]) for i in range(K)]
+    kern_ms = {}
+    for i in range(K):
+        for j, nm in enumerate(names):
+            kern_ms.setdefault(nm, []).append(ev[i][j].elapsed_time(ev[i][j + 1]))
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * cfg.T * K / (total_ms / 1e3)
+
+    # ---- end to end through the C ABI with host buffers (copies inside the timed region)
+    x_h = inp["x"].pin_memory()
+    y_h = torch.empty(cfg.T, cfg.d, dtype=layer.act_dtype).pin_memory()
+    x_d = torch.empty_like(layer.x)
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for _ in range(2):
+        x_d.copy_(x_h, non_blocking=True)
+        layer.forward(x=x_d, out=out, routing_out=False)
+        y_h.copy_(out["y"], non_blocking=True)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        e2e_ev[i][0].record(stream)
+        x_d.copy_(x_h, non_blocking=True)
+        layer.forward(x=x_d, out=out, routing_out=False)
+        y_h.copy_(out["y"], non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * cfg.T * K / (e2e_ms / 1e3)
+    act_b = 2 if cfg.dtype == "bf16" else 4
+
+    # ---- roofline of the dominant kernel
+    peaks, peak_src = load_peaks()
+    dom = max(kern_ms, key=lambda n: sum(kern_ms[n]))
+    dom_ms = statistics.mean(kern_ms[dom])
+    f_up, f_down = workload.ffn_flops(cfg)
+    if "up" in dom:
+        dom_flops = f_up
+    elif "down" in dom:
+        dom_flops = f_down
+    else:
+        dom_flops = workload.flops(cfg)
+    tensor_bound = cfg.T >= 512
+    if tensor_bound:
+        achieved = dom_flops / (dom_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 2),
+                "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "peak_source": f"{peak_src} bf16_tflops (burst: kernel timed within one step)",
+                "algorithmic_flops_per_launch": dom_flops, "traffic": None}
+    else:
+        byts = workload.bytes_moved(cfg, groups_hit, experts_hit)
+        achieved = byts / (dom_ms / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "peak_source": f"{peak_src} hbm_gbs", "traffic": None}
+    step_mean = statistics.mean(step_ms)
+
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(step_mean, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": {"workload": workload_name(cfg), "T": cfg.T, "d_model": cfg.d, "d_ff": cfg.f,
+                   "E": cfg.E, "G": cfg.G, "top_k_group": cfg.kg, "top_k_expert": cfg.ke,
+                   "rank": cfg.r, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "flushed between timed steps (256 MiB write)",
+                   "groups_hit": groups_hit, "experts_hit": experts_hit},
+        "roofline": roof,
+        "achieved_tflops_step": round(workload.flops(cfg) / (step_mean / 1e3) / 1e12, 2),
+        "kernels_ms": {n: round(statistics.mean(v), 5) for n, v in kern_ms.items()},
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": cfg.T * cfg.d * act_b, "d2h_bytes_per_step": cfg.T * cfg.d * act_b},
+        "gpu_launches": n_k * K,
+        "clocks": clk,
+        "wall_s_timed": round(wall, 3),
+    }
+    return res, inp
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    res, inp = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            tps, n, el = oracle_tokens_per_s(inp, args.cpu_seconds, CPU_CHUNK.get(args.config, 256))
+            res["cpu_baseline"] = {"value": round(tps, 2), "unit": "tokens/s", "cores": cpu_cores(),
+                                   "kind": "oracle",
+                                   "sample": f"{n} tokens of the same workload (chunks of "
+                                             f"{CPU_CHUNK.get(args.config, 256)}; route + FP64 FFN with "
+                                             f"every W~ materialised) in {el:.1f} s"}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_reference(args):
+    """The oracle as the reference arm, on the host cores, each step a bounded token sample."""
+    from synth import CONFIGS, make_inputs
+    cfg = CONFIGS[args.config]
+    inp = make_inputs(cfg)
+    chunk = CPU_CHUNK.get(args.config, 256)
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        tps, n, el = oracle_tokens_per_s(inp, 0.0, chunk)
+        if i >= args.warmup:
+            per_step.append((n, el))
+    tok = sum(n for n, _ in per_step)
+    sec = sum(e for _, e in per_step)
+    value = tok / sec
+    res = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(1e3 * sec / max(len(per_step), 1), 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded; shapes and distributions of the workload)",
+           "config": {"workload": workload_name(cfg), "T": cfg.T, "sample_tokens_per_step": chunk},
+           "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cpu_cores(),
+                            "kind": "oracle",
+                            "sample": f"{chunk} tokens per step (route + FP64 FFN, every W~ materialised)"},
+           "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,147 @@
+"""ctypes binding of libmoehier.so: the C-ABI entry points under the same names.
+
+Argument marshalling only (tensor -> device pointer, dataclass -> C struct).  Every step of the
+layer runs in the library's CUDA kernels; there is no fallback.  Importing this module fails
+loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmoehier.so")
+
+MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = \
+    0, -1, -2, -3, -4, -5
+MOE_F32, MOE_BF16 = 0, 1
+MOE_RESID_F32, MOE_RESID_INT4_G64 = 0, 1
+
+
+class MoeHierDesc(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("G", ctypes.c_int32), ("topk_group", ctypes.c_int32),
+                ("topk_expert", ctypes.c_int32), ("rank", ctypes.c_int32),
+                ("act_dtype", ctypes.c_int32), ("resid_fmt", ctypes.c_int32)]
+
+
+class MoeHierResid(ctypes.Structure):
+    _fields_ = [("A", ctypes.c_void_p * 3), ("B", ctypes.c_void_p * 3),
+                ("sA", ctypes.c_void_p * 3), ("sB", ctypes.c_void_p * 3)]
+
+
+EXPORTS = ["moe_hier_workspace_size", "moe_hier_route", "moe_hier_permute", "moe_hier_ffn",
+           "moe_hier_combine", "moe_hier_forward", "moe_hier_get_status", "moe_hier_status_string",
+           "moe_hier_profile_begin", "moe_hier_profile_end"]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {code} ({status_string(code)})")
+        self.code = code
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libmoehier.so is not built ({LIB_PATH}); run "
+                          "`python -m compressed_expert_two_b300.build` or __graft_entry__.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    D, Rp = ctypes.POINTER(MoeHierDesc), ctypes.POINTER(MoeHierResid)
+    lib.moe_hier_workspace_size.argtypes = [D, ctypes.POINTER(ctypes.c_int)]
+    lib.moe_hier_workspace_size.restype = S
+    lib.moe_hier_route.argtypes = [D, P, P, P, P, P, P, P, P, P, S, P]
+    lib.moe_hier_permute.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P, S, P]
+    lib.moe_hier_ffn.argtypes = [D, P, P, P, P, P, Rp, P, P, P, P, P, P, S, P]
+    lib.moe_hier_combine.argtypes = [D, P, P, P]
+    lib.moe_hier_forward.argtypes = [D, P, P, P, P, P, P, P, P, Rp, P, P, P, P, P, P, S, P]
+    lib.moe_hier_get_status.argtypes = [P, P]
+    lib.moe_hier_profile_begin.argtypes = [ctypes.POINTER(ctypes.c_void_p), I]
+    lib.moe_hier_profile_end.argtypes = [ctypes.POINTER(ctypes.c_char_p), I]
+    lib.moe_hier_status_string.argtypes = [I]
+    lib.moe_hier_status_string.restype = ctypes.c_char_p
+    for name in EXPORTS:
+        if name not in ("moe_hier_workspace_size", "moe_hier_status_string"):
+            getattr(lib, name).restype = I
+    return lib
+
+
+lib = _load()
+
+
+def _p(t) -> Optional[int]:
+    """Device (or host) address of a tensor; None for None."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != MOE_OK:
+        raise MoeError(fn, rc)
+
+
+def status_string(code: int) -> str:
+    return lib.moe_hier_status_string(code).decode()
+
+
+def moe_hier_workspace_size(desc: MoeHierDesc) -> int:
+    st = ctypes.c_int(0)
+    n = lib.moe_hier_workspace_size(ctypes.byref(desc), ctypes.byref(st))
+    _check("moe_hier_workspace_size", st.value)
+    return n
+
+
+def moe_hier_route(desc, x, w_group, b_group, w_expert, group_map_host, gidx, eidx, gate, ws, ws_bytes, stream):
+    _check("moe_hier_route", lib.moe_hier_route(
+        ctypes.byref(desc), _p(x), _p(w_group), _p(b_group), _p(w_expert), _p(group_map_host),
+        _p(gidx), _p(eidx), _p(gate), _p(ws), ws_bytes, stream))
+
+
+def moe_hier_permute(desc, group_map_host, eidx, perm, inv_pos, expert_begin, expert_count,
+                     group_begin, row_asg, row_of, row_begin, ws, ws_bytes, stream):
+    _check("moe_hier_permute", lib.moe_hier_permute(
+        ctypes.byref(desc), _p(group_map_host), _p(eidx), _p(perm), _p(inv_pos), _p(expert_begin),
+        _p(expert_count), _p(group_begin), _p(row_asg), _p(row_of), _p(row_begin), _p(ws),
+        ws_bytes, stream))
+
+
+def moe_hier_ffn(desc, x, group_map_host, w_gate, w_up, w_down, resid, eidx, gate, row_asg,
+                 row_begin, y_rows, ws, ws_bytes, stream):
+    _check("moe_hier_ffn", lib.moe_hier_ffn(
+        ctypes.byref(desc), _p(x), _p(group_map_host), _p(w_gate), _p(w_up), _p(w_down),
+        ctypes.byref(resid), _p(eidx), _p(gate), _p(row_asg), _p(row_begin), _p(y_rows), _p(ws),
+        ws_bytes, stream))
+
+
+def moe_hier_combine(desc, y_rows, y, stream):
+    _check("moe_hier_combine", lib.moe_hier_combine(ctypes.byref(desc), _p(y_rows), _p(y), stream))
+
+
+def moe_hier_forward(desc, x, w_group, b_group, w_expert, group_map_host, w_gate, w_up, w_down,
+                     resid, y, gidx, eidx, gate, perm, ws, ws_bytes, stream):
+    _check("moe_hier_forward", lib.moe_hier_forward(
+        ctypes.byref(desc), _p(x), _p(w_group), _p(b_group), _p(w_expert), _p(group_map_host),
+        _p(w_gate), _p(w_up), _p(w_down), ctypes.byref(resid), _p(y), _p(gidx), _p(eidx),
+        _p(gate), _p(perm), _p(ws), ws_bytes, stream))
+
+
+def moe_hier_profile_begin(event_handles) -> ctypes.Array:
+    """Start marking kernel launches with the given cudaEvent_t handles (ints); returns the C
+    array, which the caller keeps alive until moe_hier_profile_end."""
+    arr = (ctypes.c_void_p * len(event_handles))(*event_handles)
+    _check("moe_hier_profile_begin", lib.moe_hier_profile_begin(arr, len(event_handles)))
+    return arr
+
+
+def moe_hier_profile_end(max_names: int = 256) -> list:
+    names = (ctypes.c_char_p * max_names)()
+    n = lib.moe_hier_profile_end(names, max_names)
+    return [names[i].decode() for i in range(min(n, max_names))]
+
+
+def moe_hier_get_status(ws, stream) -> int:
+    return lib.moe_hier_get_status(_p(ws), stream)

@@ -1,0 +1,278 @@
+// C ABI of libmoehier: descriptor validation, workspace planning and launch sequencing.
+#include <string.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// ---- profiling marks (per host thread) ----
+static thread_local void* const* g_prof_ev = nullptr;
+static thread_local int g_prof_n = 0, g_prof_i = 0, g_prof_launches = 0;
+static thread_local const char* g_prof_names[256];
+
+void prof_start(cudaStream_t st) {
+  if (g_prof_ev && g_prof_i == 0 && g_prof_n > 0) {
+    cudaEventRecord((cudaEvent_t)g_prof_ev[0], st);
+    g_prof_i = 1;
+  }
+}
+
+void prof_mark(const char* name, cudaStream_t st) {
+  if (!g_prof_ev) return;
+  if (g_prof_launches < 256) g_prof_names[g_prof_launches] = name;
+  ++g_prof_launches;
+  if (g_prof_i > 0 && g_prof_i < g_prof_n) cudaEventRecord((cudaEvent_t)g_prof_ev[g_prof_i++], st);
+}
+
+static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+Plan make_plan(const LayerArgs& a) {
+  Plan p{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
+  const size_t T = a.T, R = a.R, k = a.k, E = a.E, G = a.G;
+  p.status = take(sizeof(DevStatus));
+  p.logits = take(T * (G + E) * 4);
+  p.gidx = take(T * a.kg * 4);
+  p.eidx = take(T * k * 4);
+  p.gate = take(T * k * 4);
+  p.perm = take(T * k * 4);
+  p.inv_pos = take(T * k * 4);
+  p.ebeg = take(E * 4);
+  p.ecnt = take(E * 4);
+  p.gbeg = take((G + 1) * 4);
+  p.row_asg = take(R * 4);
+  p.row_of = take(R * 4);
+  p.rbeg = take((G + 1) * 4);
+  p.nblk = (a.T + 255) / 256;
+  p.cnt = take((size_t)p.nblk * (E + G) * 4);
+  p.off = take((size_t)p.nblk * (E + G) * 4);
+  p.U = take(R * a.ke * 2 * a.r * 4);
+  p.H = take(R * a.ke * (size_t)a.f * 4);
+  p.hsum = take(R * (size_t)a.f * 4);
+  p.V = take(R * a.ke * a.r * 4);
+  p.yrows = take(a.kg > 1 ? T * a.kg * (size_t)a.d * (a.bf16 ? 2 : 4) : 0);
+  p.total = o;
+  return p;
+}
+
+// Host-side validation of the descriptor and group map; fills the kernel argument block.
+static int validate(const moe_hier_desc* desc, const int32_t* group_map, LayerArgs* a) {
+  if (!desc) return MOE_ERR_INVALID;
+  const moe_hier_desc& D = *desc;
+  if (D.T < 0 || D.d_model <= 0 || D.d_ff <= 0 || D.E <= 0 || D.G <= 0) return MOE_ERR_INVALID;
+  if (D.E % D.G != 0 || D.E > kMaxE) return MOE_ERR_INVALID;
+  const int K = D.E / D.G;
+  if (D.topk_group < 1 || D.topk_group > D.G) return MOE_ERR_INVALID;
+  if (D.topk_expert < 1 || D.topk_expert > K) return MOE_ERR_INVALID;
+  if (D.topk_group * D.topk_expert > kMaxK) return MOE_ERR_UNSUPPORTED;
+  if (K > 32) return MOE_ERR_UNSUPPORTED;
+  if (D.d_model % 128 != 0 || D.d_ff % 64 != 0) return MOE_ERR_INVALID;
+  if (D.rank < 0) return MOE_ERR_INVALID;
+  if (D.rank > kMaxRank) return MOE_ERR_UNSUPPORTED;
+  if (D.act_dtype != MOE_F32 && D.act_dtype != MOE_BF16) return MOE_ERR_INVALID;
+  if (D.resid_fmt != MOE_RESID_F32 && D.resid_fmt != MOE_RESID_INT4_G64) return MOE_ERR_INVALID;
+  if ((D.act_dtype == MOE_BF16) != (D.resid_fmt == MOE_RESID_INT4_G64)) return MOE_ERR_UNSUPPORTED;
+  memset(a, 0, sizeof(*a));
+  a->T = D.T; a->d = D.d_model; a->f = D.d_ff; a->E = D.E; a->G = D.G; a->K = K;
+  a->kg = D.topk_group; a->ke = D.topk_expert; a->k = a->kg * a->ke; a->r = D.rank;
+  a->bf16 = D.act_dtype == MOE_BF16;
+  a->int4 = D.resid_fmt == MOE_RESID_INT4_G64;
+  a->R = a->T * a->kg;
+  a->tab.E = D.E; a->tab.G = D.G; a->tab.K = K;
+  if (group_map) {
+    int fill[kMaxE];
+    for (int g = 0; g < D.G; ++g) fill[g] = 0;
+    for (int e = 0; e < D.E; ++e) {
+      const int g = group_map[e];
+      if (g < 0 || g >= D.G || fill[g] >= K) return MOE_ERR_INVALID;
+      a->tab.member[g * K + fill[g]] = (uint8_t)e;   // ascending e inside each group
+      a->tab.group_of[e] = (uint8_t)g;
+      a->tab.local_of[e] = (uint8_t)fill[g];
+      ++fill[g];
+    }
+  }
+  return MOE_OK;
+}
+
+static int check_ws(const Plan& p, void* ws, size_t ws_bytes) {
+  if (!ws || ((uintptr_t)ws & 255) != 0 || ws_bytes < p.total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+template <typename P> static P* at(void* ws, size_t off) { return (P*)((char*)ws + off); }
+
+static ResidPtrs resid_ptrs(const LayerArgs& a, const moe_hier_resid* r) {
+  ResidPtrs rp{};
+  const int din[3] = {a.d, a.d, a.f}, dout[3] = {a.f, a.f, a.d};
+  for (int m = 0; m < 3; ++m) {
+    rp.A[m] = ResidView{r ? r->A[m] : nullptr, r ? (const __half*)r->sA[m] : nullptr, din[m], a.r, a.int4};
+    rp.B[m] = ResidView{r ? r->B[m] : nullptr, r ? (const __half*)r->sB[m] : nullptr, dout[m], a.r, a.int4};
+  }
+  return rp;
+}
+
+static bool resid_ok(const LayerArgs& a, const moe_hier_resid* r) {
+  if (a.r == 0) return true;
+  if (!r) return false;
+  for (int m = 0; m < 3; ++m) {
+    if (!r->A[m] || !r->B[m]) return false;
+    if (a.int4 && (!r->sA[m] || !r->sB[m])) return false;
+  }
+  return true;
+}
+
+static int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_hier_workspace_size(const moe_hier_desc* desc, int* status_out) {
+  LayerArgs a;
+  const int st = validate(desc, nullptr, &a);
+  if (status_out) *status_out = st;
+  if (st != MOE_OK) return 0;
+  return make_plan(a).total;
+}
+
+int moe_hier_route(const moe_hier_desc* desc, const void* x, const void* w_group,
+                   const float* b_group, const void* w_expert, const int32_t* group_map_host,
+                   int32_t* gidx, int32_t* eidx, float* gate, void* ws, size_t ws_bytes,
+                   void* stream) {
+  LayerArgs a;
+  if (!group_map_host) return MOE_ERR_INVALID;
+  int st = validate(desc, group_map_host, &a);
+  if (st != MOE_OK) return st;
+  if (a.T > 0 && (!x || !w_group || !w_expert || !gidx || !eidx || !gate)) return MOE_ERR_INVALID;
+  const Plan p = make_plan(a);
+  if ((st = check_ws(p, ws, ws_bytes)) != MOE_OK) return st;
+  prof_start((cudaStream_t)stream);
+  return cuda_status(launch_route(a, x, w_group, b_group, w_expert, at<float>(ws, p.logits), gidx,
+                                  eidx, gate, (cudaStream_t)stream));
+}
+
+int moe_hier_permute(const moe_hier_desc* desc, const int32_t* group_map_host, const int32_t* eidx,
+                     int32_t* perm, int32_t* inv_pos, int32_t* expert_begin, int32_t* expert_count,
+                     int32_t* group_begin, int32_t* row_asg, int32_t* row_of, int32_t* row_begin,
+                     void* ws, size_t ws_bytes, void* stream) {
+  LayerArgs a;
+  if (!group_map_host) return MOE_ERR_INVALID;
+  int st = validate(desc, group_map_host, &a);
+  if (st != MOE_OK) return st;
+  if (!row_begin || (a.T > 0 && (!eidx || !row_asg))) return MOE_ERR_INVALID;
+  const Plan p = make_plan(a);
+  if ((st = check_ws(p, ws, ws_bytes)) != MOE_OK) return st;
+  PermOut o{perm, inv_pos, expert_begin, expert_count, group_begin, row_asg, row_of, row_begin};
+  prof_start((cudaStream_t)stream);
+  return cuda_status(launch_permute(a, eidx, o, at<int32_t>(ws, p.cnt), at<int32_t>(ws, p.off),
+                                    p.nblk, (cudaStream_t)stream));
+}
+
+int moe_hier_ffn(const moe_hier_desc* desc, const void* x, const int32_t* group_map_host,
+                 const void* w_gate, const void* w_up, const void* w_down,
+                 const moe_hier_resid* resid, const int32_t* eidx, const float* gate,
+                 const int32_t* row_asg, const int32_t* row_begin, void* y_rows, void* ws,
+                 size_t ws_bytes, void* stream) {
+  LayerArgs a;
+  if (!group_map_host) return MOE_ERR_INVALID;
+  int st = validate(desc, group_map_host, &a);
+  if (st != MOE_OK) return st;
+  if (a.T > 0 && (!x || !w_gate || !w_up || !w_down || !eidx || !gate || !row_asg || !row_begin ||
+                  !y_rows || !resid_ok(a, resid)))
+    return MOE_ERR_INVALID;
+  const Plan p = make_plan(a);
+  if ((st = check_ws(p, ws, ws_bytes)) != MOE_OK) return st;
+  FfnBufs b{at<float>(ws, p.U), at<float>(ws, p.H), at<float>(ws, p.hsum), at<float>(ws, p.V)};
+  prof_start((cudaStream_t)stream);
+  return cuda_status(launch_ffn_simt(a, x, w_gate, w_up, w_down, resid_ptrs(a, resid), eidx, gate,
+                                     row_asg, row_begin, y_rows, b, (cudaStream_t)stream));
+}
+
+int moe_hier_combine(const moe_hier_desc* desc, const void* y_rows, void* y, void* stream) {
+  LayerArgs a;
+  int st = validate(desc, nullptr, &a);
+  if (st != MOE_OK) return st;
+  if (a.T > 0 && (!y_rows || !y)) return MOE_ERR_INVALID;
+  prof_start((cudaStream_t)stream);
+  return cuda_status(launch_combine(a, y_rows, y, (cudaStream_t)stream));
+}
+
+int moe_hier_forward(const moe_hier_desc* desc, const void* x, const void* w_group,
+                     const float* b_group, const void* w_expert, const int32_t* group_map_host,
+                     const void* w_gate, const void* w_up, const void* w_down,
+                     const moe_hier_resid* resid, void* y, int32_t* gidx_opt, int32_t* eidx_opt,
+                     float* gate_opt, int32_t* perm_opt, void* ws, size_t ws_bytes, void* stream) {
+  LayerArgs a;
+  if (!group_map_host) return MOE_ERR_INVALID;
+  int st = validate(desc, group_map_host, &a);
+  if (st != MOE_OK) return st;
+  if (a.T > 0 && (!x || !w_group || !w_expert || !w_gate || !w_up || !w_down || !y ||
+                  !resid_ok(a, resid)))
+    return MOE_ERR_INVALID;
+  const Plan p = make_plan(a);
+  if ((st = check_ws(p, ws, ws_bytes)) != MOE_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t* gidx = gidx_opt ? gidx_opt : at<int32_t>(ws, p.gidx);
+  int32_t* eidx = eidx_opt ? eidx_opt : at<int32_t>(ws, p.eidx);
+  float* gate = gate_opt ? gate_opt : at<float>(ws, p.gate);
+  int32_t* perm = perm_opt ? perm_opt : at<int32_t>(ws, p.perm);
+  prof_start(s);
+  cudaError_t e = cudaMemsetAsync(at<DevStatus>(ws, p.status), 0, sizeof(DevStatus), s);
+  if (e == cudaSuccess)
+    e = launch_route(a, x, w_group, b_group, w_expert, at<float>(ws, p.logits), gidx, eidx, gate, s);
+  PermOut o{perm, at<int32_t>(ws, p.inv_pos), at<int32_t>(ws, p.ebeg), at<int32_t>(ws, p.ecnt),
+            at<int32_t>(ws, p.gbeg), at<int32_t>(ws, p.row_asg), at<int32_t>(ws, p.row_of),
+            at<int32_t>(ws, p.rbeg)};
+  if (e == cudaSuccess)
+    e = launch_permute(a, eidx, o, at<int32_t>(ws, p.cnt), at<int32_t>(ws, p.off), p.nblk, s);
+  void* yrows = a.kg > 1 ? at<void>(ws, p.yrows) : y;
+  FfnBufs b{at<float>(ws, p.U), at<float>(ws, p.H), at<float>(ws, p.hsum), at<float>(ws, p.V)};
+  if (e == cudaSuccess)
+    e = launch_ffn_simt(a, x, w_gate, w_up, w_down, resid_ptrs(a, resid), eidx, gate, o.row_asg,
+                        o.rbeg, yrows, b, s);
+  if (e == cudaSuccess) e = launch_combine(a, yrows, y, s);
+  return cuda_status(e);
+}
+
+int moe_hier_get_status(const void* ws, void* stream) {
+  if (!ws) return MOE_ERR_WORKSPACE;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
+  DevStatus h{};
+  if (cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  return h.code;
+}
+
+int moe_hier_profile_begin(void* const* events, int n_events) {
+  if (!events || n_events < 1) return MOE_ERR_INVALID;
+  g_prof_ev = events;
+  g_prof_n = n_events;
+  g_prof_i = 0;
+  g_prof_launches = 0;
+  return MOE_OK;
+}
+
+int moe_hier_profile_end(const char** names, int max_names) {
+  const int n = g_prof_launches;
+  for (int i = 0; names && i < max_names && i < n && i < 256; ++i) names[i] = g_prof_names[i];
+  g_prof_ev = nullptr;
+  g_prof_n = g_prof_i = g_prof_launches = 0;
+  return n;
+}
+
+const char* moe_hier_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,61 @@
+// Shared device helpers of libmoehier (sm_103a).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moehier.h"
+
+namespace moe {
+
+constexpr int kMaxE = 256;
+constexpr int kMaxK = 16;     // k_g * k_e
+constexpr int kMaxRank = 64;
+constexpr int kQGroup = 64;   // INT4 elements per FP16 scale
+
+// Group membership, passed to kernels by value (no device allocation for the host group map).
+struct GroupTable {
+  int E, G, K;
+  uint8_t member[kMaxE];    // member[g*K + i] = i-th expert (ascending id) of group g
+  uint8_t group_of[kMaxE];  // group of expert e
+  uint8_t local_of[kMaxE];  // position of expert e inside its group
+};
+
+// Device status word at the start of every workspace (bounded waits report here).
+struct DevStatus {
+  int code;
+  int where;
+};
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+// Element c of an INT4 group-64 rank row (codes [n/2] bytes, scales [n/64] fp16).
+__device__ __forceinline__ float int4_at(const uint8_t* codes, const __half* scales, int c) {
+  const uint8_t b = codes[c >> 1];
+  const int u = (c & 1) ? (b & 0xF) : (b >> 4);
+  return (float)(u - 8) * __half2float(scales[c / kQGroup]);
+}
+
+// Residual factor element: rank row k of expert e, column c (n columns per rank row).
+struct ResidView {
+  const void* vals;     // F32 [E][r][n] or INT4 bytes [E][r][n/2]
+  const __half* scales; // [E][r][n/64] (INT4)
+  int n, r;
+  bool int4;
+  __device__ __forceinline__ float at(int e, int k, int c) const {
+    const size_t row = (size_t)e * r + k;
+    if (int4) return int4_at((const uint8_t*)vals + row * (n / 2), scales + row * (n / kQGroup), c);
+    return ((const float*)vals)[row * n + c];
+  }
+};
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+}  // namespace moe

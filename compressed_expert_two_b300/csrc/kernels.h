@@ -1,0 +1,61 @@
+// Host-side launchers of libmoehier (internal to the library).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+// Validated layer shape plus the group table, shared by every launcher.
+struct LayerArgs {
+  int T, d, f, E, G, K, kg, ke, k, r;
+  bool bf16;        // act dtype BF16 (else FP32)
+  bool int4;        // residual INT4 group-64 (else FP32)
+  int R;            // rows = T * kg
+  GroupTable tab;
+};
+
+// Workspace carving (offsets in bytes from ws; every region 256-byte aligned).
+struct Plan {
+  size_t status, logits, gidx, eidx, gate;
+  size_t perm, inv_pos, ebeg, ecnt, gbeg, row_asg, row_of, rbeg;
+  size_t cnt, off;   // per-block histograms and their exclusive offsets
+  int nblk;          // permutation blocks
+  size_t U, H, hsum, V, yrows;
+  size_t total;
+};
+
+Plan make_plan(const LayerArgs& a);
+
+// Profiling marks (see moe_hier_profile_begin): call right after every kernel launch.
+void prof_start(cudaStream_t st);
+void prof_mark(const char* kernel_name, cudaStream_t st);
+
+cudaError_t launch_route(const LayerArgs& a, const void* x, const void* wg, const float* bg,
+                         const void* we, float* logits, int32_t* gidx, int32_t* eidx, float* gate,
+                         cudaStream_t st);
+
+struct PermOut {
+  int32_t *perm, *inv_pos, *ebeg, *ecnt, *gbeg, *row_asg, *row_of, *rbeg;
+};
+cudaError_t launch_permute(const LayerArgs& a, const int32_t* eidx, const PermOut& o, int32_t* cnt,
+                           int32_t* off, int nblk, cudaStream_t st);
+
+struct ResidPtrs {
+  ResidView A[3], B[3];
+};
+struct FfnBufs {
+  float* U;      // [R][ke][2][r]
+  float* H;      // [R][ke][f]
+  float* hsum;   // [R][f]
+  float* V;      // [R][ke][r]
+};
+cudaError_t launch_ffn_simt(const LayerArgs& a, const void* x, const void* wg, const void* wu,
+                            const void* wd, const ResidPtrs& rp, const int32_t* eidx,
+                            const float* gate, const int32_t* row_asg, const int32_t* row_begin,
+                            void* y_rows, const FfnBufs& b, cudaStream_t st);
+
+cudaError_t launch_combine(const LayerArgs& a, const void* y_rows, void* y, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,161 @@
+/*
+ * moehier.h -- C ABI of libmoehier.so: the forward pass of a clustered, compressed
+ * Mixture-of-Experts layer on one NVIDIA B300 (sm_103a).
+ *
+ * The layer ("Breaking the MoE LLM Trilemma: Dynamic Expert Clustering with Structured
+ * Compression", paper notes, overall framework and key designs 2-4):
+ *   E experts are split into G groups of K = E/G.  Expert i of group g has, for each of its three
+ *   matrices m in {gate, up, down}, the weight  W~_i = W_base^g + B_i A_i^T  (key design 2, W~
+ *   equation), A_i in R^{d_in x r}, B_i in R^{d_out x r}; the base is BF16 (FP32 in the FP32
+ *   format) and the residual INT4 (key design 4).  A token is routed to its top-k_g groups by the
+ *   group router and, inside each chosen group, to that group's top-k_e experts by the expert
+ *   router (key design 3).  The expert body is the SwiGLU FFN  W~_down (silu(W~_gate x) * W~_up x)
+ *   and the layer output is the gated sum  y = sum_i G_i(x) E_i(x)  ("混合专家模型的路由机制与
+ *   工程落地", section 1.2).  Gates: softmax over the k_g selected group logits times the softmax
+ *   over the k_e selected expert logits inside the group ("MoE架构演进白皮书", chapter 1 top-2
+ *   code: top-k of the logits, then softmax of the selected ones).  Dropless.
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller, except group_map_host (host
+ *     memory, read during the call only).  Row-major, nn.Linear layout (W is [d_out][d_in]).
+ *   - The library never allocates, frees or synchronises (except moe_hier_get_status, which
+ *     synchronises the given stream).  Work is enqueued on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream) and the call returns.  Scratch memory is the caller's workspace
+ *     `ws` of `ws_bytes` bytes (>= moe_hier_workspace_size), 256-byte aligned.  Calls that share
+ *     a workspace must be ordered on one stream; distinct workspaces may run concurrently.
+ *   - Return value: MOE_OK, or a negative moe_status.  MOE_ERR_INVALID / _UNSUPPORTED /
+ *     _WORKSPACE are detected on the host before anything is enqueued.  MOE_ERR_CUDA means a
+ *     launch failed (cudaGetLastError); earlier steps of the call may already be enqueued.
+ *     Conditions found on the device (a bounded wait that ran out) are written to a status word
+ *     in the workspace and reported by moe_hier_get_status.
+ *   - Inputs must be finite; NaN logits give unspecified routing.
+ *
+ * Shapes (T tokens, d = d_model, f = d_ff, k = k_g * k_e routed experts per token)
+ *   x         [T][d]            act dtype          y [T][d] act dtype
+ *   w_group   [G][d]            act dtype          b_group [G] float32 or NULL
+ *   w_expert  [E][d]            act dtype          group_map_host [E] int32, exactly K per group
+ *   w_gate, w_up [G][f][d]      act dtype          w_down [G][d][f] act dtype
+ *   residual of matrix m (0 gate, 1 up, 2 down), d_in/d_out = (d,f), (d,f), (f,d):
+ *     A[m] = A^T rank-major [E][r][d_in],  B[m] = B^T rank-major [E][r][d_out]
+ *     MOE_RESID_F32:      float32 values; sA/sB unused (NULL)
+ *     MOE_RESID_INT4_G64: uint8 [E][r][n/2], element 2j in the HIGH nibble and 2j+1 in the LOW
+ *       nibble of byte j, value = (nibble - 8) * scale, one FP16 scale per 64 consecutive
+ *       elements: sA[m] [E][r][d_in/64], sB[m] [E][r][d_out/64] ("MoE架构演进白皮书" section 3.2
+ *       unpack convention: even offset high nibble, zero point 8).
+ *   Routing outputs: gidx [T][k_g] int32 (best group first); eidx [T][k] int32 global expert ids,
+ *     slot = group rank * k_e + expert rank (best first); gate [T][k] float32.
+ *   Router arithmetic ("混合专家模型的路由机制与工程落地" section 3.1: the router runs in FP32),
+ *     in a fixed order so indices are reproducible: 32 partial sums, partial l owning the
+ *     elements i with (i mod 128) div 4 == l added in ascending i (fl32 product, fl32 add), then
+ *     s_l += s_{l xor o} for o = 16, 8, 4, 2, 1; logit = fl32(s_0 + b).  Ties: lower index first.
+ */
+#ifndef MOEHIER_H
+#define MOEHIER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID = -1,      /* bad shape, pointer, group map or descriptor                    */
+  MOE_ERR_UNSUPPORTED = -2,  /* valid layer, but no kernel for this dtype / format / size       */
+  MOE_ERR_WORKSPACE = -3,    /* ws NULL, misaligned, or smaller than moe_hier_workspace_size    */
+  MOE_ERR_CUDA = -4,         /* a CUDA launch or runtime call failed                           */
+  MOE_ERR_TIMEOUT = -5       /* a bounded device-side wait ran out (reported via get_status)   */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+typedef enum { MOE_RESID_F32 = 0, MOE_RESID_INT4_G64 = 1 } moe_resid_fmt;
+
+typedef struct {
+  int32_t T, d_model, d_ff, E, G;
+  int32_t topk_group;   /* k_g, 1 <= k_g <= G                                                  */
+  int32_t topk_expert;  /* k_e, 1 <= k_e <= K = E/G (per chosen group)                         */
+  int32_t rank;         /* r >= 0; r == 0 means no residual (residual pointers may be NULL)      */
+  int32_t act_dtype;    /* moe_dtype of x, y, routers and base weights                           */
+  int32_t resid_fmt;    /* moe_resid_fmt                                                         */
+} moe_hier_desc;
+/* Limits: T >= 0; d_model % 128 == 0; d_ff % 64 == 0; E % G == 0; E <= 256; k_e*k_g <= 16;
+ * r <= 64.  INT4 residuals need a BF16 layer, F32 residuals an F32 layer.                    */
+
+typedef struct {
+  const void* A[3];   /* gate, up, down: A^T [E][r][d_in]  (F32 values or packed INT4)         */
+  const void* B[3];   /* gate, up, down: B^T [E][r][d_out]                                      */
+  const void* sA[3];  /* FP16 scales of A (INT4 only)                                           */
+  const void* sB[3];  /* FP16 scales of B (INT4 only)                                           */
+} moe_hier_resid;
+
+/* Bytes of workspace the calls below need for this layer (0 on an invalid descriptor; then
+ * *status_out, if non-NULL, holds the reason). */
+size_t moe_hier_workspace_size(const moe_hier_desc* desc, int* status_out);
+
+/* Level-1 and level-2 routing ("Breaking the MoE LLM Trilemma", key design 3).
+ * Writes gidx, eidx and gate (shapes above).  Uses the workspace for the logits. */
+int moe_hier_route(const moe_hier_desc* desc, const void* x, const void* w_group,
+                   const float* b_group, const void* w_expert, const int32_t* group_map_host,
+                   int32_t* gidx, int32_t* eidx, float* gate,
+                   void* ws, size_t ws_bytes, void* stream);
+
+/* Single-device form of the two-level dispatch (key design 3): stable counting sorts.
+ *   Assignments a = t*k + slot, ordered by key (group, expert, token):
+ *     perm [T*k] (position -> a), inv_pos [T*k] (a -> position),
+ *     expert_begin [E], expert_count [E] (indexed by expert id), group_begin [G+1].
+ *   (token, group-slot) rows b = t*k_g + j, ordered by key (group, token):
+ *     row_asg [T*k_g] (position -> b), row_of [T*k_g] (b -> position), row_begin [G+1].
+ * Every output is exact (integers, deterministic).  Any output pointer except row_asg and
+ * row_begin may be NULL to skip it. */
+int moe_hier_permute(const moe_hier_desc* desc, const int32_t* group_map_host, const int32_t* eidx,
+                     int32_t* perm, int32_t* inv_pos, int32_t* expert_begin, int32_t* expert_count,
+                     int32_t* group_begin, int32_t* row_asg, int32_t* row_of, int32_t* row_begin,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/* Expert computation with base reuse (key design 2: W~ x = W_base x + B (A^T x), the base term
+ * computed once per (token, group) and shared by the group's experts on that token), SwiGLU
+ * and gating.  For each row (t, j) in row_asg order with group g and experts e_s (s < k_e):
+ *   y_rows[t][j] = sum_s gate[t][j*k_e+s] * W~_down,e_s (silu(W~_gate,e_s x_t) * W~_up,e_s x_t)
+ * y_rows is [T][k_g][d] in TOKEN order (act dtype); with k_g == 1 it can be y itself.
+ * row_asg / row_begin come from moe_hier_permute. */
+int moe_hier_ffn(const moe_hier_desc* desc, const void* x, const int32_t* group_map_host,
+                 const void* w_gate, const void* w_up, const void* w_down,
+                 const moe_hier_resid* resid, const int32_t* eidx, const float* gate,
+                 const int32_t* row_asg, const int32_t* row_begin, void* y_rows,
+                 void* ws, size_t ws_bytes, void* stream);
+
+/* y[t] = sum_{j < k_g} y_rows[t][j] (slot order), act dtype in and out, FP32 sum
+ * ("混合专家模型的路由机制与工程落地" section 1.2 combine).  y may alias y_rows when k_g == 1. */
+int moe_hier_combine(const moe_hier_desc* desc, const void* y_rows, void* y, void* stream);
+
+/* The whole layer: route -> permute -> ffn -> combine, enqueued back to back.
+ * gidx_opt, eidx_opt, gate_opt, perm_opt (may be NULL) receive copies of the routing results. */
+int moe_hier_forward(const moe_hier_desc* desc, const void* x, const void* w_group,
+                     const float* b_group, const void* w_expert, const int32_t* group_map_host,
+                     const void* w_gate, const void* w_up, const void* w_down,
+                     const moe_hier_resid* resid, void* y,
+                     int32_t* gidx_opt, int32_t* eidx_opt, float* gate_opt, int32_t* perm_opt,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, then returns the device status word of `ws` (MOE_OK or
+ * MOE_ERR_TIMEOUT), or MOE_ERR_CUDA if the stream reported an error. */
+int moe_hier_get_status(const void* ws, void* stream);
+
+/* Static text for a moe_status value. */
+const char* moe_hier_status_string(int status);
+
+/* Profiling aid (the pages have no counterpart; it changes no result).  After
+ * moe_hier_profile_begin(events, n), the entry points called on this host thread record
+ * events[0] on their stream before their first kernel and events[i] right after their i-th
+ * kernel launch (i = 1 .. n-1; later launches are not marked).  `events` are cudaEvent_t
+ * handles owned by the caller.  moe_hier_profile_end stops recording and returns the number of
+ * kernels launched since begin; names[i] (i < max_names, names may be NULL) receives a static
+ * string naming the i-th kernel.  Kernel i ran between events[i] and events[i+1]. */
+int moe_hier_profile_begin(void* const* events, int n_events);
+int moe_hier_profile_end(const char** names, int max_names);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOEHIER_H */

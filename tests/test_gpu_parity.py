@@ -1,0 +1,166 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bar: routing indices, gidx and every permutation output bit-exact; gates within 1e-6; layer
+output y within max|y - y_ref| <= 2e-2 max|y_ref| and sum|y - y_ref| <= 5e-3 sum|y_ref|
+(BF16 inputs, FP32 accumulation).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import CONFIGS, MoEConfig, make_inputs, variant
+
+pytestmark = pytest.mark.gpu
+
+MAX_TOL, MEAN_TOL, GATE_TOL = 2e-2, 5e-3, 1e-6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(cuda_ok):
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def device_layer(inp):
+    from compressed_expert_two_b300.layer import DeviceLayer
+    return DeviceLayer(inp, device="cuda")
+
+
+def check_y(y_gpu, y_ref, what=""):
+    y = y_gpu.float().cpu().numpy().astype(np.float64)
+    err = np.abs(y - y_ref)
+    scale = np.abs(y_ref).max()
+    assert err.max() <= MAX_TOL * scale, f"{what} max err {err.max() / scale:.3g} of max|y|"
+    assert err.sum() <= MEAN_TOL * np.abs(y_ref).sum(), f"{what} mean rel err {err.sum() / np.abs(y_ref).sum():.3g}"
+    return err.max() / scale, err.sum() / np.abs(y_ref).sum()
+
+
+def check_routing(out, ref):
+    assert np.array_equal(out["gidx"].cpu().numpy(), ref["gidx"])
+    assert np.array_equal(out["eidx"].cpu().numpy(), ref["eidx"])
+    assert np.abs(out["gate"].cpu().numpy().astype(np.float64) - ref["gate"]).max() <= GATE_TOL
+
+
+def small(**kw):
+    base = dict(name="case", T=300, d=256, f=192, E=8, G=2, kg=1, ke=2, r=16, dtype="bf16",
+                resid="int4", group_map="perm", seed=21)
+    base.update(kw)
+    return MoEConfig(**base)
+
+
+# ------------------------------------------------------------------ whole layer, small sizes
+CASES = {
+    "tiny_f32": CONFIGS["tiny_f32"],
+    "tiny_f32_amp": variant(CONFIGS["tiny_f32"], "amplified"),
+    "tiny_f32_base0": variant(CONFIGS["tiny_f32"], "base_zero"),
+    "small_bf16_int4": CONFIGS["small_bf16_int4"],
+    "bf16_ragged": small(),
+    "bf16_amp": variant(small(seed=22), "amplified"),
+    "bf16_base0": variant(small(seed=23), "base_zero"),
+    "bf16_rank0": variant(small(seed=24), "rank0"),
+    "bf16_kg2_ke3": small(T=515, E=32, G=4, kg=2, ke=3, f=320, group_map="contiguous", seed=25,
+                          resid_std=0.2),
+    "bf16_zipf": small(T=777, d=384, E=64, G=8, kg=2, ke=3, group_map="contiguous", seed=26,
+                       zipf_s=1.2, resid_std=0.2),
+    "bf16_one_token": small(T=1, seed=27),
+    "bf16_K1": small(T=200, E=4, G=4, kg=2, ke=1, seed=28),
+    "f32_kg2": small(T=130, dtype="f32", resid="f32", r=4, kg=2, ke=1, E=8, G=4, seed=29, resid_std=0.2),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_forward_parity(name):
+    cfg = CASES[name]
+    inp = make_inputs(cfg)
+    layer = device_layer(inp)
+    out = layer.forward()
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    ref = oracle.forward(inp)
+    check_routing(out, ref)
+    assert np.array_equal(out["perm"].cpu().numpy(), ref["perm"])
+    check_y(out["y"], ref["y"], name)
+
+
+def test_stages_match_oracle_and_forward():
+    cfg = small(T=515, E=32, G=4, kg=2, ke=3, f=320, group_map="contiguous", seed=31)
+    inp = make_inputs(cfg)
+    layer = device_layer(inp)
+    ref = oracle.forward(inp)
+    r = layer.route()
+    check_routing(r, ref)
+    p = layer.permute(r["eidx"])
+    for key in ("perm", "inv_pos", "expert_begin", "expert_count", "group_begin", "row_asg",
+                "row_of", "row_begin"):
+        assert np.array_equal(p[key].cpu().numpy(), ref[key]), key
+    y_rows = layer.ffn(layer.x, r["eidx"], r["gate"], p["row_asg"], p["row_begin"])
+    y = layer.combine(y_rows)
+    y_fwd = layer.forward()["y"]
+    torch.cuda.synchronize()
+    check_y(y, ref["y"], "stages")
+    assert torch.equal(y, y_fwd)            # same kernels, same order: identical bits
+
+
+def test_all_tokens_one_group_and_empty_experts():
+    cfg = small(T=256, E=16, G=4, seed=33)
+    inp = make_inputs(cfg)
+    inp["b_group"] = torch.tensor([0.0, 0.0, 50.0, 0.0])    # every token picks group 2
+    layer = device_layer(inp)
+    out = layer.forward()
+    ref = oracle.forward(inp)
+    check_routing(out, ref)
+    assert np.all(ref["gidx"] == 2)
+    p = layer.permute(out["eidx"])
+    for key in ("expert_begin", "expert_count", "group_begin", "row_begin"):
+        assert np.array_equal(p[key].cpu().numpy(), ref[key]), key
+    check_y(out["y"], ref["y"])
+
+
+def test_empty_batch():
+    cfg = small(T=0, seed=34)
+    inp = make_inputs(cfg)
+    layer = device_layer(inp)
+    out = layer.forward()
+    p = layer.permute(out["eidx"])
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert p["row_begin"].cpu().tolist() == [0] * (cfg.G + 1)
+
+
+def test_repeat_calls_are_deterministic():
+    inp = make_inputs(small(T=400, seed=35))
+    layer = device_layer(inp)
+    a = layer.forward()
+    b = layer.forward()
+    torch.cuda.synchronize()
+    for k in ("y", "eidx", "gate", "perm"):
+        assert torch.equal(a[k], b[k]), k
+
+
+# ------------------------------------------------------------------ the full-size workloads
+def full_size_check(name, n_sample):
+    cfg = CONFIGS[name]
+    inp = make_inputs(cfg)
+    layer = device_layer(inp)
+    out = layer.forward()
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    gm = inp["group_map"].numpy()
+    routing = oracle.route(oracle.moe._np(inp["x"]), oracle.moe._np(inp["w_group"]),
+                           oracle.moe._np(inp["b_group"]), oracle.moe._np(inp["w_expert"]), gm,
+                           cfg.kg, cfg.ke)
+    check_routing(out, routing)
+    pref = oracle.permute(routing["eidx"], gm, cfg.G, cfg.ke)
+    assert np.array_equal(out["perm"].cpu().numpy(), pref["perm"])
+    rng = np.random.default_rng(cfg.seed)
+    toks = np.sort(rng.choice(cfg.T, size=min(n_sample, cfg.T), replace=False))
+    toks[0], toks[-1] = 0, cfg.T - 1
+    y_ref, _ = oracle.forward_tokens(inp, toks, routing=routing)
+    check_y(out["y"][torch.from_numpy(toks).cuda()], y_ref, name)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,n", [("mixtral_prefill", 24), ("finegrained_skewed", 64), ("decode", 8)])
+def test_full_size_sampled(name, n):
+    full_size_check(name, n)
