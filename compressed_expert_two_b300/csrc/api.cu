@@ -48,10 +48,27 @@ Plan make_plan(const LayerArgs& a) {
   p.nblk = (a.T + 255) / 256;
   p.cnt = take((size_t)p.nblk * (E + G) * 4);
   p.off = take((size_t)p.nblk * (E + G) * 4);
-  p.U = take(R * a.ke * 2 * a.r * 4);
-  p.H = take(R * a.ke * (size_t)a.f * 4);
-  p.hsum = take(R * (size_t)a.f * 4);
-  p.V = take(R * a.ke * a.r * 4);
+  p.tc = tc_path_ok(a);
+  if (p.tc) {
+    const size_t Rp = R < 128 ? 128 : R, KRP = tc_krp(a), d = a.d, f = a.f;
+    p.krp = (int)KRP;
+    p.nchunks = tc_up_chunks(a);
+    p.X = take(Rp * d * 2);
+    p.Ain = take(G * 4 * KRP * d * 2);
+    p.Bgs = take(G * f * KRP * 2);
+    p.Bus = take(G * f * KRP * 2);
+    p.Adn = take(G * KRP * f * 2);
+    p.Bdn = take(G * d * 2 * KRP * 2);
+    p.Ubf = take(Rp * 2 * KRP * 4);
+    p.hsum_bf = take(Rp * f * 2);
+    p.Vpart = take((size_t)p.nchunks * R * a.ke * a.r * 4);
+    p.Vt = take(Rp * 2 * KRP * 2);
+  } else {
+    p.U = take(R * a.ke * 2 * a.r * 4);
+    p.H = take(R * a.ke * (size_t)a.f * 4);
+    p.hsum = take(R * (size_t)a.f * 4);
+    p.V = take(R * a.ke * a.r * 4);
+  }
   p.yrows = take(a.kg > 1 ? T * a.kg * (size_t)a.d * (a.bf16 ? 2 : 4) : 0);
   p.total = o;
   return p;
@@ -123,6 +140,22 @@ static bool resid_ok(const LayerArgs& a, const moe_hier_resid* r) {
   return true;
 }
 
+static cudaError_t run_ffn(const LayerArgs& a, const Plan& p, void* ws, const void* x, const void* wg,
+                           const void* wu, const void* wd, const moe_hier_resid* resid, const int32_t* eidx,
+                           const float* gate, const int32_t* row_asg, const int32_t* row_begin, void* y_rows,
+                           cudaStream_t s) {
+  if (p.tc) {
+    TcBufs b{at<__nv_bfloat16>(ws, p.X),   at<__nv_bfloat16>(ws, p.Ain),    at<__nv_bfloat16>(ws, p.Bgs),
+             at<__nv_bfloat16>(ws, p.Bus), at<__nv_bfloat16>(ws, p.Adn),    at<__nv_bfloat16>(ws, p.Bdn),
+             at<float>(ws, p.Ubf), at<__nv_bfloat16>(ws, p.hsum_bf), at<__nv_bfloat16>(ws, p.Vt),
+             at<float>(ws, p.Vpart)};
+    return launch_ffn_tc(a, x, wg, wu, wd, resid_ptrs(a, resid), eidx, gate, row_asg, row_begin, y_rows, b,
+                         at<DevStatus>(ws, p.status), s);
+  }
+  FfnBufs b{at<float>(ws, p.U), at<float>(ws, p.H), at<float>(ws, p.hsum), at<float>(ws, p.V)};
+  return launch_ffn_simt(a, x, wg, wu, wd, resid_ptrs(a, resid), eidx, gate, row_asg, row_begin, y_rows, b, s);
+}
+
 static int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 }  // namespace moe
@@ -186,10 +219,9 @@ int moe_hier_ffn(const moe_hier_desc* desc, const void* x, const int32_t* group_
     return MOE_ERR_INVALID;
   const Plan p = make_plan(a);
   if ((st = check_ws(p, ws, ws_bytes)) != MOE_OK) return st;
-  FfnBufs b{at<float>(ws, p.U), at<float>(ws, p.H), at<float>(ws, p.hsum), at<float>(ws, p.V)};
   prof_start((cudaStream_t)stream);
-  return cuda_status(launch_ffn_simt(a, x, w_gate, w_up, w_down, resid_ptrs(a, resid), eidx, gate,
-                                     row_asg, row_begin, y_rows, b, (cudaStream_t)stream));
+  return cuda_status(run_ffn(a, p, ws, x, w_gate, w_up, w_down, resid, eidx, gate, row_asg, row_begin, y_rows,
+                             (cudaStream_t)stream));
 }
 
 int moe_hier_combine(const moe_hier_desc* desc, const void* y_rows, void* y, void* stream) {
@@ -230,10 +262,8 @@ int moe_hier_forward(const moe_hier_desc* desc, const void* x, const void* w_gro
   if (e == cudaSuccess)
     e = launch_permute(a, eidx, o, at<int32_t>(ws, p.cnt), at<int32_t>(ws, p.off), p.nblk, s);
   void* yrows = a.kg > 1 ? at<void>(ws, p.yrows) : y;
-  FfnBufs b{at<float>(ws, p.U), at<float>(ws, p.H), at<float>(ws, p.hsum), at<float>(ws, p.V)};
   if (e == cudaSuccess)
-    e = launch_ffn_simt(a, x, w_gate, w_up, w_down, resid_ptrs(a, resid), eidx, gate, o.row_asg,
-                        o.rbeg, yrows, b, s);
+    e = run_ffn(a, p, ws, x, w_gate, w_up, w_down, resid, eidx, gate, o.row_asg, o.rbeg, yrows, s);
   if (e == cudaSuccess) e = launch_combine(a, yrows, y, s);
   return cuda_status(e);
 }

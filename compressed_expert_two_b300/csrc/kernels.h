@@ -23,6 +23,10 @@ struct Plan {
   size_t cnt, off;   // per-block histograms and their exclusive offsets
   int nblk;          // permutation blocks
   size_t U, H, hsum, V, yrows;
+  // tensor-core path
+  bool tc;
+  int krp, nchunks;
+  size_t X, Ain, Bgs, Bus, Adn, Bdn, Ubf, hsum_bf, Vpart, Vt;
   size_t total;
 };
 
@@ -55,6 +59,20 @@ cudaError_t launch_ffn_simt(const LayerArgs& a, const void* x, const void* wg, c
                             const void* wd, const ResidPtrs& rp, const int32_t* eidx,
                             const float* gate, const int32_t* row_asg, const int32_t* row_begin,
                             void* y_rows, const FfnBufs& b, cudaStream_t st);
+
+struct TcBufs {
+  __nv_bfloat16 *X, *Ain, *Bgs, *Bus, *Adn, *Bdn;
+  float* U;
+  __nv_bfloat16 *hsum, *Vt;
+  float* Vpart;
+};
+bool tc_path_ok(const LayerArgs& a);
+int tc_krp(const LayerArgs& a);
+int tc_up_chunks(const LayerArgs& a);
+cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, const void* wu, const void* wd,
+                          const ResidPtrs& rp, const int32_t* eidx, const float* gate, const int32_t* row_asg,
+                          const int32_t* row_begin, void* y_rows, const TcBufs& b, DevStatus* status,
+                          cudaStream_t st);
 
 cudaError_t launch_combine(const LayerArgs& a, const void* y_rows, void* y, cudaStream_t st);
 
