@@ -249,12 +249,37 @@ cudaError_t launch_ffn_simt(const LayerArgs& a, const void* x, const void* wg, c
 template <typename T>
 __global__ void combine_kernel(const T* __restrict__ yr, T* __restrict__ y, int Tn, int d, int kg) {
   const size_t n = (size_t)Tn * d;
-  for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < n;
-       idx += (size_t)gridDim.x * blockDim.x) {
+  for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < n; idx += (size_t)gridDim.x * blockDim.x) {
     const size_t t = idx / d, c = idx % d;
     float acc = 0.f;
     for (int j = 0; j < kg; ++j) acc += to_f32(yr[(t * kg + j) * d + c]);
     y[idx] = from_f32<T>(acc);
+  }
+}
+
+// BF16, 8 columns per thread.
+__global__ void combine_bf16x8_kernel(const __nv_bfloat16* __restrict__ yr, __nv_bfloat16* __restrict__ y, int Tn,
+                                      int d, int kg) {
+  const size_t n8 = (size_t)Tn * d / 8;
+  for (size_t w = blockIdx.x * (size_t)blockDim.x + threadIdx.x; w < n8; w += (size_t)gridDim.x * blockDim.x) {
+    const size_t t = w / (d / 8), c = (w % (d / 8)) * 8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < kg; ++j) {
+      const uint4 v = *reinterpret_cast<const uint4*>(yr + (t * kg + j) * d + c);
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[2 * q] += __uint_as_float(u[q] << 16);
+        acc[2 * q + 1] += __uint_as_float(u[q] & 0xFFFF0000u);
+      }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+      o[q] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(y + t * d + c) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -267,7 +292,7 @@ cudaError_t launch_combine(const LayerArgs& a, const void* y_rows, void* y, cuda
   const size_t n = (size_t)a.T * a.d;
   const int blocks = (int)((n + 255) / 256 < 148 * 16 ? (n + 255) / 256 : 148 * 16);
   if (a.bf16)
-    combine_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)y_rows, (__nv_bfloat16*)y, a.T, a.d, a.kg);
+    combine_bf16x8_kernel<<<blocks, 256, 0, st>>>((const __nv_bfloat16*)y_rows, (__nv_bfloat16*)y, a.T, a.d, a.kg);
   else
     combine_kernel<float><<<blocks, 256, 0, st>>>((const float*)y_rows, (float*)y, a.T, a.d, a.kg);
   prof_mark("combine", st);

@@ -34,7 +34,6 @@ namespace {
 
 constexpr int kTile = 128;      // rows per tile (MMA M)
 constexpr int kNf = 64;         // d_ff columns per gate/up tile
-constexpr int kEpiThreads = 128;
 
 // Tile index -> (group, first row, end of the group's rows); false if the index is unused.
 __device__ __forceinline__ bool tile_of(const int32_t* row_begin, int G, int tile, int& g, int& r0, int& r1) {
@@ -74,16 +73,12 @@ __device__ __forceinline__ float code_at(const ResidView& v, int e, int k, int c
   return (float)(((c & 1) ? (b & 0xF) : (b >> 4)) - 8);
 }
 
-// Every output element written exactly once per launch.  Row-major outputs: 8 consecutive
-// elements per work item; transposed outputs: one KRP-wide row per work item.
-__global__ void resid_prep_kernel(PrepArgs p, GroupTable tab) {
+// Row-major stacks (Ain hi/lo, Adn): 8 consecutive elements per work item, grid-stride.
+__global__ void resid_prep_rows_kernel(PrepArgs p, GroupTable tab) {
   const int G = p.G, K = p.K, r = p.r, KRP = p.KRP, d = p.d, f = p.f;
   const size_t nAin = (size_t)G * 2 * KRP * (d / 8);   // hi/lo pairs written together
   const size_t nAdn = (size_t)G * KRP * (f / 8);
-  const size_t nBg = (size_t)G * f;
-  const size_t nBd = (size_t)G * d;
-  const size_t total = nAin + nAdn + 2 * nBg + nBd;
-  for (size_t w = blockIdx.x * (size_t)blockDim.x + threadIdx.x; w < total; w += (size_t)gridDim.x * blockDim.x) {
+  for (size_t w = blockIdx.x * (size_t)blockDim.x + threadIdx.x; w < nAin + nAdn; w += (size_t)gridDim.x * blockDim.x) {
     if (w < nAin) {
       // Ain[g][0][m*KRP + j*r + k][c] = hi, Ain[g][1][...] = lo of A_m,e_j^T[k][c]
       const int c8 = (int)(w % (d / 8)) * 8;
@@ -104,7 +99,7 @@ __global__ void resid_prep_kernel(PrepArgs p, GroupTable tab) {
       __nv_bfloat16* dst = p.Ain + ((size_t)g * 2 * (2 * KRP) + row) * d + c8;
       *reinterpret_cast<uint4*>(dst) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       *reinterpret_cast<uint4*>(dst + (size_t)2 * KRP * d) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    } else if (w < nAin + nAdn) {
+    } else {
       // Adn[g][j*r + k][c] = code of A_down,e_j^T[k][c]
       const size_t idx = w - nAin;
       const int c8 = (int)(idx % (f / 8)) * 8;
@@ -118,42 +113,64 @@ __global__ void resid_prep_kernel(PrepArgs p, GroupTable tab) {
           out[q] = tc::pack_bf16(code_at(p.A[2], e, k, c8 + 2 * q), code_at(p.A[2], e, k, c8 + 2 * q + 1));
       }
       *reinterpret_cast<uint4*>(p.Adn + rowg * f + c8) = make_uint4(out[0], out[1], out[2], out[3]);
-    } else {
-      size_t idx = w - nAin - nAdn;
-      int m, n, width;
-      __nv_bfloat16* base;
-      if (idx < nBg) { m = 0; n = f; base = p.Bgs; width = KRP; }
-      else if (idx < 2 * nBg) { idx -= nBg; m = 1; n = f; base = p.Bus; width = KRP; }
-      else { idx -= 2 * nBg; m = 2; n = d; base = p.Bdn; width = 2 * KRP; }
-      const int g = (int)(idx / n), c = (int)(idx % n);
-      const ResidView& v = p.B[m];
-      __nv_bfloat16* dst = base + idx * width;
-      for (int jk0 = 0; jk0 < KRP; jk0 += 8) {
-        uint32_t out[4], lo[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float t2[2], l2[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int jk = jk0 + 2 * q + h, j = jk / r, k = jk % r;
-            if (j >= K) { t2[h] = 0.f; l2[h] = 0.f; continue; }
-            const int e = tab.member[g * K + j];
-            if (m < 2) {            // B_gate / B_up: integer code, scale folded into U~
-              t2[h] = code_at(v, e, k, c);
-              l2[h] = 0.f;
-            } else {                // B_down: exact value as hi + lo
-              const float val = v.at(e, k, c);
-              t2[h] = __bfloat162float(__float2bfloat16_rn(val));
-              l2[h] = val - t2[h];
-            }
-          }
-          out[q] = tc::pack_bf16(t2[0], t2[1]);
-          lo[q] = tc::pack_bf16(l2[0], l2[1]);
-        }
-        *reinterpret_cast<uint4*>(dst + jk0) = make_uint4(out[0], out[1], out[2], out[3]);
-        if (m == 2) *reinterpret_cast<uint4*>(dst + KRP + jk0) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      }
     }
+  }
+}
+
+// Transposed stacks: block (m, g, 64-column chunk) reads the KRP rank rows of the chunk
+// (coalesced), transposes through shared memory and writes 64 rows of KRP (or 2*KRP) values.
+//   m = 0, 1: Bgs/Bus[g][n][j*r + k] = code of B_m,e_j^T[k][n]
+//   m = 2:    Bdn[g][n][j*r + k] = hi, Bdn[g][n][KRP + j*r + k] = lo of B_down,e_j^T[k][n]
+__global__ void __launch_bounds__(256) resid_prep_t_kernel(PrepArgs p, GroupTable tab) {
+  constexpr int CW = 64;                   // columns per block
+  __shared__ float tile[CW][128 + 1];      // [column][jk], KRP <= 128
+  const int G = p.G, K = p.K, r = p.r, KRP = p.KRP, d = p.d, f = p.f;
+  const int nf = f / CW, nd = d / CW;
+  int blk = blockIdx.x, m;
+  if (blk < G * nf) m = 0;
+  else if ((blk -= G * nf) < G * nf) m = 1;
+  else { blk -= G * nf; m = 2; }
+  const int n = m < 2 ? f : d, nchunk = m < 2 ? nf : nd;
+  const int g = blk / nchunk, c0 = (blk % nchunk) * CW;
+  const ResidView& v = p.B[m];
+  // load: a work item is 8 consecutive columns (4 bytes of codes) of one rank row
+  for (int it = threadIdx.x; it < KRP * (CW / 8); it += blockDim.x) {
+    const int jk = it / (CW / 8), c8 = (it % (CW / 8)) * 8, j = jk / r, k = jk % r;
+    float vals[8];
+    if (j < K) {
+      const int e = tab.member[g * K + j];
+      const size_t rowi = (size_t)e * r + k;
+      const uint32_t bytes = *reinterpret_cast<const uint32_t*>((const uint8_t*)v.vals + rowi * (n / 2) + (c0 + c8) / 2);
+      const float sc = m == 2 ? __half2float(v.scales[rowi * (n / 64) + (c0 + c8) / 64]) : 1.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t b8 = (bytes >> (8 * q)) & 0xFFu;
+        vals[2 * q] = (float)((int)(b8 >> 4) - 8) * sc;
+        vals[2 * q + 1] = (float)((int)(b8 & 0xF) - 8) * sc;
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) vals[q] = 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) tile[c8 + q][jk] = vals[q];
+  }
+  __syncthreads();
+  const int width = m == 2 ? 2 * KRP : KRP;
+  __nv_bfloat16* base = m == 0 ? p.Bgs : (m == 1 ? p.Bus : p.Bdn);
+  for (int it = threadIdx.x; it < CW * (KRP / 8); it += blockDim.x) {
+    const int c = it / (KRP / 8), jk0 = (it % (KRP / 8)) * 8;
+    __nv_bfloat16* dst = base + ((size_t)g * n + c0 + c) * width + jk0;
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float a0 = tile[c][jk0 + 2 * q], a1 = tile[c][jk0 + 2 * q + 1];
+      const float h0 = __bfloat162float(__float2bfloat16_rn(a0)), h1 = __bfloat162float(__float2bfloat16_rn(a1));
+      hi[q] = tc::pack_bf16(h0, h1);
+      lo[q] = tc::pack_bf16(a0 - h0, a1 - h1);
+    }
+    *reinterpret_cast<uint4*>(dst) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    if (m == 2) *reinterpret_cast<uint4*>(dst + KRP) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
   }
 }
 
@@ -282,9 +299,17 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_kernel(
 
 // ------------------------------------------------------------------------------------------
 // 4. Fused gate/up tile: base once, per-slot residual, SwiGLU, gated sum, down-residual partials
+//
+// Warp roles (11 warps): 0 TMA producer; 1 base MMA issuer (owns TMEM); 2 residual/V MMA
+// issuer; 3..10 epilogue, two warps per TMEM lane quarter, warp group h in {0,1} handling the
+// tile's d_ff columns [32h, 32h+32) (group 0 also the U~ gate block and the V readout, group 1
+// the U~ up block).  TMEM columns: base accumulators [2][128] (gate 64 | up 64, double
+// buffered so the next tile's K-loop overlaps this tile's epilogue), R [128], V [KRP].
 // ------------------------------------------------------------------------------------------
 constexpr int kMaxKe = 4;
 constexpr int kRank = 16;      // residual rank handled by this kernel
+constexpr int kUpWarps = 11;
+constexpr int kUpEpi = 256;    // epilogue threads
 
 struct UpArgs {
   const int32_t* row_begin;
@@ -300,8 +325,14 @@ struct UpArgs {
   int G, d, f, kg, ke, R, n_ftiles, ftiles_per_chunk;
 };
 
-template <int KRP, int STAGES>
-__global__ void __launch_bounds__(192, 1) ffn_up_tc_kernel(
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+
+template <int KRP, int STAGES, int KE>
+__global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
     const __grid_constant__ CUtensorMap mX, const __grid_constant__ CUtensorMap mWg,
     const __grid_constant__ CUtensorMap mWu, const __grid_constant__ CUtensorMap mBg,
     const __grid_constant__ CUtensorMap mBu, const __grid_constant__ CUtensorMap mAd, const UpArgs p) {
@@ -309,14 +340,14 @@ __global__ void __launch_bounds__(192, 1) ffn_up_tc_kernel(
   constexpr uint32_t BRES_BYTES = KRP * kNf * 2;          // one of Bg / Bu tiles (64 rows x KRP)
   constexpr uint32_t AD_BYTES = KRP * 128;                 // KRP rows x 64 columns
   constexpr uint32_t UT_BYTES = kTile * KRP * 2;           // 128 rows x KRP
-  constexpr uint32_t H_BYTES = kTile * 128;                // 128 rows x 64 columns
   constexpr int KATOM = KRP / 64;
-  constexpr uint32_t COL_BASE = 0, COL_R = 2 * kNf, COL_V = 4 * kNf;
+  constexpr uint32_t COL_R = 4 * kNf, COL_V = 6 * kNf;
   static_assert(COL_V + KRP <= 512, "TMEM budget");
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full[STAGES], empty[STAGES];
-  __shared__ uint64_t res_full, res_empty, acc_empty, u_ready, r_full, h_ready, v_full, fin;
+  __shared__ uint64_t base_full[2], base_empty[2];
+  __shared__ uint64_t res_full, res_empty, u_ready, r_full, h_ready, v_full, fin1, fin2;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
@@ -327,6 +358,7 @@ __global__ void __launch_bounds__(192, 1) ffn_up_tc_kernel(
   if (ft0 >= ft1) return;
   const int nft = ft1 - ft0;
   const int nkb = p.d / 64;
+  const int f = p.f, fg = f / 64;
 
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sStage = smem;
@@ -341,14 +373,15 @@ __global__ void __launch_bounds__(192, 1) ffn_up_tc_kernel(
   const tc::Abort ab{&abort_flag, p.status};
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { tc::bar_init(&full[s], 1); tc::bar_init(&empty[s], 1); }
+    for (int b = 0; b < 2; ++b) { tc::bar_init(&base_full[b], 1); tc::bar_init(&base_empty[b], kUpEpi); }
     tc::bar_init(&res_full, 1);
     tc::bar_init(&res_empty, 1);
-    tc::bar_init(&acc_empty, kEpiThreads);
-    tc::bar_init(&u_ready, kEpiThreads);
+    tc::bar_init(&u_ready, kUpEpi);
     tc::bar_init(&r_full, 1);
-    tc::bar_init(&h_ready, kEpiThreads);
+    tc::bar_init(&h_ready, kUpEpi);
     tc::bar_init(&v_full, 1);
-    tc::bar_init(&fin, 1);
+    tc::bar_init(&fin1, 1);
+    tc::bar_init(&fin2, 1);
     abort_flag = 0;
     tc::bar_fence_init();
   }
@@ -357,174 +390,203 @@ __global__ void __launch_bounds__(192, 1) ffn_up_tc_kernel(
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = tmem_base;
-  const int ke = p.ke, f = p.f;
 
-  if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer: per f-tile the d/64 stages, then the residual tiles
-    tc::prefetch_map(&mX); tc::prefetch_map(&mWg); tc::prefetch_map(&mWu);
-    tc::prefetch_map(&mBg); tc::prefetch_map(&mBu); tc::prefetch_map(&mAd);
-    int kc = 0;
-    bool ok = true;
-    for (int lt = 0; lt < nft && ok; ++lt) {
-      const int n0 = (ft0 + lt) * kNf;
-      for (int kb = 0; kb < nkb; ++kb, ++kc) {
-        const int s = kc % STAGES, it = kc / STAGES;
-        if (kc >= STAGES && !tc::bar_wait(&empty[s], (it - 1) & 1, ab, 11)) { ok = false; break; }
-        uint8_t* st = sStage + s * STAGE_BYTES;
-        tc::bar_expect_tx(&full[s], STAGE_BYTES);
-        tc::tma_load_2d(st, &mX, &full[s], kb * 64, r0);
-        tc::tma_load_2d(st + X_BYTES, &mWg, &full[s], kb * 64, g * f + n0);
-        tc::tma_load_2d(st + X_BYTES + kNf * 128, &mWu, &full[s], kb * 64, g * f + n0);
-      }
-      if (!ok) break;
-      if (lt > 0 && !tc::bar_wait(&res_empty, (lt - 1) & 1, ab, 12)) break;
-      tc::bar_expect_tx(&res_full, 2 * BRES_BYTES + AD_BYTES);
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer: per f-tile the d/64 stages, then the residual tiles
+      tc::prefetch_map(&mX); tc::prefetch_map(&mWg); tc::prefetch_map(&mWu);
+      tc::prefetch_map(&mBg); tc::prefetch_map(&mBu); tc::prefetch_map(&mAd);
+      int kc = 0;
+      bool ok = true;
+      for (int lt = 0; lt < nft && ok; ++lt) {
+        const int n0 = (ft0 + lt) * kNf;
+        for (int kb = 0; kb < nkb; ++kb, ++kc) {
+          const int s = kc % STAGES, it = kc / STAGES;
+          if (kc >= STAGES && !tc::bar_wait(&empty[s], (it - 1) & 1, ab, 11)) { ok = false; break; }
+          uint8_t* st = sStage + s * STAGE_BYTES;
+          tc::bar_expect_tx(&full[s], STAGE_BYTES);
+          tc::tma_load_2d(st, &mX, &full[s], kb * 64, r0);
+          tc::tma_load_2d(st + X_BYTES, &mWg, &full[s], kb * 64, g * f + n0);
+          tc::tma_load_2d(st + X_BYTES + kNf * 128, &mWu, &full[s], kb * 64, g * f + n0);
+        }
+        if (!ok) break;
+        if (lt > 0 && !tc::bar_wait(&res_empty, (lt - 1) & 1, ab, 12)) break;
+        tc::bar_expect_tx(&res_full, 2 * BRES_BYTES + AD_BYTES);
 #pragma unroll
-      for (int a = 0; a < KATOM; ++a) {
-        tc::tma_load_2d(sBg + a * kNf * 128, &mBg, &res_full, a * 64, g * f + n0);
-        tc::tma_load_2d(sBu + a * kNf * 128, &mBu, &res_full, a * 64, g * f + n0);
+        for (int a = 0; a < KATOM; ++a) {
+          tc::tma_load_2d(sBg + a * kNf * 128, &mBg, &res_full, a * 64, g * f + n0);
+          tc::tma_load_2d(sBu + a * kNf * 128, &mBu, &res_full, a * 64, g * f + n0);
+        }
+        tc::tma_load_2d(sAd, &mAd, &res_full, n0, g * KRP);
       }
-      tc::tma_load_2d(sAd, &mAd, &res_full, n0, g * KRP);
+      if (abort_flag) tc::drain_copies();
     }
-    if (abort_flag) tc::drain_copies();
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer
-    constexpr uint32_t id_base = tc::idesc_bf16(kTile, 2 * kNf);
-    constexpr uint32_t id_res = tc::idesc_bf16(kTile, kNf);
-    constexpr uint32_t id_v = tc::idesc_bf16(kTile, KRP);
-    int kc = 0, pu = 0, ph = 0;
-    bool ok = true;
-    for (int lt = 0; lt < nft && ok; ++lt) {
-      if (lt > 0 && !tc::bar_wait(&acc_empty, (lt - 1) & 1, ab, 21)) break;
-      tc::fence_after();
-      for (int kb = 0; kb < nkb; ++kb, ++kc) {
-        const int s = kc % STAGES, it = kc / STAGES;
-        if (!tc::bar_wait(&full[s], it & 1, ab, 22)) { ok = false; break; }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- base MMA issuer: [Hg | Hu] = X [Wg | Wu]^T into base[lt & 1]
+      constexpr uint32_t id_base = tc::idesc_bf16(kTile, 2 * kNf);
+      int kc = 0;
+      bool ok = true;
+      for (int lt = 0; lt < nft && ok; ++lt) {
+        const int b = lt & 1;
+        if (lt >= 2 && !tc::bar_wait(&base_empty[b], ((lt >> 1) - 1) & 1, ab, 21)) break;
         tc::fence_after();
-        const uint32_t a0 = tc::smem_u32(sStage + s * STAGE_BYTES);
-        const uint32_t b0 = a0 + X_BYTES;
+        const uint32_t dcol = tmem + b * 2 * kNf;
+        for (int kb = 0; kb < nkb; ++kb, ++kc) {
+          const int s = kc % STAGES, it = kc / STAGES;
+          if (!tc::bar_wait(&full[s], it & 1, ab, 22)) { ok = false; break; }
+          tc::fence_after();
+          const uint32_t a0 = tc::smem_u32(sStage + s * STAGE_BYTES);
+          const uint32_t b0 = a0 + X_BYTES;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          tc::mma_bf16(tmem + COL_BASE, tc::sdesc(a0 + 32 * k), tc::sdesc(b0 + 32 * k), id_base, (kb | k) != 0);
-        tc::mma_commit(&empty[s]);
+          for (int k = 0; k < 4; ++k)
+            tc::mma_bf16(dcol, tc::sdesc(a0 + 32 * k), tc::sdesc(b0 + 32 * k), id_base, (kb | k) != 0);
+          tc::mma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        tc::mma_commit(&base_full[b]);
       }
-      if (!ok) break;
-      if (!tc::bar_wait(&res_full, lt & 1, ab, 23)) break;
-      tc::fence_after();
+      tc::mma_commit(&fin1);
+      const uint64_t t0 = tc::now_ns();
+      while (!tc::bar_test(&fin1, 0) && tc::now_ns() - t0 < tc::kWaitNs) {}
+    }
+  } else if (warp == 2) {
+    if (lane == 0) {
+      // ---------------- residual issuer: R = U~_s [Bg | Bu]^T, V = H_s Adn^T per slot
+      constexpr uint32_t id_res = tc::idesc_bf16(kTile, kNf);
+      constexpr uint32_t id_v = tc::idesc_bf16(kTile, KRP);
       const uint32_t ug = tc::smem_u32(sUg), uu = tc::smem_u32(sUu);
       const uint32_t bg = tc::smem_u32(sBg), bu = tc::smem_u32(sBu);
       const uint32_t hh = tc::smem_u32(sH), ad = tc::smem_u32(sAd);
-      for (int s = 0; s < ke && ok; ++s) {
-        if (!tc::bar_wait(&u_ready, pu & 1, ab, 24)) { ok = false; break; }
-        ++pu;
+      int pu = 0, ph = 0;
+      bool ok = true;
+      for (int lt = 0; lt < nft && ok; ++lt) {
+        if (!tc::bar_wait(&res_full, lt & 1, ab, 23)) break;
         tc::fence_after();
+        for (int s = 0; s < KE; ++s) {
+          if (!tc::bar_wait(&u_ready, pu & 1, ab, 24)) { ok = false; break; }
+          ++pu;
+          tc::fence_after();
 #pragma unroll
-        for (int kk = 0; kk < KRP / 16; ++kk) {
-          const uint32_t off_u = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          const uint32_t off_b = (kk >> 2) * (kNf * 128) + (kk & 3) * 32;
-          tc::mma_bf16(tmem + COL_R, tc::sdesc(ug + off_u), tc::sdesc(bg + off_b), id_res, kk != 0);
-          tc::mma_bf16(tmem + COL_R + kNf, tc::sdesc(uu + off_u), tc::sdesc(bu + off_b), id_res, kk != 0);
+          for (int kk = 0; kk < KRP / 16; ++kk) {
+            const uint32_t off_u = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+            const uint32_t off_b = (kk >> 2) * (kNf * 128) + (kk & 3) * 32;
+            tc::mma_bf16(tmem + COL_R, tc::sdesc(ug + off_u), tc::sdesc(bg + off_b), id_res, kk != 0);
+            tc::mma_bf16(tmem + COL_R + kNf, tc::sdesc(uu + off_u), tc::sdesc(bu + off_b), id_res, kk != 0);
+          }
+          tc::mma_commit(&r_full);
+          if (!tc::bar_wait(&h_ready, ph & 1, ab, 25)) { ok = false; break; }
+          ++ph;
+          tc::fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc::mma_bf16(tmem + COL_V, tc::sdesc(hh + 32 * kk), tc::sdesc(ad + 32 * kk), id_v, kk != 0);
+          tc::mma_commit(&v_full);
         }
-        tc::mma_commit(&r_full);
-        if (!tc::bar_wait(&h_ready, ph & 1, ab, 25)) { ok = false; break; }
-        ++ph;
-        tc::fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc::mma_bf16(tmem + COL_V, tc::sdesc(hh + 32 * kk), tc::sdesc(ad + 32 * kk), id_v, kk != 0);
-        tc::mma_commit(&v_full);
+        if (!ok) break;
+        tc::mma_commit(&res_empty);
       }
-      tc::mma_commit(&res_empty);
+      tc::mma_commit(&fin2);
+      const uint64_t t0 = tc::now_ns();
+      while (!tc::bar_test(&fin2, 0) && tc::now_ns() - t0 < tc::kWaitNs) {}
     }
-    tc::mma_commit(&fin);
-    const uint64_t t0 = tc::now_ns();
-    while (!tc::bar_test(&fin, 0) && tc::now_ns() - t0 < tc::kWaitNs) {}
-  } else if (warp >= 2) {
-    // ---------------- epilogue: one thread per tile row
-    const int q = warp & 3, row = q * 32 + lane, i = r0 + row;
+  } else {
+    // ---------------- epilogue: one thread per (tile row, column half)
+    const int q = warp & 3, half = (warp - 3) >> 2, row = q * 32 + lane, i = r0 + row;
     const bool valid = i < r1;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    int le[kMaxKe];
-    float gt[kMaxKe];
-    const float* urow = nullptr;
-    int eid[kMaxKe];
-    for (int s = 0; s < kMaxKe; ++s) eid[s] = 0;
-    for (int s = 0; s < kMaxKe; ++s) { le[s] = 0; gt[s] = 0.f; }
+    const int c_half = half * 32;                    // this group's first column of the tile
+    uint8_t* sU = half == 0 ? sUg : sUu;             // U~ block this group writes
+    const __half* sB = half == 0 ? p.sBg : p.sBu;
+    int le[KE], eid[KE];
+    float gt[KE];
+#pragma unroll
+    for (int s = 0; s < KE; ++s) { le[s] = 0; eid[s] = 0; gt[s] = 0.f; }
+    const float* urow = p.U;
     if (valid) {
-      const int b = p.row_asg[i], t = b / p.kg, j = b % p.kg, k = p.kg * ke;
-      for (int s = 0; s < ke; ++s) {
-        const int e = p.eidx[(size_t)t * k + j * ke + s];
+      const int b = p.row_asg[i], t = b / p.kg, j = b % p.kg, k = p.kg * KE;
+#pragma unroll
+      for (int s = 0; s < KE; ++s) {
+        const int e = p.eidx[(size_t)t * k + j * KE + s];
         le[s] = p.tab.local_of[e];
         eid[s] = e;
-        gt[s] = p.gate[(size_t)t * k + j * ke + s];
+        gt[s] = p.gate[(size_t)t * k + j * KE + s];
       }
-      urow = p.U + (size_t)i * 2 * KRP;
+      urow = p.U + (size_t)i * 2 * KRP + half * KRP;
     }
-    // zero this row of U~gate / U~up
-    for (int a = 0; a < KATOM; ++a) {
-      uint4* zg = reinterpret_cast<uint4*>(sUg + a * kTile * 128 + (row >> 3) * 1024 + (row & 7) * 128);
-      uint4* zu = reinterpret_cast<uint4*>(sUu + a * kTile * 128 + (row >> 3) * 1024 + (row & 7) * 128);
+    {   // zero this row of this group's U~ matrix
+      for (int a = 0; a < KATOM; ++a) {
+        uint4* z = reinterpret_cast<uint4*>(sU + a * kTile * 128 + (row >> 3) * 1024 + (row & 7) * 128);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) { zg[c] = make_uint4(0, 0, 0, 0); zu[c] = make_uint4(0, 0, 0, 0); }
+        for (int c = 0; c < 8; ++c) z[c] = make_uint4(0, 0, 0, 0);
+      }
     }
-    float vacc[kMaxKe][kRank];
+    float vacc[KE][kRank];
 #pragma unroll
-    for (int s = 0; s < kMaxKe; ++s)
+    for (int s = 0; s < KE; ++s)
 #pragma unroll
       for (int k = 0; k < kRank; ++k) vacc[s][k] = 0.f;
+
+    // U~ block values of (tile lt, slot s) for this row: bf16(U * scale), loaded one step ahead
+    auto load_u = [&](int lt, int s, uint32_t (&pk)[8]) {
+      if (!valid) return;
+      const int ng = (ft0 + lt) * kNf / 64;
+      const float* u = urow + le[s] * kRank;
+      const __half* sc = sB + (size_t)eid[s] * kRank * fg + ng;
+#pragma unroll
+      for (int k = 0; k < kRank; k += 2)
+        pk[k / 2] = tc::pack_bf16(u[k] * __half2float(sc[(size_t)k * fg]), u[k + 1] * __half2float(sc[(size_t)(k + 1) * fg]));
+    };
+    uint32_t unext[8];
+    load_u(0, 0, unext);
     int pr = 0, pv = 0, cur = -1;
     bool ok = true;
     for (int lt = 0; lt < nft && ok; ++lt) {
       const int n0 = (ft0 + lt) * kNf;
-      float hs[kNf];
+      const int bsel = lt & 1;
+      const uint32_t base_col = bsel * 2 * kNf;
+      float hs[32];
 #pragma unroll
-      for (int c = 0; c < kNf; ++c) hs[c] = 0.f;
-      for (int s = 0; s < ke; ++s) {
-        // U~ for slot s: this row's block le[s] holds A^T x of expert e_s times the B scales of
-        // this 64-column tile (one scale group), every other block 0
+      for (int c = 0; c < 32; ++c) hs[c] = 0.f;
+      bool waited_base = false;
+#pragma unroll
+      for (int s = 0; s < KE; ++s) {
+        // U~ block for slot s (this group's matrix), previous block cleared
         if (valid) {
-          const uint4 zero = make_uint4(0, 0, 0, 0);
           if (cur >= 0 && cur != le[s]) {
-            *reinterpret_cast<uint4*>(sUg + tc::sw128_offset(row, cur * kRank, kTile)) = zero;
-            *reinterpret_cast<uint4*>(sUg + tc::sw128_offset(row, cur * kRank + 8, kTile)) = zero;
-            *reinterpret_cast<uint4*>(sUu + tc::sw128_offset(row, cur * kRank, kTile)) = zero;
-            *reinterpret_cast<uint4*>(sUu + tc::sw128_offset(row, cur * kRank + 8, kTile)) = zero;
+            const uint4 zero = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, cur * kRank, kTile)) = zero;
+            *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, cur * kRank + 8, kTile)) = zero;
           }
-          const float* ug = urow + le[s] * kRank;
-          const float* uu = urow + KRP + le[s] * kRank;
-          const size_t sc0 = (size_t)eid[s] * kRank * (f / 64) + n0 / 64;
-          uint32_t pg[8], pu_[8];
-#pragma unroll
-          for (int k2 = 0; k2 < kRank; k2 += 2) {
-            const float g0 = ug[k2] * __half2float(p.sBg[sc0 + (size_t)k2 * (f / 64)]);
-            const float g1 = ug[k2 + 1] * __half2float(p.sBg[sc0 + (size_t)(k2 + 1) * (f / 64)]);
-            const float u0 = uu[k2] * __half2float(p.sBu[sc0 + (size_t)k2 * (f / 64)]);
-            const float u1 = uu[k2 + 1] * __half2float(p.sBu[sc0 + (size_t)(k2 + 1) * (f / 64)]);
-            pg[k2 / 2] = tc::pack_bf16(g0, g1);
-            pu_[k2 / 2] = tc::pack_bf16(u0, u1);
-          }
-          *reinterpret_cast<uint4*>(sUg + tc::sw128_offset(row, le[s] * kRank, kTile)) = make_uint4(pg[0], pg[1], pg[2], pg[3]);
-          *reinterpret_cast<uint4*>(sUg + tc::sw128_offset(row, le[s] * kRank + 8, kTile)) = make_uint4(pg[4], pg[5], pg[6], pg[7]);
-          *reinterpret_cast<uint4*>(sUu + tc::sw128_offset(row, le[s] * kRank, kTile)) = make_uint4(pu_[0], pu_[1], pu_[2], pu_[3]);
-          *reinterpret_cast<uint4*>(sUu + tc::sw128_offset(row, le[s] * kRank + 8, kTile)) = make_uint4(pu_[4], pu_[5], pu_[6], pu_[7]);
+          *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, le[s] * kRank, kTile)) =
+              make_uint4(unext[0], unext[1], unext[2], unext[3]);
+          *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, le[s] * kRank + 8, kTile)) =
+              make_uint4(unext[4], unext[5], unext[6], unext[7]);
           cur = le[s];
         }
         tc::fence_async_smem();
         tc::bar_arrive(&u_ready);
+        // prefetch the next slot's U~ values while the residual MMA runs
+        if (s + 1 < KE) load_u(lt, s + 1, unext);
+        else if (lt + 1 < nft) load_u(lt + 1, 0, unext);
+        if (!waited_base) {
+          if (!tc::bar_wait(&base_full[bsel], (lt >> 1) & 1, ab, 30)) { ok = false; break; }
+          waited_base = true;
+        }
         if (!tc::bar_wait(&r_full, pr & 1, ab, 31)) { ok = false; break; }
         ++pr;
         tc::fence_after();
 #pragma unroll
-        for (int c = 0; c < kNf; c += 16) {
-          uint32_t bgv[16], buv[16], rgv[16], ruv[16];
-          tc::tmem_ld16(tmem + lane_off + COL_BASE + c, bgv);
-          tc::tmem_ld16(tmem + lane_off + COL_BASE + kNf + c, buv);
-          tc::tmem_ld16(tmem + lane_off + COL_R + c, rgv);
-          tc::tmem_ld16(tmem + lane_off + COL_R + kNf + c, ruv);
+        for (int c = 0; c < 32; c += 8) {
+          uint32_t bgv[8], buv[8], rgv[8], ruv[8];
+          tmem_ld8(tmem + lane_off + base_col + c_half + c, bgv);
+          tmem_ld8(tmem + lane_off + base_col + kNf + c_half + c, buv);
+          tmem_ld8(tmem + lane_off + COL_R + c_half + c, rgv);
+          tmem_ld8(tmem + lane_off + COL_R + kNf + c_half + c, ruv);
           tc::tmem_ld_wait();
-          uint32_t pk[8];
+          uint32_t pk[4];
 #pragma unroll
-          for (int e = 0; e < 16; e += 2) {
+          for (int e = 0; e < 8; e += 2) {
             float h2[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
@@ -535,50 +597,56 @@ __global__ void __launch_bounds__(192, 1) ffn_up_tc_kernel(
             }
             pk[e / 2] = tc::pack_bf16(h2[0], h2[1]);
           }
-          *reinterpret_cast<uint4*>(sH + tc::sw128_offset(row, c, kTile)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4*>(sH + tc::sw128_offset(row, c + 8, kTile)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          *reinterpret_cast<uint4*>(sH + tc::sw128_offset(row, c_half + c, kTile)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
         tc::fence_before();
         tc::fence_async_smem();
         tc::bar_arrive(&h_ready);
+        __half2 sc_ad[kRank / 2];
+        if (half == 0 && valid) {
+          const __half* sc = p.sAd + (size_t)eid[s] * kRank * fg + n0 / 64;
+#pragma unroll
+          for (int k = 0; k < kRank; k += 2) sc_ad[k / 2] = __halves2half2(sc[(size_t)k * fg], sc[(size_t)(k + 1) * fg]);
+        }
         if (!tc::bar_wait(&v_full, pv & 1, ab, 32)) { ok = false; break; }
         ++pv;
         tc::fence_after();
+        if (half == 0) {
 #pragma unroll
-        for (int jb = 0; jb < KRP / 16; ++jb) {
-          uint32_t vv[16];
-          tc::tmem_ld16(tmem + lane_off + COL_V + jb * 16, vv);
-          tc::tmem_ld_wait();
-          if (jb == le[s] && valid) {
-            const size_t sc0 = (size_t)eid[s] * kRank * (f / 64) + n0 / 64;
+          for (int jb = 0; jb < KRP / 16; ++jb) {
+            uint32_t vv[16];
+            tc::tmem_ld16(tmem + lane_off + COL_V + jb * 16, vv);
+            tc::tmem_ld_wait();
+            if (jb == le[s] && valid) {
 #pragma unroll
-            for (int k = 0; k < kRank; ++k) {
-              const float val = __uint_as_float(vv[k]) * __half2float(p.sAd[sc0 + (size_t)k * (f / 64)]);
-#pragma unroll
-              for (int s2 = 0; s2 < kMaxKe; ++s2)
-                if (s2 == s) vacc[s2][k] += val;
+              for (int k = 0; k < kRank; k += 2) {
+                const float2 sf = __half22float2(sc_ad[k / 2]);
+                vacc[s][k] += __uint_as_float(vv[k]) * sf.x;
+                vacc[s][k + 1] += __uint_as_float(vv[k + 1]) * sf.y;
+              }
             }
           }
         }
       }
       if (!ok) break;
       if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(p.hsum + (size_t)i * f + n0);
+        uint4* dst = reinterpret_cast<uint4*>(p.hsum + (size_t)i * f + n0 + c_half);
 #pragma unroll
-        for (int c = 0; c < kNf; c += 8)
+        for (int c = 0; c < 32; c += 8)
           dst[c / 8] = make_uint4(tc::pack_bf16(hs[c], hs[c + 1]), tc::pack_bf16(hs[c + 2], hs[c + 3]),
                                   tc::pack_bf16(hs[c + 4], hs[c + 5]), tc::pack_bf16(hs[c + 6], hs[c + 7]));
       }
       tc::fence_before();
-      tc::bar_arrive(&acc_empty);
+      tc::bar_arrive(&base_empty[bsel]);
     }
-    if (ok && valid) {
-      float* vp = p.Vpart + ((size_t)blockIdx.x * p.R + i) * ke * kRank;
+    if (ok && valid && half == 0) {
+      float* vp = p.Vpart + ((size_t)blockIdx.x * p.R + i) * KE * kRank;
 #pragma unroll
-      for (int s = 0; s < kMaxKe; ++s)
-        if (s < ke)
+      for (int s = 0; s < KE; ++s)
 #pragma unroll
-          for (int k = 0; k < kRank; ++k) vp[s * kRank + k] = gt[s] * vacc[s][k];
+        for (int k = 0; k < kRank; k += 4)
+          *reinterpret_cast<float4*>(vp + s * kRank + k) =
+              make_float4(gt[s] * vacc[s][k], gt[s] * vacc[s][k + 1], gt[s] * vacc[s][k + 2], gt[s] * vacc[s][k + 3]);
     }
   }
   tc::fence_before();
@@ -595,19 +663,33 @@ __global__ void __launch_bounds__(192, 1) ffn_up_tc_kernel(
 __global__ void v_reduce_kernel(const float* __restrict__ Vpart, const int32_t* __restrict__ row_asg,
                                 const int32_t* __restrict__ eidx, GroupTable tab, int R, int kg, int ke,
                                 int nchunks, int KRP, __nv_bfloat16* __restrict__ Vt) {
-  const size_t n = (size_t)R * KRP;
-  for (size_t w = blockIdx.x * (size_t)blockDim.x + threadIdx.x; w < n; w += (size_t)gridDim.x * blockDim.x) {
-    const int i = (int)(w / KRP), col = (int)(w % KRP), jl = col / kRank, k = col % kRank;
-    const int b = row_asg[i], t = b / kg, j = b % kg;
-    float acc = 0.f;
-    for (int s = 0; s < ke; ++s) {
-      const int e = eidx[(size_t)t * kg * ke + j * ke + s];
-      if (tab.local_of[e] != jl) continue;
-      for (int c = 0; c < nchunks; ++c) acc += Vpart[(((size_t)c * R + i) * ke + s) * kRank + k];
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= R) return;
+  uint4* row = reinterpret_cast<uint4*>(Vt + (size_t)i * 2 * KRP);
+  for (int c = 0; c < 2 * KRP / 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
+  const int b = row_asg[i], t = b / kg, j = b % kg;
+  for (int s = 0; s < ke; ++s) {
+    const int jl = tab.local_of[eidx[(size_t)t * kg * ke + j * ke + s]];
+    float acc[kRank];
+#pragma unroll
+    for (int k = 0; k < kRank; ++k) acc[k] = 0.f;
+    for (int c = 0; c < nchunks; ++c) {
+      const float4* src = reinterpret_cast<const float4*>(Vpart + (((size_t)c * R + i) * ke + s) * kRank);
+#pragma unroll
+      for (int q = 0; q < kRank / 4; ++q) {
+        const float4 v4 = src[q];
+        acc[4 * q] += v4.x; acc[4 * q + 1] += v4.y; acc[4 * q + 2] += v4.z; acc[4 * q + 3] += v4.w;
+      }
     }
-    const __nv_bfloat16 v = __float2bfloat16_rn(acc);
-    Vt[(size_t)i * 2 * KRP + col] = v;          // multiplies the hi half of Bdn
-    Vt[(size_t)i * 2 * KRP + KRP + col] = v;    // and the lo half
+    uint32_t pk[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) pk[k] = tc::pack_bf16(acc[2 * k], acc[2 * k + 1]);
+    const uint4 lo4 = make_uint4(pk[0], pk[1], pk[2], pk[3]), hi4 = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+    // the same block multiplies the hi half and the lo half of Bdn
+    row[(jl * kRank) / 8] = lo4;
+    row[(jl * kRank) / 8 + 1] = hi4;
+    row[(KRP + jl * kRank) / 8] = lo4;
+    row[(KRP + jl * kRank) / 8 + 1] = hi4;
   }
 }
 
@@ -681,20 +763,31 @@ static cudaError_t launch_gemm(const CUtensorMap& A0, const CUtensorMap& A1, con
   return cudaGetLastError();
 }
 
-template <int KRP>
-static cudaError_t launch_up(const CUtensorMap* maps, const UpArgs& p, int nchunks, int tiles, cudaStream_t stream) {
+template <int KRP, int KE>
+static cudaError_t launch_up_ke(const CUtensorMap* maps, const UpArgs& p, int nchunks, int tiles, cudaStream_t stream) {
   constexpr int STAGES = KRP >= 128 ? 3 : 4;
   const size_t smem = 1024 + (size_t)STAGES * (kTile * 128 + 2 * kNf * 128) + 2 * (KRP * kNf * 2) + KRP * 128 +
                       2 * (kTile * KRP * 2) + kTile * 128;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = set_smem(ffn_up_tc_kernel<KRP, STAGES>, smem);
+    cudaError_t e = set_smem(ffn_up_tc_kernel<KRP, STAGES, KE>, smem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   dim3 grid(nchunks, tiles);
-  ffn_up_tc_kernel<KRP, STAGES><<<grid, 192, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+  ffn_up_tc_kernel<KRP, STAGES, KE><<<grid, kUpWarps * 32, smem, stream>>>(maps[0], maps[1], maps[2], maps[3],
+                                                                          maps[4], maps[5], p);
   return cudaGetLastError();
+}
+
+template <int KRP>
+static cudaError_t launch_up(const CUtensorMap* maps, const UpArgs& p, int nchunks, int tiles, cudaStream_t stream) {
+  switch (p.ke) {
+    case 1: return launch_up_ke<KRP, 1>(maps, p, nchunks, tiles, stream);
+    case 2: return launch_up_ke<KRP, 2>(maps, p, nchunks, tiles, stream);
+    case 3: return launch_up_ke<KRP, 3>(maps, p, nchunks, tiles, stream);
+    default: return launch_up_ke<KRP, 4>(maps, p, nchunks, tiles, stream);
+  }
 }
 
 cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, const void* wu, const void* wd,
@@ -711,7 +804,8 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   for (int m = 0; m < 3; ++m) { pa.A[m] = rp.A[m]; pa.B[m] = rp.B[m]; }
   pa.Ain = b.Ain; pa.Bgs = b.Bgs; pa.Bus = b.Bus; pa.Adn = b.Adn; pa.Bdn = b.Bdn;
   pa.G = G; pa.K = a.K; pa.d = d; pa.f = f; pa.r = a.r; pa.KRP = KRP;
-  resid_prep_kernel<<<148 * 8, 256, 0, st>>>(pa, a.tab);
+  resid_prep_rows_kernel<<<148 * 4, 256, 0, st>>>(pa, a.tab);
+  resid_prep_t_kernel<<<G * (2 * (f / 64) + d / 64), 256, 0, st>>>(pa, a.tab);
   prof_mark("resid_prep", st);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
@@ -757,7 +851,7 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   if (e != cudaSuccess) return e;
 
   // 5. V~
-  v_reduce_kernel<<<148 * 4, 256, 0, st>>>(b.Vpart, row_asg, eidx, a.tab, R, a.kg, a.ke, nchunks, KRP, b.Vt);
+  v_reduce_kernel<<<(R + 127) / 128, 128, 0, st>>>(b.Vpart, row_asg, eidx, a.tab, R, a.kg, a.ke, nchunks, KRP, b.Vt);
   prof_mark("v_reduce", st);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 

@@ -9,24 +9,109 @@
 
 namespace moe {
 
-// Logits of TPW tokens x RB router rows per warp; 8 warps share the rows of one CTA.
-// Row index rr in [0, G) is group row rr (plus b_group[rr]); rr in [G, G+E) is expert row rr-G.
-// Canonical order: lane l owns elements 128*j + 4*l + u (u = 0..3), adds them in ascending
-// index with one rounding per product and per add, then an xor butterfly 16, 8, 4, 2, 1.
-template <typename T, int TPW, int RB>
-__global__ void __launch_bounds__(256) router_logits_kernel(
-    const T* __restrict__ x, const T* __restrict__ wg, const float* __restrict__ bg,
-    const T* __restrict__ we, float* __restrict__ logits, int Tn, int d, int G, int E) {
+// Two independent IEEE round-to-nearest FMAs in one instruction: (a.x*b.x + c.x, a.y*b.y + c.y).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  unsigned long long ra = *reinterpret_cast<unsigned long long*>(&a);
+  unsigned long long rb = *reinterpret_cast<unsigned long long*>(&b);
+  unsigned long long rc = *reinterpret_cast<unsigned long long*>(&c);
+  unsigned long long rd;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+  return *reinterpret_cast<float2*>(&rd);
+}
+
+// BF16 router logits.  Warp (tg, rg) of the CTA owns TPW tokens x RPW router rows; the CTA is
+// WT x WR warps.  Canonical order: lane l owns elements 128*j + 4*l + u (u = 0..3) and adds them
+// in ascending index, one rounding per product (exact: BF16 x BF16 fits FP32) and per add; then
+// an xor butterfly 16, 8, 4, 2, 1.  Row rr < G is group row rr (+ b_group[rr]), else expert rr-G.
+template <int TPW, int RPW, int WT, int WR>
+__global__ void __launch_bounds__(WT * WR * 32) router_logits_bf16_kernel(
+    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ wg, const float* __restrict__ bg,
+    const __nv_bfloat16* __restrict__ we, float* __restrict__ logits, int Tn, int d, int G, int E) {
+  static_assert(TPW % 2 == 0, "token pairs feed the paired FMA");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int tg = warp % WT, rg = warp / WT;
+  const int R = G + E;
+  const int t0 = (blockIdx.x * WT + tg) * TPW;
+  const int r0 = (blockIdx.y * WR + rg) * RPW;
+  if (t0 >= Tn || r0 >= R) return;
+  const uint2* xp[TPW];
+#pragma unroll
+  for (int i = 0; i < TPW; ++i) xp[i] = reinterpret_cast<const uint2*>(x + (size_t)min(t0 + i, Tn - 1) * d) + lane;
+  const uint2* wp[RPW];
+#pragma unroll
+  for (int q = 0; q < RPW; ++q) {
+    const int rr = min(r0 + q, R - 1);
+    wp[q] = reinterpret_cast<const uint2*>(rr < G ? wg + (size_t)rr * d : we + (size_t)(rr - G) * d) + lane;
+  }
+  float2 acc[TPW / 2][RPW];
+#pragma unroll
+  for (int i = 0; i < TPW / 2; ++i)
+#pragma unroll
+    for (int q = 0; q < RPW; ++q) acc[i][q] = make_float2(0.f, 0.f);
+  const int nb = d / 128;
+#pragma unroll 2
+  for (int jb = 0; jb < nb; ++jb) {
+    uint2 xr[TPW], wr[RPW];
+#pragma unroll
+    for (int i = 0; i < TPW; ++i) xr[i] = __ldg(xp[i] + jb * 32);
+#pragma unroll
+    for (int q = 0; q < RPW; ++q) wr[q] = __ldg(wp[q] + jb * 32);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      // element u of this lane's 4-element chunk
+      float2 xv[TPW / 2];
+#pragma unroll
+      for (int i = 0; i < TPW / 2; ++i) {
+        const uint32_t a = u < 2 ? xr[2 * i].x : xr[2 * i].y, b = u < 2 ? xr[2 * i + 1].x : xr[2 * i + 1].y;
+        xv[i] = (u & 1) ? make_float2(__uint_as_float(a & 0xFFFF0000u), __uint_as_float(b & 0xFFFF0000u))
+                        : make_float2(__uint_as_float(a << 16), __uint_as_float(b << 16));
+      }
+#pragma unroll
+      for (int q = 0; q < RPW; ++q) {
+        const uint32_t w = u < 2 ? wr[q].x : wr[q].y;
+        const float wf = (u & 1) ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
+        const float2 w2 = make_float2(wf, wf);
+#pragma unroll
+        for (int i = 0; i < TPW / 2; ++i) acc[i][q] = fma2(xv[i], w2, acc[i][q]);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < TPW / 2; ++i)
+#pragma unroll
+    for (int q = 0; q < RPW; ++q)
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        acc[i][q].x = __fadd_rn(acc[i][q].x, __shfl_xor_sync(0xffffffffu, acc[i][q].x, o));
+        acc[i][q].y = __fadd_rn(acc[i][q].y, __shfl_xor_sync(0xffffffffu, acc[i][q].y, o));
+      }
+#pragma unroll
+  for (int i = 0; i < TPW; ++i)
+#pragma unroll
+    for (int q = 0; q < RPW; ++q) {
+      const int t = t0 + i, rr = r0 + q;
+      if (((i * RPW + q) & 31) == lane && t < Tn && rr < R) {
+        float v = (i & 1) ? acc[i / 2][q].y : acc[i / 2][q].x;
+        if (rr < G && bg != nullptr) v = __fadd_rn(v, bg[rr]);
+        logits[(size_t)t * R + rr] = v;
+      }
+    }
+}
+
+// FP32 router logits (same canonical order; products rounded before the add, no contraction).
+template <int TPW, int RB>
+__global__ void __launch_bounds__(256) router_logits_f32_kernel(
+    const float* __restrict__ x, const float* __restrict__ wg, const float* __restrict__ bg,
+    const float* __restrict__ we, float* __restrict__ logits, int Tn, int d, int G, int E) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int R = G + E;
   const int t0 = (blockIdx.x * 8 + warp) * TPW;
   const int r0 = blockIdx.y * RB;
   if (t0 >= Tn) return;
-
-  const T* xp[TPW];
+  const float* xp[TPW];
 #pragma unroll
   for (int i = 0; i < TPW; ++i) xp[i] = x + (size_t)min(t0 + i, Tn - 1) * d;
-  const T* wp[RB];
+  const float* wp[RB];
 #pragma unroll
   for (int q = 0; q < RB; ++q) {
     const int rr = min(r0 + q, R - 1);
@@ -37,40 +122,29 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
   for (int i = 0; i < TPW; ++i)
 #pragma unroll
     for (int q = 0; q < RB; ++q) acc[i][q] = 0.f;
-
   for (int base = 4 * lane; base < d; base += 128) {
-    float xv[TPW][4];
+    float4 xv[TPW];
 #pragma unroll
-    for (int i = 0; i < TPW; ++i)
-#pragma unroll
-      for (int u = 0; u < 4; ++u) xv[i][u] = to_f32(xp[i][base + u]);
+    for (int i = 0; i < TPW; ++i) xv[i] = *reinterpret_cast<const float4*>(xp[i] + base);
 #pragma unroll
     for (int q = 0; q < RB; ++q) {
-      float wv[4];
+      const float4 wv = *reinterpret_cast<const float4*>(wp[q] + base);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) wv[u] = to_f32(wp[q][base + u]);
-#pragma unroll
-      for (int i = 0; i < TPW; ++i)
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if constexpr (sizeof(T) == 2) {
-            // BF16 x BF16 is exact in FP32, so the fused form equals fl(s + fl(x*w)).
-            acc[i][q] = __fmaf_rn(xv[i][u], wv[u], acc[i][q]);
-          } else {
-            acc[i][q] = __fadd_rn(acc[i][q], __fmul_rn(xv[i][u], wv[u]));
-          }
-        }
+      for (int i = 0; i < TPW; ++i) {
+        acc[i][q] = __fadd_rn(acc[i][q], __fmul_rn(xv[i].x, wv.x));
+        acc[i][q] = __fadd_rn(acc[i][q], __fmul_rn(xv[i].y, wv.y));
+        acc[i][q] = __fadd_rn(acc[i][q], __fmul_rn(xv[i].z, wv.z));
+        acc[i][q] = __fadd_rn(acc[i][q], __fmul_rn(xv[i].w, wv.w));
+      }
     }
   }
 #pragma unroll
   for (int i = 0; i < TPW; ++i)
 #pragma unroll
-    for (int q = 0; q < RB; ++q) {
+    for (int q = 0; q < RB; ++q)
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1)
         acc[i][q] = __fadd_rn(acc[i][q], __shfl_xor_sync(0xffffffffu, acc[i][q], o));
-    }
-  // every lane holds every sum; lane (i*RB+q) % 32 writes it
 #pragma unroll
   for (int i = 0; i < TPW; ++i)
 #pragma unroll
@@ -141,14 +215,26 @@ __global__ void router_select_kernel(const float* __restrict__ logits, GroupTabl
   }
 }
 
-template <typename T>
-static cudaError_t launch_logits(const void* x, const void* wg, const float* bg, const void* we,
-                                 float* logits, int Tn, int d, int G, int E, cudaStream_t st) {
-  constexpr int TPW = 4, RB = 8;
+template <int TPW, int RPW, int WT, int WR>
+static void launch_bf16_logits(const void* x, const void* wg, const float* bg, const void* we, float* logits,
+                               int Tn, int d, int G, int E, cudaStream_t st) {
   const int R = G + E;
-  dim3 grid((Tn + 8 * TPW - 1) / (8 * TPW), (R + RB - 1) / RB);
-  router_logits_kernel<T, TPW, RB><<<grid, 256, 0, st>>>(
-      (const T*)x, (const T*)wg, bg, (const T*)we, logits, Tn, d, G, E);
+  dim3 grid((Tn + WT * TPW - 1) / (WT * TPW), (R + WR * RPW - 1) / (WR * RPW));
+  router_logits_bf16_kernel<TPW, RPW, WT, WR><<<grid, WT * WR * 32, 0, st>>>(
+      (const __nv_bfloat16*)x, (const __nv_bfloat16*)wg, bg, (const __nv_bfloat16*)we, logits, Tn, d, G, E);
+}
+
+static cudaError_t launch_logits(bool bf16, const void* x, const void* wg, const float* bg, const void* we,
+                                 float* logits, int Tn, int d, int G, int E, cudaStream_t st) {
+  if (bf16) {
+    if (Tn >= 4096) launch_bf16_logits<8, 8, 2, 4>(x, wg, bg, we, logits, Tn, d, G, E, st);
+    else launch_bf16_logits<2, 4, 4, 2>(x, wg, bg, we, logits, Tn, d, G, E, st);
+  } else {
+    constexpr int TPW = 4, RB = 8;
+    dim3 grid((Tn + 8 * TPW - 1) / (8 * TPW), (G + E + RB - 1) / RB);
+    router_logits_f32_kernel<TPW, RB><<<grid, 256, 0, st>>>((const float*)x, (const float*)wg, bg,
+                                                            (const float*)we, logits, Tn, d, G, E);
+  }
   prof_mark("router_logits", st);
   return cudaGetLastError();
 }
@@ -157,8 +243,7 @@ cudaError_t launch_route(const LayerArgs& a, const void* x, const void* wg, cons
                          const void* we, float* logits, int32_t* gidx, int32_t* eidx, float* gate,
                          cudaStream_t st) {
   if (a.T == 0) return cudaSuccess;
-  cudaError_t err = a.bf16 ? launch_logits<__nv_bfloat16>(x, wg, bg, we, logits, a.T, a.d, a.G, a.E, st)
-                           : launch_logits<float>(x, wg, bg, we, logits, a.T, a.d, a.G, a.E, st);
+  cudaError_t err = launch_logits(a.bf16, x, wg, bg, we, logits, a.T, a.d, a.G, a.E, st);
   if (err != cudaSuccess) return err;
   router_select_kernel<<<(a.T + 127) / 128, 128, 0, st>>>(logits, a.tab, a.T, a.kg, a.ke, gidx, eidx, gate);
   prof_mark("router_select", st);

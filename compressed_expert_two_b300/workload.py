@@ -34,3 +34,34 @@ def bytes_moved(cfg, groups_hit: int, experts_hit: int, T=None) -> float:
     s_res = (0.5 + 2.0 / 64) if cfg.resid == "int4" else 4.0
     return (groups_hit * 3.0 * cfg.d * cfg.f * s_act + experts_hit * 3.0 * cfg.r * (cfg.d + cfg.f) * s_res
             + (cfg.G + cfg.E) * cfg.d * s_act + 2.0 * T * cfg.d * s_act)
+
+
+def kernel_work(cfg, kernel: str, groups_hit: int, experts_hit: int, T=None):
+    """(algorithmic FLOPs, algorithmic DRAM bytes) of one launch of a named kernel.
+
+    Rows R = T k_g.  Weights are counted once per launch at their stored size (BF16 base,
+    INT4 + FP16-scale residual), activations once in and once out.
+      ffn_up:   4 d f R (gate/up base) + 6 r f R k_e (B_gate U, B_up U, A_down^T h);
+                bytes: gate/up bases of the groups hit, B_gate/B_up/A_down of the experts hit,
+                X rows in, hsum rows out.
+      ffn_down: 2 d f R (down base) + 2 r d R k_e (B_down v); bytes: down bases, B_down, hsum in, y out.
+      u_gemm:   4 r d R k_e (A_gate^T x, A_up^T x); bytes: A_gate/A_up of the experts hit, X rows.
+      router:   2 d (G + E) T; bytes: x and the router rows.
+    Other kernels fall back to the whole-layer figures.
+    """
+    T = cfg.T if T is None else T
+    R = T * cfg.kg
+    s_act = 2 if cfg.dtype == "bf16" else 4
+    s_res = (0.5 + 2.0 / 64) if cfg.resid == "int4" else 4.0
+    d, f, r, ke = cfg.d, cfg.f, cfg.r, cfg.ke
+    if kernel.startswith("ffn_up"):
+        return (4.0 * d * f * R + 6.0 * r * f * R * ke,
+                groups_hit * 2.0 * d * f * s_act + experts_hit * 3.0 * r * f * s_res + R * (d + f) * s_act)
+    if kernel.startswith("ffn_down"):
+        return (2.0 * d * f * R + 2.0 * r * d * R * ke,
+                groups_hit * 1.0 * d * f * s_act + experts_hit * r * d * s_res + R * (d + f) * s_act)
+    if kernel.startswith("u_gemm"):
+        return 4.0 * r * d * R * ke, experts_hit * 2.0 * r * d * s_res + R * d * s_act
+    if kernel.startswith("router"):
+        return 2.0 * d * (cfg.G + cfg.E) * T, (T + cfg.G + cfg.E) * d * s_act
+    return flops(cfg, T), bytes_moved(cfg, groups_hit, experts_hit, T)
