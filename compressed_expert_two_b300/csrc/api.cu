@@ -1,6 +1,8 @@
 // C ABI of libmoehier: descriptor validation, workspace planning and launch sequencing.
 #include <string.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -306,3 +308,65 @@ const char* moe_hier_status_string(int status) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------------
+// Permutation without a workspace argument.
+//
+// Some callers cannot hand the library a workspace: a host that owns every byte of device
+// memory through its own pool and forbids any other allocation, or a latency-critical loop in
+// which the implicit device synchronisation of an allocation is not allowed.  For them the
+// permutation's only scratch -- the per-block histograms and their offsets -- lives in the
+// fixed array below, which every GPU that loads the library holds until the process exits.
+// ------------------------------------------------------------------------------------------
+namespace moe {
+
+constexpr int kNoAllocScratchInts = 65536;  // 256 KiB: histograms + offsets, 2 * nblk * (E + G) ints
+static __device__ __align__(256) int32_t g_perm_scratch[kNoAllocScratchInts];
+
+constexpr int kMaxDevices = 64;
+static std::mutex g_scratch_mu;
+static int32_t* g_scratch_dev[kMaxDevices];   // device address of g_perm_scratch, per device
+
+// Device address of the scratch array on the current device (looked up on the first call made
+// with that device current).  In host code `g_perm_scratch` names a host-side stand-in, never
+// the device memory, so kernels must receive this address instead.
+static cudaError_t scratch_on_current_device(int32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_dev[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_perm_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_dev[dev] = (int32_t*)p;
+  }
+  *out = g_scratch_dev[dev];
+  return cudaSuccess;
+}
+
+}  // namespace moe
+
+extern "C" int moe_hier_permute_noalloc(const moe_hier_desc* desc, const int32_t* group_map_host,
+                                        const int32_t* eidx, int32_t* perm, int32_t* inv_pos,
+                                        int32_t* expert_begin, int32_t* expert_count, int32_t* group_begin,
+                                        int32_t* row_asg, int32_t* row_of, int32_t* row_begin, void* stream) {
+  LayerArgs a;
+  if (!group_map_host) return MOE_ERR_INVALID;
+  int st = validate(desc, group_map_host, &a);
+  if (st != MOE_OK) return st;
+  if (!row_begin || (a.T > 0 && (!eidx || !row_asg))) return MOE_ERR_INVALID;
+  const int nblk = (a.T + 255) / 256;
+  const size_t need = 2 * (size_t)nblk * (size_t)(a.E + a.G);
+  if (need > (size_t)kNoAllocScratchInts) return MOE_ERR_WORKSPACE;   // layer too large for the fixed scratch
+  int32_t* scratch = nullptr;
+  if (scratch_on_current_device(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+  // The count kernel writes every histogram entry and the scan every offset it later reads, so
+  // nothing left in the array by an earlier call is used.
+  int32_t* cnt = scratch;
+  int32_t* off = scratch + (size_t)nblk * (a.E + a.G);
+  PermOut o{perm, inv_pos, expert_begin, expert_count, group_begin, row_asg, row_of, row_begin};
+  prof_start((cudaStream_t)stream);
+  return cuda_status(launch_permute(a, eidx, o, cnt, off, nblk, (cudaStream_t)stream));
+}

@@ -155,6 +155,23 @@ const char* moe_hier_status_string(int status);
 int moe_hier_profile_begin(void* const* events, int n_events);
 int moe_hier_profile_end(const char** names, int max_names);
 
+/* moe_hier_permute for callers that cannot supply a workspace: a host that owns all device
+ * memory through its own pool and allows no other allocation, or a latency-critical loop that
+ * may not pay an allocation's implicit device synchronisation.  The paper has no counterpart;
+ * this is a deployment convenience.  Arguments and outputs are those of moe_hier_permute,
+ * without ws/ws_bytes.  The scratch (per-block histograms and offsets) is a fixed array of
+ * 65,536 int32 (256 KiB) inside the library, held by every GPU that loads the library until the
+ * process exits; a layer needs 2 * ceil(T/256) * (E + G) of them, and larger layers are rejected
+ * with MOE_ERR_WORKSPACE before anything is enqueued.  The call allocates nothing.  The first
+ * call on a device looks up the array's device address (with that device current); make that
+ * first call before any stream capture.  All calls share the one array and each kernel
+ * overwrites every entry it later reads, so nothing needs clearing between calls, but calls
+ * whose work overlaps on the GPU (other streams, other host threads) race on it. */
+int moe_hier_permute_noalloc(const moe_hier_desc* desc, const int32_t* group_map_host,
+                             const int32_t* eidx, int32_t* perm, int32_t* inv_pos,
+                             int32_t* expert_begin, int32_t* expert_count, int32_t* group_begin,
+                             int32_t* row_asg, int32_t* row_of, int32_t* row_begin, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
