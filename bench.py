@@ -4,9 +4,15 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
 
 One step = one whole forward pass (route, permute, gate/up GEMM with the residual/SwiGLU epilogue,
-down GEMM, combine) over the workload's T tokens, inputs resident in HBM.  Between timed steps the
-L2 is flushed (a 256 MiB write).  Multi-GPU (torchrun): every rank runs an independent replica on
-its own GPU (tokens are independent; no collective on the data path), weak scaling.
+down GEMM, combine) over the workload's T tokens, inputs resident in HBM.  The timed steps replay
+a CUDA graph captured from one moe_hier_forward call (the same kernels, without the host's
+per-call launch work); the end-to-end figure calls moe_hier_forward directly every step, with the
+host-to-device copy of x and the device-to-host copy of y inside the timed region.  Between timed
+steps the L2 is flushed (a 256 MiB write).  Per-kernel times come from CUDA events that the
+library records between its launches, in a pass whose launches are queued behind a sleep kernel
+so that the intervals hold device time only.  Multi-GPU (torchrun): every rank runs an
+independent replica on its own GPU (tokens are independent; no collective on the data path),
+weak scaling.
 The oracle is only imported by the CPU-baseline leg and by --impl reference.
 """
 from __future__ import annotations
@@ -205,12 +211,41 @@ def run_ours(args, rank, world, local_rank):
     groups_hit = int(torch.unique(out["gidx"].cpu()).numel())
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_k + 1)] for _ in range(K)]
-    for row in ev:
+
+    # ---- per-kernel device times: launches queued behind a sleep kernel, events between them
+    n_prof = max(3, min(args.steps, 10))
+    pev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_k + 1)] for _ in range(n_prof)]
+    for row in pev:
         for e in row:
             e.record(stream)
     torch.cuda.synchronize(dev)
+    for i in range(n_prof):
+        flush.fill_(i & 0xFF)
+        torch.cuda._sleep(2_000_000)               # ~1 ms: the host queues the whole forward meanwhile
+        arr = L.moe_hier_profile_begin([e.cuda_event for e in pev[i]])
+        layer.forward(out=out, routing_out=False)
+        L.moe_hier_profile_end()
+    torch.cuda.synchronize(dev)
+    kern_ms = {}
+    for i in range(n_prof):
+        for j, nm in enumerate(names):
+            kern_ms.setdefault(nm, []).append(pev[i][j].elapsed_time(pev[i][j + 1]))
+
+    # ---- the timed steps: replays of a CUDA graph of one forward call
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        layer.forward(out=out, routing_out=False)          # outside capture: attributes, maps
+        torch.cuda.synchronize(dev)
+        with torch.cuda.graph(graph, stream=cap):
+            layer.forward(out=out, routing_out=False)
+    stream.wait_stream(cap)
+    for _ in range(max(args.warmup, 3)):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     gpu_index = local_rank
     if os.environ.get("CUDA_VISIBLE_DEVICES"):
         ids = os.environ["CUDA_VISIBLE_DEVICES"].split(",")
@@ -225,9 +260,9 @@ def run_ours(args, rank, world, local_rank):
     wall0 = time.perf_counter()
     for i in range(K):
         flush.fill_(i & 0xFF)                      # evict the weights from L2 between steps
-        arr = L.moe_hier_profile_begin([e.cuda_event for e in ev[i]])
-        layer.forward(out=out, routing_out=False)
-        L.moe_hier_profile_end()
+        ev[i][0].record(stream)
+        graph.replay()
+        ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
     if world > 1:
@@ -236,11 +271,7 @@ def run_ours(args, rank, world, local_rank):
     if layer.status() != 0:
         raise RuntimeError("device status after timed steps: %d" % layer.status())
 
-    step_ms = [ev[i][0].elapsed_time(ev[i][n_k]) for i in range(K)]
-    kern_ms = {}
-    for i in range(K):
-        for j, nm in enumerate(names):
-            kern_ms.setdefault(nm, []).append(ev[i][j].elapsed_time(ev[i][j + 1]))
+    step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = sum(step_ms)
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
@@ -314,6 +345,8 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": cfg.T * cfg.d * act_b, "d2h_bytes_per_step": cfg.T * cfg.d * act_b},
         "gpu_launches": n_k * K,
+        "timing": "graph replay of one moe_hier_forward per step (kernels_ms: per-kernel device time, "
+                  "launches queued behind a sleep kernel)",
         "clocks": clk,
         "wall_s_timed": round(wall, 3),
     }

@@ -61,7 +61,7 @@ Plan make_plan(const LayerArgs& a) {
     p.Bus = take(G * f * KRP * 2);
     p.Adn = take(G * KRP * f * 2);
     p.Bdn = take(G * d * 2 * KRP * 2);
-    p.Ubf = take(Rp * 2 * KRP * 4);
+    p.Ubf = take(Rp * 2 * KRP * 2);
     p.hsum_bf = take(Rp * f * 2);
     p.Vpart = take((size_t)p.nchunks * R * a.ke * a.r * 4);
     p.Vt = take(Rp * 2 * KRP * 2);
@@ -147,9 +147,9 @@ static cudaError_t run_ffn(const LayerArgs& a, const Plan& p, void* ws, const vo
                            const float* gate, const int32_t* row_asg, const int32_t* row_begin, void* y_rows,
                            cudaStream_t s) {
   if (p.tc) {
-    TcBufs b{at<__nv_bfloat16>(ws, p.X),   at<__nv_bfloat16>(ws, p.Ain),    at<__nv_bfloat16>(ws, p.Bgs),
-             at<__nv_bfloat16>(ws, p.Bus), at<__nv_bfloat16>(ws, p.Adn),    at<__nv_bfloat16>(ws, p.Bdn),
-             at<float>(ws, p.Ubf), at<__nv_bfloat16>(ws, p.hsum_bf), at<__nv_bfloat16>(ws, p.Vt),
+    TcBufs b{at<__nv_bfloat16>(ws, p.X),   at<__nv_bfloat16>(ws, p.Ain),    at<__half>(ws, p.Bgs),
+             at<__half>(ws, p.Bus),        at<__nv_bfloat16>(ws, p.Adn),    at<__nv_bfloat16>(ws, p.Bdn),
+             at<__half>(ws, p.Ubf), at<__nv_bfloat16>(ws, p.hsum_bf), at<__nv_bfloat16>(ws, p.Vt),
              at<float>(ws, p.Vpart)};
     return launch_ffn_tc(a, x, wg, wu, wd, resid_ptrs(a, resid), eidx, gate, row_asg, row_begin, y_rows, b,
                          at<DevStatus>(ws, p.status), s);

@@ -57,5 +57,8 @@ struct ResidView {
 };
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+// SiLU from the fast exponential and reciprocal intrinsics (relative error ~1e-6); for z << 0
+// the denominator overflows to +inf and the result is -0.
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 }  // namespace moe

@@ -6,17 +6,18 @@
 // BF16/FP16 base, INT4 residual.  Expert body: SwiGLU ("混合专家模型的路由机制与工程落地" 1.2).
 //
 // Rows are (token, group) pairs in (group, token) order; each row carries k_e experts.
-//   1. resid_prep   BF16 stacks of the group's K experts, KRP = K*r padded to 64, holding the
-//                   dequantised values exactly: A_gate^T/A_up^T as hi+lo BF16 pairs
-//                   (Ain [G][2][2*KRP][d]), B_gate/B_up and A_down^T as their integer codes
-//                   (Bgs/Bus [G][f][KRP], Adn [G][KRP][f]; the FP16 scale, constant over a
-//                   64-column tile, is applied on the other side of the product), B_down as a
-//                   hi|lo pair along K (Bdn [G][d][2*KRP]).
+//   1. resid_prep   stacks of the group's K experts, KRP = K*r padded to 64: A_gate^T/A_up^T
+//                   as hi+lo BF16 pairs holding the dequantised values exactly (Ain
+//                   [G][2][2*KRP][d]); B_gate/B_up dequantised to FP16 (Bgs/Bus [G][f][KRP],
+//                   relative rounding <= 2^-11); A_down^T as its integer codes (Adn [G][KRP][f];
+//                   the FP16 scale, constant over a 64-column tile, is applied to the product);
+//                   B_down as a hi|lo BF16 pair along K (Bdn [G][d][2*KRP]).
 //   2. gather_rows  X[i] = x[token(i)] (BF16 rows in (group, token) order).
-//   3. U GEMM       U[i] = X[i] (Ain_hi + Ain_lo)_g^T, FP32: A^T x for every expert of the group.
+//   3. U GEMM       U[i] = X[i] (Ain_hi + Ain_lo)_g^T, FP32 accumulation, stored as FP16:
+//                   A^T x for every expert of the group.
 //   4. ffn_up       per 128-row x 64-column tile of group g: base [Hg|Hu] = X [Wg|Wu]^T once;
-//                   per expert slot s: R_s = U~_s [Bgs|Bus]^T (U~_s = the row's slot-s block of U
-//                   times the tile's B scales, other blocks zero), h_s = silu(Hg + R_gate) *
+//                   per expert slot s: R_s = U~_s [Bgs|Bus]^T (FP16 MMA; U~_s = the row's slot-s
+//                   block of U, other blocks zero), h_s = silu(Hg + R_gate) *
 //                   (Hu + R_up), hsum += gate_s h_s, and v_s += A_down,e_s^T h_s via
 //                   V = h_s Adn_g^T times the tile's A_down scales (tcgen05).
 //   5. v_reduce     sums the v partials of the column chunks into V~ [R][2*KRP] (gate-scaled,
@@ -63,7 +64,8 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 // ------------------------------------------------------------------------------------------
 struct PrepArgs {
   ResidView A[3], B[3];
-  __nv_bfloat16 *Ain, *Bgs, *Bus, *Adn, *Bdn;
+  __nv_bfloat16 *Ain, *Adn, *Bdn;
+  __half *Bgs, *Bus;
   int G, K, d, f, r, KRP;
 };
 
@@ -119,7 +121,7 @@ __global__ void resid_prep_rows_kernel(PrepArgs p, GroupTable tab) {
 
 // Transposed stacks: block (m, g, 64-column chunk) reads the KRP rank rows of the chunk
 // (coalesced), transposes through shared memory and writes 64 rows of KRP (or 2*KRP) values.
-//   m = 0, 1: Bgs/Bus[g][n][j*r + k] = code of B_m,e_j^T[k][n]
+//   m = 0, 1: Bgs/Bus[g][n][j*r + k] = fp16(dequantised B_m,e_j^T[k][n])
 //   m = 2:    Bdn[g][n][j*r + k] = hi, Bdn[g][n][KRP + j*r + k] = lo of B_down,e_j^T[k][n]
 __global__ void __launch_bounds__(256) resid_prep_t_kernel(PrepArgs p, GroupTable tab) {
   constexpr int CW = 64;                   // columns per block
@@ -141,7 +143,7 @@ __global__ void __launch_bounds__(256) resid_prep_t_kernel(PrepArgs p, GroupTabl
       const int e = tab.member[g * K + j];
       const size_t rowi = (size_t)e * r + k;
       const uint32_t bytes = *reinterpret_cast<const uint32_t*>((const uint8_t*)v.vals + rowi * (n / 2) + (c0 + c8) / 2);
-      const float sc = m == 2 ? __half2float(v.scales[rowi * (n / 64) + (c0 + c8) / 64]) : 1.f;
+      const float sc = __half2float(v.scales[rowi * (n / 64) + (c0 + c8) / 64]);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const uint32_t b8 = (bytes >> (8 * q)) & 0xFFu;
@@ -157,17 +159,23 @@ __global__ void __launch_bounds__(256) resid_prep_t_kernel(PrepArgs p, GroupTabl
   }
   __syncthreads();
   const int width = m == 2 ? 2 * KRP : KRP;
-  __nv_bfloat16* base = m == 0 ? p.Bgs : (m == 1 ? p.Bus : p.Bdn);
+  void* base = m == 0 ? (void*)p.Bgs : (m == 1 ? (void*)p.Bus : (void*)p.Bdn);
   for (int it = threadIdx.x; it < CW * (KRP / 8); it += blockDim.x) {
     const int c = it / (KRP / 8), jk0 = (it % (KRP / 8)) * 8;
-    __nv_bfloat16* dst = base + ((size_t)g * n + c0 + c) * width + jk0;
+    uint16_t* dst = (uint16_t*)base + ((size_t)g * n + c0 + c) * width + jk0;
     uint32_t hi[4], lo[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const float a0 = tile[c][jk0 + 2 * q], a1 = tile[c][jk0 + 2 * q + 1];
-      const float h0 = __bfloat162float(__float2bfloat16_rn(a0)), h1 = __bfloat162float(__float2bfloat16_rn(a1));
-      hi[q] = tc::pack_bf16(h0, h1);
-      lo[q] = tc::pack_bf16(a0 - h0, a1 - h1);
+      if (m == 2) {
+        const float h0 = __bfloat162float(__float2bfloat16_rn(a0)), h1 = __bfloat162float(__float2bfloat16_rn(a1));
+        hi[q] = tc::pack_bf16(h0, h1);
+        lo[q] = tc::pack_bf16(a0 - h0, a1 - h1);
+      } else {
+        __half2 h2 = __floats2half2_rn(a0, a1);
+        hi[q] = *reinterpret_cast<uint32_t*>(&h2);
+        lo[q] = 0u;
+      }
     }
     *reinterpret_cast<uint4*>(dst) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
     if (m == 2) *reinterpret_cast<uint4*>(dst + KRP) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
@@ -189,10 +197,11 @@ __global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ x, const in
 }
 
 // ------------------------------------------------------------------------------------------
-// 3/6. Generic grouped GEMM: out[row] = [A0 | A1][i] [B0_g | B1_g]^T (BF16 in, FP32 acc, BF16 or
-//      FP32 out).  Group g's B rows start at g*b_stride in B0 and at g*b_stride + b1_off in B1.
+// 3/6. Generic grouped GEMM: out[row] = [A0 | A1][i] [B0_g | B1_g]^T (BF16 in, FP32 acc, BF16,
+//      FP32 or FP16 out).  Group g's B rows start at g*b_stride in B0 and at g*b_stride + b1_off in B1.
+enum OutKind { kOutBf16 = 0, kOutF32 = 1, kOutF16 = 2 };
 // ------------------------------------------------------------------------------------------
-template <int BN, int STAGES, bool OUT_F32>
+template <int BN, int STAGES, int OUT>
 __global__ void __launch_bounds__(192, 1) tc_gemm_kernel(
     const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
     const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1, int nk0, int nk1,
@@ -273,10 +282,20 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_kernel(
         tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c, v);
         tc::tmem_ld_wait();
         if (valid) {
-          if constexpr (OUT_F32) {
+          if constexpr (OUT == kOutF32) {
             uint4* d4 = reinterpret_cast<uint4*>((float*)out + orow * out_ld + n0 + c);
 #pragma unroll
             for (int e = 0; e < 4; ++e) d4[e] = make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+          } else if constexpr (OUT == kOutF16) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              __half2 h2 = __floats2half2_rn(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+              pk[e] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            uint4* d4 = reinterpret_cast<uint4*>((__half*)out + orow * out_ld + n0 + c);
+            d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           } else {
             uint32_t pk[8];
 #pragma unroll
@@ -300,24 +319,35 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_kernel(
 // ------------------------------------------------------------------------------------------
 // 4. Fused gate/up tile: base once, per-slot residual, SwiGLU, gated sum, down-residual partials
 //
-// Warp roles (11 warps): 0 TMA producer; 1 base MMA issuer (owns TMEM); 2 residual/V MMA
-// issuer; 3..10 epilogue, two warps per TMEM lane quarter, warp group h in {0,1} handling the
-// tile's d_ff columns [32h, 32h+32) (group 0 also the U~ gate block and the V readout, group 1
-// the U~ up block).  TMEM columns: base accumulators [2][128] (gate 64 | up 64, double
-// buffered so the next tile's K-loop overlaps this tile's epilogue), R [128], V [KRP].
+// One CTA owns a 128-row tile of one group and a chunk of 64-column d_ff tiles.  Warp roles
+// (12 warps): 0 TMA producer of the base stages (X, W_gate, W_up); 1 base MMA issuer (owns TMEM);
+// 2 residual/V MMA issuer; 3 TMA producer of the residual tiles (B_gate, B_up, A_down^T codes);
+// 4..11 epilogue, two warps per TMEM lane quarter, warp group h in {0,1} handling the tile's d_ff
+// columns [32h, 32h+32) (group 0 also builds the gate half of U~ and reads V out, group 1 the up
+// half of U~).
+//
+// TMEM columns: two accumulators acc[b] = [gate 64 | up 64] (double buffered so that the next
+// tile's K-loop overlaps this tile's slots) and V (KRP).  The residual is added INTO the
+// accumulator: for slot s of a tile the residual MMA adds D_s [B_gate | B_up]^T, where
+// D_0 = U~_0 and D_s = U~_s - U~_{s-1}, so that after it acc = base + R_s exactly up to FP32
+// rounding (the blocks of U~_s and U~_{s-1} are disjoint: a row's experts are distinct).  The
+// epilogue reads acc once per slot (no separate residual buffer), forms h_s = silu(a) * b, adds
+// gate_s h_s into the tile's hsum, and stores h_s (BF16) for the V MMA V = h_s A_down^T, which
+// runs one slot behind so that it leaves the slot chain.
 // ------------------------------------------------------------------------------------------
 constexpr int kMaxKe = 4;
 constexpr int kRank = 16;      // residual rank handled by this kernel
-constexpr int kUpWarps = 11;
+constexpr int kUpWarps = 12;
 constexpr int kUpEpi = 256;    // epilogue threads
+constexpr int kUpEpiWarp0 = 4;
 
 struct UpArgs {
   const int32_t* row_begin;
   const int32_t* row_asg;
   const int32_t* eidx;
   const float* gate;
-  const float* U;           // [R][2*KRP]: A_gate^T x | A_up^T x of the group's experts
-  const __half *sBg, *sBu, *sAd;   // FP16 scales [E][16][f/64] of B_gate, B_up, A_down^T
+  const __half* U;          // [R][2*KRP] FP16: A_gate^T x | A_up^T x of the group's experts
+  const __half* sAd;        // FP16 scales [E][16][f/64] of A_down^T
   __nv_bfloat16* hsum;      // [R][f]
   float* Vpart;             // [nchunks][R][ke][16]
   DevStatus* status;
@@ -331,7 +361,7 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
                : "r"(taddr));
 }
 
-template <int KRP, int STAGES, int KE>
+template <int KRP, int STAGES, int KE, int RBUF>
 __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
     const __grid_constant__ CUtensorMap mX, const __grid_constant__ CUtensorMap mWg,
     const __grid_constant__ CUtensorMap mWu, const __grid_constant__ CUtensorMap mBg,
@@ -339,15 +369,18 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
   constexpr uint32_t X_BYTES = kTile * 128, W_BYTES = 2 * kNf * 128, STAGE_BYTES = X_BYTES + W_BYTES;
   constexpr uint32_t BRES_BYTES = KRP * kNf * 2;          // one of Bg / Bu tiles (64 rows x KRP)
   constexpr uint32_t AD_BYTES = KRP * 128;                 // KRP rows x 64 columns
+  constexpr uint32_t RES_BYTES = 2 * BRES_BYTES + AD_BYTES;
   constexpr uint32_t UT_BYTES = kTile * KRP * 2;           // 128 rows x KRP
   constexpr int KATOM = KRP / 64;
-  constexpr uint32_t COL_R = 4 * kNf, COL_V = 6 * kNf;
+  constexpr uint32_t COL_V = 4 * kNf;
   static_assert(COL_V + KRP <= 512, "TMEM budget");
+  static_assert(KE >= 1 && KE <= kMaxKe, "slots");
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full[STAGES], empty[STAGES];
-  __shared__ uint64_t base_full[2], base_empty[2];
-  __shared__ uint64_t res_full, res_empty, u_ready, r_full, h_ready, v_full, fin1, fin2;
+  __shared__ uint64_t base_full[2], acc_empty[2];
+  __shared__ uint64_t rb_full[RBUF], rb_empty[RBUF], ad_full[RBUF], ad_empty[RBUF];
+  __shared__ uint64_t acc_full, acc_read, u_ready, h_ready, v_full, v_empty, fin1, fin2;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
@@ -362,10 +395,8 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
 
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sStage = smem;
-  uint8_t* sBg = sStage + STAGES * STAGE_BYTES;
-  uint8_t* sBu = sBg + BRES_BYTES;
-  uint8_t* sAd = sBu + BRES_BYTES;
-  uint8_t* sUg = sAd + AD_BYTES;
+  uint8_t* sRes = sStage + STAGES * STAGE_BYTES;     // RBUF x [Bg | Bu | Ad]
+  uint8_t* sUg = sRes + RBUF * RES_BYTES;
   uint8_t* sUu = sUg + UT_BYTES;
   uint8_t* sH = sUu + UT_BYTES;
 
@@ -373,13 +404,17 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
   const tc::Abort ab{&abort_flag, p.status};
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { tc::bar_init(&full[s], 1); tc::bar_init(&empty[s], 1); }
-    for (int b = 0; b < 2; ++b) { tc::bar_init(&base_full[b], 1); tc::bar_init(&base_empty[b], kUpEpi); }
-    tc::bar_init(&res_full, 1);
-    tc::bar_init(&res_empty, 1);
+    for (int b = 0; b < 2; ++b) { tc::bar_init(&base_full[b], 1); tc::bar_init(&acc_empty[b], kUpEpi); }
+    for (int b = 0; b < RBUF; ++b) {
+      tc::bar_init(&rb_full[b], 1); tc::bar_init(&rb_empty[b], 1);
+      tc::bar_init(&ad_full[b], 1); tc::bar_init(&ad_empty[b], 1);
+    }
+    tc::bar_init(&acc_full, 1);
+    tc::bar_init(&acc_read, kUpEpi);
     tc::bar_init(&u_ready, kUpEpi);
-    tc::bar_init(&r_full, 1);
     tc::bar_init(&h_ready, kUpEpi);
     tc::bar_init(&v_full, 1);
+    tc::bar_init(&v_empty, kUpEpi);
     tc::bar_init(&fin1, 1);
     tc::bar_init(&fin2, 1);
     abort_flag = 0;
@@ -393,9 +428,8 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer: per f-tile the d/64 stages, then the residual tiles
+      // ---------------- TMA producer of the base stages
       tc::prefetch_map(&mX); tc::prefetch_map(&mWg); tc::prefetch_map(&mWu);
-      tc::prefetch_map(&mBg); tc::prefetch_map(&mBu); tc::prefetch_map(&mAd);
       int kc = 0;
       bool ok = true;
       for (int lt = 0; lt < nft && ok; ++lt) {
@@ -409,27 +443,38 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
           tc::tma_load_2d(st + X_BYTES, &mWg, &full[s], kb * 64, g * f + n0);
           tc::tma_load_2d(st + X_BYTES + kNf * 128, &mWu, &full[s], kb * 64, g * f + n0);
         }
-        if (!ok) break;
-        if (lt > 0 && !tc::bar_wait(&res_empty, (lt - 1) & 1, ab, 12)) break;
-        tc::bar_expect_tx(&res_full, 2 * BRES_BYTES + AD_BYTES);
+      }
+      if (abort_flag) tc::drain_copies();
+    }
+  } else if (warp == 3) {
+    if (lane == 0) {
+      // ---------------- TMA producer of the residual tiles (one set per d_ff tile)
+      tc::prefetch_map(&mBg); tc::prefetch_map(&mBu); tc::prefetch_map(&mAd);
+      for (int lt = 0; lt < nft; ++lt) {
+        const int n0 = (ft0 + lt) * kNf, rb = lt % RBUF, use = lt / RBUF;
+        uint8_t* sr = sRes + rb * RES_BYTES;
+        if (use > 0 && !tc::bar_wait(&rb_empty[rb], (use - 1) & 1, ab, 13)) break;
+        tc::bar_expect_tx(&rb_full[rb], 2 * BRES_BYTES);
 #pragma unroll
         for (int a = 0; a < KATOM; ++a) {
-          tc::tma_load_2d(sBg + a * kNf * 128, &mBg, &res_full, a * 64, g * f + n0);
-          tc::tma_load_2d(sBu + a * kNf * 128, &mBu, &res_full, a * 64, g * f + n0);
+          tc::tma_load_2d(sr + a * kNf * 128, &mBg, &rb_full[rb], a * 64, g * f + n0);
+          tc::tma_load_2d(sr + BRES_BYTES + a * kNf * 128, &mBu, &rb_full[rb], a * 64, g * f + n0);
         }
-        tc::tma_load_2d(sAd, &mAd, &res_full, n0, g * KRP);
+        if (use > 0 && !tc::bar_wait(&ad_empty[rb], (use - 1) & 1, ab, 14)) break;
+        tc::bar_expect_tx(&ad_full[rb], AD_BYTES);
+        tc::tma_load_2d(sr + 2 * BRES_BYTES, &mAd, &ad_full[rb], n0, g * KRP);
       }
       if (abort_flag) tc::drain_copies();
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---------------- base MMA issuer: [Hg | Hu] = X [Wg | Wu]^T into base[lt & 1]
+      // ---------------- base MMA issuer: [Hg | Hu] = X [Wg | Wu]^T into acc[lt & 1]
       constexpr uint32_t id_base = tc::idesc_bf16(kTile, 2 * kNf);
       int kc = 0;
       bool ok = true;
       for (int lt = 0; lt < nft && ok; ++lt) {
         const int b = lt & 1;
-        if (lt >= 2 && !tc::bar_wait(&base_empty[b], ((lt >> 1) - 1) & 1, ab, 21)) break;
+        if (lt >= 2 && !tc::bar_wait(&acc_empty[b], ((lt >> 1) - 1) & 1, ab, 21)) break;
         tc::fence_after();
         const uint32_t dcol = tmem + b * 2 * kNf;
         for (int kb = 0; kb < nkb; ++kb, ++kc) {
@@ -452,57 +497,67 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
     }
   } else if (warp == 2) {
     if (lane == 0) {
-      // ---------------- residual issuer: R = U~_s [Bg | Bu]^T, V = H_s Adn^T per slot
-      constexpr uint32_t id_res = tc::idesc_bf16(kTile, kNf);
+      // ---------------- residual issuer: acc[b] += D_s [Bg | Bu]^T, then (one slot behind)
+      //                  V = h_s Adn^T
+      constexpr uint32_t id_res = tc::idesc_f16(kTile, kNf);     // FP16 U~ x FP16 B
       constexpr uint32_t id_v = tc::idesc_bf16(kTile, KRP);
-      const uint32_t ug = tc::smem_u32(sUg), uu = tc::smem_u32(sUu);
-      const uint32_t bg = tc::smem_u32(sBg), bu = tc::smem_u32(sBu);
-      const uint32_t hh = tc::smem_u32(sH), ad = tc::smem_u32(sAd);
-      int pu = 0, ph = 0;
-      bool ok = true;
-      for (int lt = 0; lt < nft && ok; ++lt) {
-        if (!tc::bar_wait(&res_full, lt & 1, ab, 23)) break;
+      const uint32_t ug = tc::smem_u32(sUg), uu = tc::smem_u32(sUu), hh = tc::smem_u32(sH);
+      const int n_slots = nft * KE;
+      // V MMA of slot index tau (tile tau / KE, slot tau % KE)
+      auto issue_v = [&](int tau) -> bool {
+        const int lt = tau / KE, s = tau % KE, rb = lt % RBUF, use = lt / RBUF;
+        if (s == 0 && !tc::bar_wait(&ad_full[rb], use & 1, ab, 26)) return false;
+        if (!tc::bar_wait(&h_ready, tau & 1, ab, 27)) return false;
+        if (tau >= 1 && !tc::bar_wait(&v_empty, (tau - 1) & 1, ab, 28)) return false;
         tc::fence_after();
-        for (int s = 0; s < KE; ++s) {
-          if (!tc::bar_wait(&u_ready, pu & 1, ab, 24)) { ok = false; break; }
-          ++pu;
-          tc::fence_after();
+        const uint32_t ad = tc::smem_u32(sRes + rb * RES_BYTES + 2 * BRES_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < KRP / 16; ++kk) {
-            const uint32_t off_u = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-            const uint32_t off_b = (kk >> 2) * (kNf * 128) + (kk & 3) * 32;
-            tc::mma_bf16(tmem + COL_R, tc::sdesc(ug + off_u), tc::sdesc(bg + off_b), id_res, kk != 0);
-            tc::mma_bf16(tmem + COL_R + kNf, tc::sdesc(uu + off_u), tc::sdesc(bu + off_b), id_res, kk != 0);
-          }
-          tc::mma_commit(&r_full);
-          if (!tc::bar_wait(&h_ready, ph & 1, ab, 25)) { ok = false; break; }
-          ++ph;
-          tc::fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc::mma_bf16(tmem + COL_V, tc::sdesc(hh + 32 * kk), tc::sdesc(ad + 32 * kk), id_v, kk != 0);
-          tc::mma_commit(&v_full);
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma_bf16(tmem + COL_V, tc::sdesc(hh + 32 * kk), tc::sdesc(ad + 32 * kk), id_v, kk != 0);
+        tc::mma_commit(&v_full);
+        if (s == KE - 1) tc::mma_commit(&ad_empty[rb]);
+        return true;
+      };
+      bool ok = true;
+      for (int sig = 0; sig < n_slots && ok; ++sig) {
+        const int lt = sig / KE, s = sig % KE, b = lt & 1, rb = lt % RBUF, use = lt / RBUF;
+        if (sig >= 1 && !issue_v(sig - 1)) { ok = false; break; }
+        if (s == 0) {
+          if (!tc::bar_wait(&base_full[b], (lt >> 1) & 1, ab, 23)) { ok = false; break; }
+          if (!tc::bar_wait(&rb_full[rb], use & 1, ab, 24)) { ok = false; break; }
         }
-        if (!ok) break;
-        tc::mma_commit(&res_empty);
+        if (!tc::bar_wait(&u_ready, sig & 1, ab, 25)) { ok = false; break; }
+        if (s > 0 && !tc::bar_wait(&acc_read, (sig - 1) & 1, ab, 29)) { ok = false; break; }
+        tc::fence_after();
+        const uint32_t bg = tc::smem_u32(sRes + rb * RES_BYTES), bu = bg + BRES_BYTES;
+        const uint32_t dcol = tmem + b * 2 * kNf;
+#pragma unroll
+        for (int kk = 0; kk < KRP / 16; ++kk) {
+          const uint32_t off_u = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+          const uint32_t off_b = (kk >> 2) * (kNf * 128) + (kk & 3) * 32;
+          tc::mma_bf16(dcol, tc::sdesc(ug + off_u), tc::sdesc(bg + off_b), id_res, 1u);
+          tc::mma_bf16(dcol + kNf, tc::sdesc(uu + off_u), tc::sdesc(bu + off_b), id_res, 1u);
+        }
+        tc::mma_commit(&acc_full);
+        if (s == KE - 1) tc::mma_commit(&rb_empty[rb]);
       }
+      if (ok && n_slots > 0) issue_v(n_slots - 1);
       tc::mma_commit(&fin2);
       const uint64_t t0 = tc::now_ns();
       while (!tc::bar_test(&fin2, 0) && tc::now_ns() - t0 < tc::kWaitNs) {}
     }
   } else {
     // ---------------- epilogue: one thread per (tile row, column half)
-    const int q = warp & 3, half = (warp - 3) >> 2, row = q * 32 + lane, i = r0 + row;
+    const int q = warp & 3, half = (warp - kUpEpiWarp0) >> 2, row = q * 32 + lane, i = r0 + row;
     const bool valid = i < r1;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const int c_half = half * 32;                    // this group's first column of the tile
-    uint8_t* sU = half == 0 ? sUg : sUu;             // U~ block this group writes
-    const __half* sB = half == 0 ? p.sBg : p.sBu;
+    uint8_t* sU = half == 0 ? sUg : sUu;             // U~ half this group writes
     int le[KE], eid[KE];
     float gt[KE];
 #pragma unroll
     for (int s = 0; s < KE; ++s) { le[s] = 0; eid[s] = 0; gt[s] = 0.f; }
-    const float* urow = p.U;
+    const __half* urow = p.U;
     if (valid) {
       const int b = p.row_asg[i], t = b / p.kg, j = b % p.kg, k = p.kg * KE;
 #pragma unroll
@@ -514,75 +569,116 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
       }
       urow = p.U + (size_t)i * 2 * KRP + half * KRP;
     }
-    {   // zero this row of this group's U~ matrix
-      for (int a = 0; a < KATOM; ++a) {
-        uint4* z = reinterpret_cast<uint4*>(sU + a * kTile * 128 + (row >> 3) * 1024 + (row & 7) * 128);
+    // this row of this half's U~ starts at zero
 #pragma unroll
-        for (int c = 0; c < 8; ++c) z[c] = make_uint4(0, 0, 0, 0);
-      }
+    for (int a = 0; a < KATOM; ++a) {
+      uint4* z = reinterpret_cast<uint4*>(sU + a * kTile * 128 + (row >> 3) * 1024 + (row & 7) * 128);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) z[c] = make_uint4(0, 0, 0, 0);
     }
-    float vacc[KE][kRank];
+    // V accumulators: half h keeps the slots s with s % 2 == h (vacc[s / 2])
+    constexpr int KV = (KE + 1) / 2;
+    float vacc[KV][kRank];
 #pragma unroll
-    for (int s = 0; s < KE; ++s)
+    for (int s = 0; s < KV; ++s)
 #pragma unroll
       for (int k = 0; k < kRank; ++k) vacc[s][k] = 0.f;
 
-    // U~ block values of (tile lt, slot s) for this row: bf16(U * scale), loaded one step ahead
+    // U~ values of slot s for this row (FP16, the same for every d_ff tile)
     auto load_u = [&](int lt, int s, uint32_t (&pk)[8]) {
+      (void)lt;
       if (!valid) return;
-      const int ng = (ft0 + lt) * kNf / 64;
-      const float* u = urow + le[s] * kRank;
-      const __half* sc = sB + (size_t)eid[s] * kRank * fg + ng;
-#pragma unroll
-      for (int k = 0; k < kRank; k += 2)
-        pk[k / 2] = tc::pack_bf16(u[k] * __half2float(sc[(size_t)k * fg]), u[k + 1] * __half2float(sc[(size_t)(k + 1) * fg]));
+      const uint4* u4 = reinterpret_cast<const uint4*>(urow + le[s] * kRank);
+      const uint4 a = u4[0], b = u4[1];
+      pk[0] = a.x; pk[1] = a.y; pk[2] = a.z; pk[3] = a.w;
+      pk[4] = b.x; pk[5] = b.y; pk[6] = b.z; pk[7] = b.w;
     };
+    auto put_block = [&](int blk, const uint32_t (&pk)[8], uint32_t flip) {
+      *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, blk * kRank, kTile)) =
+          make_uint4(pk[0] ^ flip, pk[1] ^ flip, pk[2] ^ flip, pk[3] ^ flip);
+      *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, blk * kRank + 8, kTile)) =
+          make_uint4(pk[4] ^ flip, pk[5] ^ flip, pk[6] ^ flip, pk[7] ^ flip);
+    };
+    auto zero_block = [&](int blk) {
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, blk * kRank, kTile)) = z;
+      *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, blk * kRank + 8, kTile)) = z;
+    };
+    // U~ holds the last delta: +values in block nz_pos, -values in block nz_neg (or none).
+    int nz_pos = -1, nz_neg = -1;
     uint32_t unext[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) unext[c] = 0u;
+    // Writes the delta of slot s (first slot of a tile: no subtraction) from unext.
+    auto build_delta = [&](int s) {
+      if (!valid) return;
+      const int pos = le[s], neg = s > 0 ? le[s - 1] : -1;
+      if (neg >= 0) {
+        // the previous slot's values are still in block neg (= the last nz_pos): negate in place
+        uint4* b0 = reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, neg * kRank, kTile));
+        uint4* b1 = reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, neg * kRank + 8, kTile));
+        const uint4 v0 = *b0, v1 = *b1;
+        constexpr uint32_t F = 0x80008000u;          // exact FP16 negation
+        *b0 = make_uint4(v0.x ^ F, v0.y ^ F, v0.z ^ F, v0.w ^ F);
+        *b1 = make_uint4(v1.x ^ F, v1.y ^ F, v1.z ^ F, v1.w ^ F);
+      }
+      if (nz_neg >= 0 && nz_neg != pos && nz_neg != neg) zero_block(nz_neg);
+      if (nz_pos >= 0 && nz_pos != pos && nz_pos != neg) zero_block(nz_pos);
+      put_block(pos, unext, 0u);
+      nz_pos = pos; nz_neg = neg;
+    };
+
     load_u(0, 0, unext);
-    int pr = 0, pv = 0, cur = -1;
+    build_delta(0);
+    tc::fence_async_smem();
+    tc::bar_arrive(&u_ready);
+    if (KE > 1) load_u(0, KE > 1 ? 1 : 0, unext);
+    else if (nft > 1) load_u(1, 0, unext);
+
+    __half2 sc_ad[kRank / 2];                        // A_down scales of the slot V is pending for
     bool ok = true;
+    int sig = 0;
     for (int lt = 0; lt < nft && ok; ++lt) {
-      const int n0 = (ft0 + lt) * kNf;
       const int bsel = lt & 1;
-      const uint32_t base_col = bsel * 2 * kNf;
+      const uint32_t acc_col = bsel * 2 * kNf;
       float hs[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) hs[c] = 0.f;
-      bool waited_base = false;
 #pragma unroll
-      for (int s = 0; s < KE; ++s) {
-        // U~ block for slot s (this group's matrix), previous block cleared
-        if (valid) {
-          if (cur >= 0 && cur != le[s]) {
-            const uint4 zero = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, cur * kRank, kTile)) = zero;
-            *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, cur * kRank + 8, kTile)) = zero;
+      for (int s = 0; s < KE; ++s, ++sig) {
+        // (A) V of the previous slot: wait (this also frees sH), read the row's block, scale
+        if (sig >= 1) {
+          if (!tc::bar_wait(&v_full, (sig - 1) & 1, ab, 30)) { ok = false; break; }
+          tc::fence_after();
+          const int ps = s > 0 ? s - 1 : KE - 1;
+          if (half == (ps & 1)) {
+#pragma unroll 1
+            for (int jb = 0; jb < KRP / 16; ++jb) {
+              uint32_t vv[16];
+              tc::tmem_ld16(tmem + lane_off + COL_V + jb * 16, vv);
+              tc::tmem_ld_wait();
+              if (valid && jb == le[ps]) {
+#pragma unroll
+                for (int k = 0; k < kRank; k += 2) {
+                  const float2 sf = __half22float2(sc_ad[k / 2]);
+                  vacc[ps / 2][k] += __uint_as_float(vv[k]) * sf.x;
+                  vacc[ps / 2][k + 1] += __uint_as_float(vv[k + 1]) * sf.y;
+                }
+              }
+            }
           }
-          *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, le[s] * kRank, kTile)) =
-              make_uint4(unext[0], unext[1], unext[2], unext[3]);
-          *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, le[s] * kRank + 8, kTile)) =
-              make_uint4(unext[4], unext[5], unext[6], unext[7]);
-          cur = le[s];
+          tc::fence_before();
+          tc::bar_arrive(&v_empty);
         }
-        tc::fence_async_smem();
-        tc::bar_arrive(&u_ready);
-        // prefetch the next slot's U~ values while the residual MMA runs
-        if (s + 1 < KE) load_u(lt, s + 1, unext);
-        else if (lt + 1 < nft) load_u(lt + 1, 0, unext);
-        if (!waited_base) {
-          if (!tc::bar_wait(&base_full[bsel], (lt >> 1) & 1, ab, 30)) { ok = false; break; }
-          waited_base = true;
-        }
-        if (!tc::bar_wait(&r_full, pr & 1, ab, 31)) { ok = false; break; }
-        ++pr;
+        // (B) acc = base + R_s
+        if (!tc::bar_wait(&acc_full, sig & 1, ab, 31)) { ok = false; break; }
         tc::fence_after();
+        // (C) h_s = silu(a) * b for this half's 32 columns; hsum; h_s -> sH
 #pragma unroll
         for (int c = 0; c < 32; c += 8) {
-          uint32_t bgv[8], buv[8], rgv[8], ruv[8];
-          tmem_ld8(tmem + lane_off + base_col + c_half + c, bgv);
-          tmem_ld8(tmem + lane_off + base_col + kNf + c_half + c, buv);
-          tmem_ld8(tmem + lane_off + COL_R + c_half + c, rgv);
-          tmem_ld8(tmem + lane_off + COL_R + kNf + c_half + c, ruv);
+          uint32_t av[8], bv[8];
+          tmem_ld8(tmem + lane_off + acc_col + c_half + c, av);
+          tmem_ld8(tmem + lane_off + acc_col + kNf + c_half + c, bv);
           tc::tmem_ld_wait();
           uint32_t pk[4];
 #pragma unroll
@@ -590,63 +686,80 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
             float h2[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-              const float a = __uint_as_float(bgv[e + u]) + __uint_as_float(rgv[e + u]);
-              const float bb = __uint_as_float(buv[e + u]) + __uint_as_float(ruv[e + u]);
-              h2[u] = silu_f(a) * bb;
+              h2[u] = silu_fast(__uint_as_float(av[e + u])) * __uint_as_float(bv[e + u]);
               hs[c + e + u] += gt[s] * h2[u];
             }
             pk[e / 2] = tc::pack_bf16(h2[0], h2[1]);
           }
           *reinterpret_cast<uint4*>(sH + tc::sw128_offset(row, c_half + c, kTile)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
+        // (D) acc read
         tc::fence_before();
+        tc::bar_arrive(&acc_read);
+        if (s == KE - 1) tc::bar_arrive(&acc_empty[bsel]);
+        // (E) h_s ready for the V MMA
         tc::fence_async_smem();
         tc::bar_arrive(&h_ready);
-        __half2 sc_ad[kRank / 2];
-        if (half == 0 && valid) {
-          const __half* sc = p.sAd + (size_t)eid[s] * kRank * fg + n0 / 64;
+        if (half == (s & 1) && valid) {
+          const __half* sc = p.sAd + (size_t)eid[s] * kRank * fg + ft0 + lt;
 #pragma unroll
           for (int k = 0; k < kRank; k += 2) sc_ad[k / 2] = __halves2half2(sc[(size_t)k * fg], sc[(size_t)(k + 1) * fg]);
         }
-        if (!tc::bar_wait(&v_full, pv & 1, ab, 32)) { ok = false; break; }
-        ++pv;
-        tc::fence_after();
-        if (half == 0) {
-#pragma unroll
-          for (int jb = 0; jb < KRP / 16; ++jb) {
-            uint32_t vv[16];
-            tc::tmem_ld16(tmem + lane_off + COL_V + jb * 16, vv);
-            tc::tmem_ld_wait();
-            if (jb == le[s] && valid) {
-#pragma unroll
-              for (int k = 0; k < kRank; k += 2) {
-                const float2 sf = __half22float2(sc_ad[k / 2]);
-                vacc[s][k] += __uint_as_float(vv[k]) * sf.x;
-                vacc[s][k + 1] += __uint_as_float(vv[k + 1]) * sf.y;
-              }
-            }
-          }
+        // (F) delta for the next slot (U~ is free: the residual MMA of this slot has completed)
+        const bool more = s + 1 < KE || lt + 1 < nft;
+        if (more) {
+          build_delta(s + 1 < KE ? s + 1 : 0);
+          tc::fence_async_smem();
+          tc::bar_arrive(&u_ready);
+          // prefetch the slot after that
+          const int s2 = (s + 2) % KE;
+          const int lt2 = lt + (s + 2) / KE;
+          if (lt2 < nft) load_u(lt2, s2, unext);
         }
       }
       if (!ok) break;
+      // (G) hsum of this tile
       if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(p.hsum + (size_t)i * f + n0 + c_half);
+        uint4* dst = reinterpret_cast<uint4*>(p.hsum + (size_t)i * f + (ft0 + lt) * kNf + c_half);
 #pragma unroll
         for (int c = 0; c < 32; c += 8)
           dst[c / 8] = make_uint4(tc::pack_bf16(hs[c], hs[c + 1]), tc::pack_bf16(hs[c + 2], hs[c + 3]),
                                   tc::pack_bf16(hs[c + 4], hs[c + 5]), tc::pack_bf16(hs[c + 6], hs[c + 7]));
       }
-      tc::fence_before();
-      tc::bar_arrive(&base_empty[bsel]);
     }
-    if (ok && valid && half == 0) {
+    // V of the last slot
+    if (ok && sig >= 1) {
+      if (!tc::bar_wait(&v_full, (sig - 1) & 1, ab, 33)) ok = false;
+      tc::fence_after();
+      constexpr int ps = KE - 1;
+      if (ok && half == (ps & 1)) {
+#pragma unroll 1
+        for (int jb = 0; jb < KRP / 16; ++jb) {
+          uint32_t vv[16];
+          tc::tmem_ld16(tmem + lane_off + COL_V + jb * 16, vv);
+          tc::tmem_ld_wait();
+          if (valid && jb == le[ps]) {
+#pragma unroll
+            for (int k = 0; k < kRank; k += 2) {
+              const float2 sf = __half22float2(sc_ad[k / 2]);
+              vacc[ps / 2][k] += __uint_as_float(vv[k]) * sf.x;
+              vacc[ps / 2][k + 1] += __uint_as_float(vv[k + 1]) * sf.y;
+            }
+          }
+        }
+      }
+    }
+    if (ok && valid) {
       float* vp = p.Vpart + ((size_t)blockIdx.x * p.R + i) * KE * kRank;
 #pragma unroll
       for (int s = 0; s < KE; ++s)
+        if (half == (s & 1)) {
 #pragma unroll
-        for (int k = 0; k < kRank; k += 4)
-          *reinterpret_cast<float4*>(vp + s * kRank + k) =
-              make_float4(gt[s] * vacc[s][k], gt[s] * vacc[s][k + 1], gt[s] * vacc[s][k + 2], gt[s] * vacc[s][k + 3]);
+          for (int k = 0; k < kRank; k += 4)
+            *reinterpret_cast<float4*>(vp + s * kRank + k) =
+                make_float4(gt[s] * vacc[s / 2][k], gt[s] * vacc[s / 2][k + 1], gt[s] * vacc[s / 2][k + 2],
+                            gt[s] * vacc[s / 2][k + 3]);
+        }
     }
   }
   tc::fence_before();
@@ -663,34 +776,40 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
 __global__ void v_reduce_kernel(const float* __restrict__ Vpart, const int32_t* __restrict__ row_asg,
                                 const int32_t* __restrict__ eidx, GroupTable tab, int R, int kg, int ke,
                                 int nchunks, int KRP, __nv_bfloat16* __restrict__ Vt) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= R) return;
-  uint4* row = reinterpret_cast<uint4*>(Vt + (size_t)i * 2 * KRP);
-  for (int c = 0; c < 2 * KRP / 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
+  // one thread per (row, 16-wide block of V~): the block of local expert jb holds the gated v of
+  // the row's slot routed to that expert (zero if none); both halves (hi, lo of Bdn) get a copy
+  const int nblk = KRP / kRank;
+  const int w = blockIdx.x * blockDim.x + threadIdx.x;
+  if (w >= R * nblk) return;
+  const int i = w / nblk, jb = w % nblk;
   const int b = row_asg[i], t = b / kg, j = b % kg;
-  for (int s = 0; s < ke; ++s) {
-    const int jl = tab.local_of[eidx[(size_t)t * kg * ke + j * ke + s]];
-    float acc[kRank];
+  int slot = -1;
+  for (int s = 0; s < ke; ++s)
+    if (jb < tab.K && tab.local_of[eidx[(size_t)t * kg * ke + j * ke + s]] == jb) slot = s;
+  float acc[kRank];
 #pragma unroll
-    for (int k = 0; k < kRank; ++k) acc[k] = 0.f;
+  for (int k = 0; k < kRank; ++k) acc[k] = 0.f;
+  if (slot >= 0) {
+    const float4* src = reinterpret_cast<const float4*>(Vpart + ((size_t)i * ke + slot) * kRank);
+    const size_t cstride = (size_t)R * ke * kRank / 4;   // float4s per chunk
+#pragma unroll 4
     for (int c = 0; c < nchunks; ++c) {
-      const float4* src = reinterpret_cast<const float4*>(Vpart + (((size_t)c * R + i) * ke + s) * kRank);
 #pragma unroll
       for (int q = 0; q < kRank / 4; ++q) {
-        const float4 v4 = src[q];
+        const float4 v4 = src[c * cstride + q];
         acc[4 * q] += v4.x; acc[4 * q + 1] += v4.y; acc[4 * q + 2] += v4.z; acc[4 * q + 3] += v4.w;
       }
     }
-    uint32_t pk[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) pk[k] = tc::pack_bf16(acc[2 * k], acc[2 * k + 1]);
-    const uint4 lo4 = make_uint4(pk[0], pk[1], pk[2], pk[3]), hi4 = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-    // the same block multiplies the hi half and the lo half of Bdn
-    row[(jl * kRank) / 8] = lo4;
-    row[(jl * kRank) / 8 + 1] = hi4;
-    row[(KRP + jl * kRank) / 8] = lo4;
-    row[(KRP + jl * kRank) / 8 + 1] = hi4;
   }
+  uint32_t pk[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) pk[k] = tc::pack_bf16(acc[2 * k], acc[2 * k + 1]);
+  const uint4 lo4 = make_uint4(pk[0], pk[1], pk[2], pk[3]), hi4 = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  uint4* row = reinterpret_cast<uint4*>(Vt + (size_t)i * 2 * KRP);
+  row[(jb * kRank) / 8] = lo4;
+  row[(jb * kRank) / 8 + 1] = hi4;
+  row[(KRP + jb * kRank) / 8] = lo4;
+  row[(KRP + jb * kRank) / 8 + 1] = hi4;
 }
 
 // ------------------------------------------------------------------------------------------
@@ -734,17 +853,29 @@ bool tc_path_ok(const LayerArgs& a) {
 
 int tc_krp(const LayerArgs& a) { return ((a.K * a.r + 63) / 64) * 64; }
 
+// Number of d_ff chunks per row tile.  Row tiles are only known on the device, so the host
+// estimates them (full tiles plus about half a partial tile per group, or one tile per group
+// when groups hold fewer than 128 rows) and picks the chunk count whose waves of one CTA per SM
+// cost least: ceil(CTAs / SMs) x (tiles per chunk + a fixed per-CTA overhead of half a tile).
 int tc_up_chunks(const LayerArgs& a) {
   const int n_ft = a.f / kNf;
-  const int tiles = (a.R + kTile - 1) / kTile + 1;
-  int want = (2 * 148 + tiles - 1) / tiles;
-  if (want < 1) want = 1;
-  if (want > n_ft) want = n_ft;
-  const int per = (n_ft + want - 1) / want;
-  return (n_ft + per - 1) / per;
+  const int full = (a.R + kTile - 1) / kTile;
+  int tiles = a.R >= kTile * a.G ? full + (a.G + 1) / 2 : (a.R < a.G ? a.R : a.G);
+  if (tiles < 1) tiles = 1;
+  const int sms = 148;
+  int best = 1;
+  double best_cost = 1e30;
+  for (int c = 1; c <= n_ft; ++c) {
+    const int per = (n_ft + c - 1) / c;
+    if (c > 1 && (n_ft + per - 1) / per != c) continue;     // same split as a smaller count
+    const double waves = (double)((tiles * c + sms - 1) / sms);
+    const double cost = waves * (per + 0.5);
+    if (cost < best_cost - 1e-9) { best_cost = cost; best = c; }
+  }
+  return best;
 }
 
-template <int BN, bool OUT_F32>
+template <int BN, int OUT>
 static cudaError_t launch_gemm(const CUtensorMap& A0, const CUtensorMap& A1, const CUtensorMap& B0,
                                const CUtensorMap& B1, int nk0, int nk1, const int32_t* row_begin, int G,
                                int n_out, int b_stride, int b1_off, int tiles, void* out, int out_ld,
@@ -753,12 +884,12 @@ static cudaError_t launch_gemm(const CUtensorMap& A0, const CUtensorMap& A1, con
   const size_t smem = 1024 + (size_t)STAGES * (kTile * 128 + BN * 128);
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = set_smem(tc_gemm_kernel<BN, STAGES, OUT_F32>, smem);
+    cudaError_t e = set_smem(tc_gemm_kernel<BN, STAGES, OUT>, smem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   dim3 grid(n_out / BN, tiles);
-  tc_gemm_kernel<BN, STAGES, OUT_F32><<<grid, 192, smem, stream>>>(A0, A1, B0, B1, nk0, nk1, row_begin, G,
+  tc_gemm_kernel<BN, STAGES, OUT><<<grid, 192, smem, stream>>>(A0, A1, B0, B1, nk0, nk1, row_begin, G,
                                                                   b_stride, b1_off, out, out_ld, scatter, st);
   return cudaGetLastError();
 }
@@ -766,17 +897,18 @@ static cudaError_t launch_gemm(const CUtensorMap& A0, const CUtensorMap& A1, con
 template <int KRP, int KE>
 static cudaError_t launch_up_ke(const CUtensorMap* maps, const UpArgs& p, int nchunks, int tiles, cudaStream_t stream) {
   constexpr int STAGES = KRP >= 128 ? 3 : 4;
-  const size_t smem = 1024 + (size_t)STAGES * (kTile * 128 + 2 * kNf * 128) + 2 * (KRP * kNf * 2) + KRP * 128 +
-                      2 * (kTile * KRP * 2) + kTile * 128;
+  constexpr int RBUF = KRP >= 128 ? 1 : 2;
+  const size_t smem = 1024 + (size_t)STAGES * (kTile * 128 + 2 * kNf * 128) +
+                      (size_t)RBUF * (2 * (KRP * kNf * 2) + KRP * 128) + 2 * (kTile * KRP * 2) + kTile * 128;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = set_smem(ffn_up_tc_kernel<KRP, STAGES, KE>, smem);
+    cudaError_t e = set_smem(ffn_up_tc_kernel<KRP, STAGES, KE, RBUF>, smem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   dim3 grid(nchunks, tiles);
-  ffn_up_tc_kernel<KRP, STAGES, KE><<<grid, kUpWarps * 32, smem, stream>>>(maps[0], maps[1], maps[2], maps[3],
-                                                                          maps[4], maps[5], p);
+  ffn_up_tc_kernel<KRP, STAGES, KE, RBUF><<<grid, kUpWarps * 32, smem, stream>>>(maps[0], maps[1], maps[2],
+                                                                               maps[3], maps[4], maps[5], p);
   return cudaGetLastError();
 }
 
@@ -828,11 +960,11 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   ok = ok && make_map(&mWd, wd, (uint64_t)G * d, f, BN2) && make_map(&mBd, b.Bdn, (uint64_t)G * d, 2 * KRP, BN2);
   if (!ok) return cudaErrorInvalidValue;
 
-  // 3. U = X (Ain_hi + Ain_lo)^T in FP32: the hi stack is at rows g*4*KRP, the lo stack 2*KRP later
+  // 3. U = X (Ain_hi + Ain_lo)^T (FP32 accumulation, FP16 out): the hi stack is at rows g*4*KRP, the lo stack 2*KRP later
   e = (2 * KRP == 256)
-          ? launch_gemm<256, true>(mX, mX, mAhi, mAlo, d / 64, d / 64, row_begin, G, 2 * KRP, 4 * KRP, 2 * KRP,
+          ? launch_gemm<256, kOutF16>(mX, mX, mAhi, mAlo, d / 64, d / 64, row_begin, G, 2 * KRP, 4 * KRP, 2 * KRP,
                                    tiles, b.U, 2 * KRP, nullptr, status, st)
-          : launch_gemm<128, true>(mX, mX, mAhi, mAlo, d / 64, d / 64, row_begin, G, 2 * KRP, 4 * KRP, 2 * KRP,
+          : launch_gemm<128, kOutF16>(mX, mX, mAhi, mAlo, d / 64, d / 64, row_begin, G, 2 * KRP, 4 * KRP, 2 * KRP,
                                    tiles, b.U, 2 * KRP, nullptr, status, st);
   prof_mark("u_gemm", st);
   if (e != cudaSuccess) return e;
@@ -840,7 +972,7 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   // 4. fused gate/up
   UpArgs p;
   p.row_begin = row_begin; p.row_asg = row_asg; p.eidx = eidx; p.gate = gate; p.U = b.U; p.hsum = b.hsum;
-  p.sBg = rp.B[0].scales; p.sBu = rp.B[1].scales; p.sAd = rp.A[2].scales;
+  p.sAd = rp.A[2].scales;
   p.Vpart = b.Vpart; p.status = status; p.tab = a.tab; p.G = G; p.d = d; p.f = f; p.kg = a.kg; p.ke = a.ke;
   p.R = R; p.n_ftiles = f / kNf;
   const int nchunks = tc_up_chunks(a);
@@ -851,14 +983,14 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   if (e != cudaSuccess) return e;
 
   // 5. V~
-  v_reduce_kernel<<<(R + 127) / 128, 128, 0, st>>>(b.Vpart, row_asg, eidx, a.tab, R, a.kg, a.ke, nchunks, KRP, b.Vt);
+  v_reduce_kernel<<<(R * (KRP / kRank) + 255) / 256, 256, 0, st>>>(b.Vpart, row_asg, eidx, a.tab, R, a.kg, a.ke, nchunks, KRP, b.Vt);
   prof_mark("v_reduce", st);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   // 6. Y = [hsum | V~] [Wd | Bdn]^T, rows to their token slot
-  e = BN2 == 256 ? launch_gemm<256, false>(mH, mVt, mWd, mBd, f / 64, 2 * KRP / 64, row_begin, G, d, d, 0,
+  e = BN2 == 256 ? launch_gemm<256, kOutBf16>(mH, mVt, mWd, mBd, f / 64, 2 * KRP / 64, row_begin, G, d, d, 0,
                                            tiles, y_rows, d, row_asg, status, st)
-                 : launch_gemm<128, false>(mH, mVt, mWd, mBd, f / 64, 2 * KRP / 64, row_begin, G, d, d, 0,
+                 : launch_gemm<128, kOutBf16>(mH, mVt, mWd, mBd, f / 64, 2 * KRP / 64, row_begin, G, d, d, 0,
                                            tiles, y_rows, d, row_asg, status, st);
   prof_mark("ffn_down_tc", st);
   return e;

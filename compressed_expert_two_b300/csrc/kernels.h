@@ -61,8 +61,10 @@ cudaError_t launch_ffn_simt(const LayerArgs& a, const void* x, const void* wg, c
                             void* y_rows, const FfnBufs& b, cudaStream_t st);
 
 struct TcBufs {
-  __nv_bfloat16 *X, *Ain, *Bgs, *Bus, *Adn, *Bdn;
-  float* U;
+  __nv_bfloat16 *X, *Ain;
+  __half *Bgs, *Bus;
+  __nv_bfloat16 *Adn, *Bdn;
+  __half* U;
   __nv_bfloat16 *hsum, *Vt;
   float* Vpart;
 };
