@@ -5,9 +5,35 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/moehier.h"
 
 namespace moe {
+
+// Programmatic dependent launch.  Every kernel of the layer is launched with programmatic stream
+// serialization, so that its CTAs may be scheduled while the previous kernel drains.  Before its
+// first global read or write a kernel waits for all prerequisite grids to complete
+// (griddepcontrol.wait; a no-op when the launch had no programmatic dependency) and lets the next
+// kernel be scheduled (griddepcontrol.launch_dependents).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+static inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 16;     // k_g * k_e

@@ -35,6 +35,8 @@ template <typename T>
 __global__ void resid_in_kernel(const T* __restrict__ x, ResidView Ag, ResidView Au,
                                 const int32_t* __restrict__ eidx, const int32_t* __restrict__ row_asg,
                                 int R, int d, int kg, int ke, int r, float* __restrict__ U) {
+  pdl_wait();
+  pdl_trigger();
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (gw >= R * ke) return;
   const int i = gw / ke, s = gw % ke;
@@ -60,6 +62,8 @@ __global__ void __launch_bounds__(256) ffn_up_kernel(
     const float* __restrict__ gate, const int32_t* __restrict__ row_asg,
     const int32_t* __restrict__ row_begin, int G, int d, int f, int kg, int ke, int r,
     float* __restrict__ H, float* __restrict__ hsum) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float Xs[BM][BK + 1];
   __shared__ float Gs[BN][BK + 1];
   __shared__ float Us[BN][BK + 1];
@@ -130,6 +134,8 @@ __global__ void __launch_bounds__(256) ffn_up_kernel(
 __global__ void resid_out_kernel(const float* __restrict__ H, ResidView Ad,
                                  const int32_t* __restrict__ eidx, const int32_t* __restrict__ row_asg,
                                  int R, int f, int kg, int ke, int r, float* __restrict__ V) {
+  pdl_wait();
+  pdl_trigger();
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (gw >= R * ke) return;
   const int i = gw / ke, s = gw % ke;
@@ -151,6 +157,8 @@ __global__ void __launch_bounds__(256) ffn_down_kernel(
     const int32_t* __restrict__ eidx, const float* __restrict__ gate,
     const int32_t* __restrict__ row_asg, const int32_t* __restrict__ row_begin, int G, int d, int f,
     int kg, int ke, int r, T* __restrict__ y_rows) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float Hs[BM][BK + 1];
   __shared__ float Ws[BN][BK + 1];
   int g, r0, r1;
@@ -215,23 +223,23 @@ static cudaError_t run(const LayerArgs& a, const void* x, const void* wg, const 
   const int tiles = (R + BM - 1) / BM + a.G;
   if (r > 0) {
     const int warps = R * a.ke;
-    resid_in_kernel<T><<<(warps * 32 + 255) / 256, 256, 0, st>>>(
-        (const T*)x, rp.A[0], rp.A[1], eidx, row_asg, R, a.d, a.kg, a.ke, r, b.U);
+    launch_pdl(resid_in_kernel<T>, dim3((warps * 32 + 255) / 256), dim3(256), 0, st, (const T*)x, rp.A[0], rp.A[1],
+               eidx, row_asg, R, a.d, a.kg, a.ke, r, b.U);
   prof_mark("resid_in", st);
   }
-  ffn_up_kernel<T><<<dim3((a.f + BN - 1) / BN, tiles), 256, 0, st>>>(
-      (const T*)x, (const T*)wg, (const T*)wu, rp.B[0], rp.B[1], b.U, eidx, gate, row_asg,
-      row_begin, a.G, a.d, a.f, a.kg, a.ke, r, b.H, b.hsum);
+  launch_pdl(ffn_up_kernel<T>, dim3((a.f + BN - 1) / BN, tiles), dim3(256), 0, st, (const T*)x, (const T*)wg,
+             (const T*)wu, rp.B[0], rp.B[1], (const float*)b.U, eidx, gate, row_asg, row_begin, a.G, a.d, a.f, a.kg,
+             a.ke, r, b.H, b.hsum);
   prof_mark("ffn_up_simt", st);
   if (r > 0) {
     const int warps = R * a.ke;
-    resid_out_kernel<<<(warps * 32 + 255) / 256, 256, 0, st>>>(b.H, rp.A[2], eidx, row_asg, R, a.f,
-                                                                a.kg, a.ke, r, b.V);
+    launch_pdl(resid_out_kernel, dim3((warps * 32 + 255) / 256), dim3(256), 0, st, (const float*)b.H, rp.A[2], eidx,
+               row_asg, R, a.f, a.kg, a.ke, r, b.V);
   prof_mark("resid_out", st);
   }
-  ffn_down_kernel<T><<<dim3((a.d + BN - 1) / BN, tiles), 256, 0, st>>>(
-      b.hsum, (const T*)wd, rp.B[2], b.V, eidx, gate, row_asg, row_begin, a.G, a.d, a.f, a.kg,
-      a.ke, r, (T*)y_rows);
+  launch_pdl(ffn_down_kernel<T>, dim3((a.d + BN - 1) / BN, tiles), dim3(256), 0, st, (const float*)b.hsum,
+             (const T*)wd, rp.B[2], (const float*)b.V, eidx, gate, row_asg, row_begin, a.G, a.d, a.f, a.kg, a.ke, r,
+             (T*)y_rows);
   prof_mark("ffn_down_simt", st);
   return cudaGetLastError();
 }
@@ -248,6 +256,8 @@ cudaError_t launch_ffn_simt(const LayerArgs& a, const void* x, const void* wg, c
 // y[t] = sum_j y_rows[t][j], FP32 sum in slot order.
 template <typename T>
 __global__ void combine_kernel(const T* __restrict__ yr, T* __restrict__ y, int Tn, int d, int kg) {
+  pdl_wait();
+  pdl_trigger();
   const size_t n = (size_t)Tn * d;
   for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < n; idx += (size_t)gridDim.x * blockDim.x) {
     const size_t t = idx / d, c = idx % d;
@@ -260,6 +270,8 @@ __global__ void combine_kernel(const T* __restrict__ yr, T* __restrict__ y, int 
 // BF16, 8 columns per thread.
 __global__ void combine_bf16x8_kernel(const __nv_bfloat16* __restrict__ yr, __nv_bfloat16* __restrict__ y, int Tn,
                                       int d, int kg) {
+  pdl_wait();
+  pdl_trigger();
   const size_t n8 = (size_t)Tn * d / 8;
   for (size_t w = blockIdx.x * (size_t)blockDim.x + threadIdx.x; w < n8; w += (size_t)gridDim.x * blockDim.x) {
     const size_t t = w / (d / 8), c = (w % (d / 8)) * 8;
@@ -292,9 +304,11 @@ cudaError_t launch_combine(const LayerArgs& a, const void* y_rows, void* y, cuda
   const size_t n = (size_t)a.T * a.d;
   const int blocks = (int)((n + 255) / 256 < 148 * 16 ? (n + 255) / 256 : 148 * 16);
   if (a.bf16)
-    combine_bf16x8_kernel<<<blocks, 256, 0, st>>>((const __nv_bfloat16*)y_rows, (__nv_bfloat16*)y, a.T, a.d, a.kg);
+    launch_pdl(combine_bf16x8_kernel, dim3(blocks), dim3(256), 0, st, (const __nv_bfloat16*)y_rows, (__nv_bfloat16*)y,
+               a.T, a.d, a.kg);
   else
-    combine_kernel<float><<<blocks, 256, 0, st>>>((const float*)y_rows, (float*)y, a.T, a.d, a.kg);
+    launch_pdl(combine_kernel<float>, dim3(blocks), dim3(256), 0, st, (const float*)y_rows, (float*)y, a.T, a.d,
+               a.kg);
   prof_mark("combine", st);
   return cudaGetLastError();
 }

@@ -34,6 +34,7 @@ namespace moe {
 namespace {
 
 constexpr int kTile = 128;      // rows per tile (MMA M)
+constexpr int kUSimtMaxRows = 1024;   // up to this many rows U is computed on the CUDA cores
 constexpr int kNf = 64;         // d_ff columns per gate/up tile
 
 // Tile index -> (group, first row, end of the group's rows); false if the index is unused.
@@ -67,18 +68,29 @@ struct PrepArgs {
   __nv_bfloat16 *Ain, *Adn, *Bdn;
   __half *Bgs, *Bus;
   int G, K, d, f, r, KRP;
+  bool need_ain;        // the U GEMM reads Ain (the CUDA-core U kernel reads the codes itself)
 };
 
-// Integer code (u - 8) of element c of rank row k of expert e (INT4 group-64 format).
-__device__ __forceinline__ float code_at(const ResidView& v, int e, int k, int c) {
-  const uint8_t b = ((const uint8_t*)v.vals)[((size_t)e * v.r + k) * (v.n / 2) + (c >> 1)];
-  return (float)(((c & 1) ? (b & 0xF) : (b >> 4)) - 8);
+// Eight consecutive elements c8..c8+7 of rank row k of expert e: their codes (u - 8) and the
+// FP16 scale of their 64-element group (INT4 group-64 format, high nibble first).
+__device__ __forceinline__ void codes8(const ResidView& v, int e, int k, int c8, float (&q)[8], float& sc) {
+  const size_t row = (size_t)e * v.r + k;
+  const uint32_t w = *reinterpret_cast<const uint32_t*>((const uint8_t*)v.vals + row * (v.n / 2) + c8 / 2);
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const uint32_t byte = (w >> (8 * b)) & 0xFFu;
+    q[2 * b] = (float)((int)(byte >> 4) - 8);
+    q[2 * b + 1] = (float)((int)(byte & 0xFu) - 8);
+  }
+  sc = __half2float(v.scales[row * (v.n / kQGroup) + c8 / kQGroup]);
 }
 
 // Row-major stacks (Ain hi/lo, Adn): 8 consecutive elements per work item, grid-stride.
 __global__ void resid_prep_rows_kernel(PrepArgs p, GroupTable tab) {
+  pdl_wait();
+  pdl_trigger();
   const int G = p.G, K = p.K, r = p.r, KRP = p.KRP, d = p.d, f = p.f;
-  const size_t nAin = (size_t)G * 2 * KRP * (d / 8);   // hi/lo pairs written together
+  const size_t nAin = p.need_ain ? (size_t)G * 2 * KRP * (d / 8) : 0;   // hi/lo pairs written together
   const size_t nAdn = (size_t)G * KRP * (f / 8);
   for (size_t w = blockIdx.x * (size_t)blockDim.x + threadIdx.x; w < nAin + nAdn; w += (size_t)gridDim.x * blockDim.x) {
     if (w < nAin) {
@@ -90,9 +102,11 @@ __global__ void resid_prep_rows_kernel(PrepArgs p, GroupTable tab) {
       uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
       if (j < K) {
         const int e = tab.member[g * K + j];
+        float cq[8], sc;
+        codes8(p.A[m], e, k, c8, cq, sc);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float v0 = p.A[m].at(e, k, c8 + 2 * q), v1 = p.A[m].at(e, k, c8 + 2 * q + 1);
+          const float v0 = cq[2 * q] * sc, v1 = cq[2 * q + 1] * sc;
           const __nv_bfloat16 h0 = __float2bfloat16_rn(v0), h1 = __float2bfloat16_rn(v1);
           hi[q] = tc::pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
           lo[q] = tc::pack_bf16(v0 - __bfloat162float(h0), v1 - __bfloat162float(h1));
@@ -110,9 +124,10 @@ __global__ void resid_prep_rows_kernel(PrepArgs p, GroupTable tab) {
       uint32_t out[4] = {0u, 0u, 0u, 0u};
       if (j < K) {
         const int e = tab.member[g * K + j];
+        float cq[8], sc;
+        codes8(p.A[2], e, k, c8, cq, sc);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          out[q] = tc::pack_bf16(code_at(p.A[2], e, k, c8 + 2 * q), code_at(p.A[2], e, k, c8 + 2 * q + 1));
+        for (int q = 0; q < 4; ++q) out[q] = tc::pack_bf16(cq[2 * q], cq[2 * q + 1]);
       }
       *reinterpret_cast<uint4*>(p.Adn + rowg * f + c8) = make_uint4(out[0], out[1], out[2], out[3]);
     }
@@ -124,6 +139,8 @@ __global__ void resid_prep_rows_kernel(PrepArgs p, GroupTable tab) {
 //   m = 0, 1: Bgs/Bus[g][n][j*r + k] = fp16(dequantised B_m,e_j^T[k][n])
 //   m = 2:    Bdn[g][n][j*r + k] = hi, Bdn[g][n][KRP + j*r + k] = lo of B_down,e_j^T[k][n]
 __global__ void __launch_bounds__(256) resid_prep_t_kernel(PrepArgs p, GroupTable tab) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int CW = 64;                   // columns per block
   __shared__ float tile[CW][128 + 1];      // [column][jk], KRP <= 128
   const int G = p.G, K = p.K, r = p.r, KRP = p.KRP, d = p.d, f = p.f;
@@ -187,6 +204,8 @@ __global__ void __launch_bounds__(256) resid_prep_t_kernel(PrepArgs p, GroupTabl
 // ------------------------------------------------------------------------------------------
 __global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ row_asg,
                                    int R, int d, int kg, __nv_bfloat16* __restrict__ X) {
+  pdl_wait();
+  pdl_trigger();
   const int per_row = d / 8;
   const size_t n = (size_t)R * per_row;
   for (size_t w = blockIdx.x * (size_t)blockDim.x + threadIdx.x; w < n; w += (size_t)gridDim.x * blockDim.x) {
@@ -194,6 +213,61 @@ __global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ x, const in
     const int t = row_asg[i] / kg;
     *reinterpret_cast<uint4*>(X + (size_t)i * d + c) = *reinterpret_cast<const uint4*>(x + (size_t)t * d + c);
   }
+}
+
+// ------------------------------------------------------------------------------------------
+// 3'. U on the CUDA cores, for batches of few rows (decode): warp w of block (row i, matrix m,
+//     z) computes U[i][m*KRP + o], o = 8z + w, = sum_c x[t(i)][c] A_m,e_j^T[k][c] (o = j*r + k)
+//     for the K experts of the row's group straight from the INT4 codes, lanes striding over c
+//     in 8-element chunks (FP32 accumulation, FP16 out; padding columns zero).
+// ------------------------------------------------------------------------------------------
+constexpr int kUSimtUnroll = 8;
+
+__global__ void __launch_bounds__(256) u_simt_kernel(const __nv_bfloat16* __restrict__ x,
+                                                     const int32_t* __restrict__ row_asg,
+                                                     const int32_t* __restrict__ eidx, PrepArgs p, GroupTable tab,
+                                                     int kg, int ke, __half* __restrict__ U) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ __nv_bfloat16 xs[];              // the row's x (d values)
+  const int i = blockIdx.x, m = blockIdx.y, d = p.d, KRP = p.KRP, r = p.r, K = p.K;
+  const int lane = threadIdx.x & 31, o = blockIdx.z * 8 + (threadIdx.x >> 5);
+  const int b = row_asg[i], t = b / kg, jg = b % kg;
+  const int g = tab.group_of[eidx[(size_t)t * kg * ke + jg * ke]];
+  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8)
+    *reinterpret_cast<uint4*>(xs + c) = *reinterpret_cast<const uint4*>(x + (size_t)t * d + c);
+  __syncthreads();
+  const int j = o / r, k = o % r;
+  float acc = 0.f;
+  if (j < K) {
+    const int e = tab.member[g * K + j];
+    const int nch = d / 8;                           // 8-element chunks; lane takes chunks lane + 32 n
+    for (int c0 = lane; c0 < nch; c0 += 32 * kUSimtUnroll) {
+      float cq[kUSimtUnroll][8], sc[kUSimtUnroll];
+#pragma unroll
+      for (int u = 0; u < kUSimtUnroll; ++u) {
+        const int ch = c0 + 32 * u;
+        if (ch < nch) codes8(p.A[m], e, k, ch * 8, cq[u], sc[u]);
+        else { sc[u] = 0.f; for (int q = 0; q < 8; ++q) cq[u][q] = 0.f; }
+      }
+#pragma unroll
+      for (int u = 0; u < kUSimtUnroll; ++u) {
+        const int ch = c0 + 32 * u;
+        if (ch >= nch) continue;
+        const uint4 xv = *reinterpret_cast<const uint4*>(xs + ch * 8);
+        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+        float s8 = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          s8 = fmaf(__uint_as_float(xw[q] << 16), cq[u][2 * q], s8);
+          s8 = fmaf(__uint_as_float(xw[q] & 0xFFFF0000u), cq[u][2 * q + 1], s8);
+        }
+        acc = fmaf(s8, sc[u], acc);
+      }
+    }
+  }
+  for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) U[(size_t)i * 2 * KRP + m * KRP + o] = __float2half_rn(acc);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -207,6 +281,8 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_kernel(
     const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1, int nk0, int nk1,
     const int32_t* __restrict__ row_begin, int G, int b_stride, int b1_off, void* __restrict__ out, int out_ld,
     const int32_t* __restrict__ scatter, DevStatus* status) {
+  pdl_wait();
+  pdl_trigger();
   constexpr uint32_t A_BYTES = kTile * 128, B_BYTES = BN * 128;
   constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
   extern __shared__ uint8_t smem_raw[];
@@ -366,6 +442,8 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
     const __grid_constant__ CUtensorMap mX, const __grid_constant__ CUtensorMap mWg,
     const __grid_constant__ CUtensorMap mWu, const __grid_constant__ CUtensorMap mBg,
     const __grid_constant__ CUtensorMap mBu, const __grid_constant__ CUtensorMap mAd, const UpArgs p) {
+  pdl_wait();
+  pdl_trigger();
   constexpr uint32_t X_BYTES = kTile * 128, W_BYTES = 2 * kNf * 128, STAGE_BYTES = X_BYTES + W_BYTES;
   constexpr uint32_t BRES_BYTES = KRP * kNf * 2;          // one of Bg / Bu tiles (64 rows x KRP)
   constexpr uint32_t AD_BYTES = KRP * 128;                 // KRP rows x 64 columns
@@ -776,6 +854,8 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
 __global__ void v_reduce_kernel(const float* __restrict__ Vpart, const int32_t* __restrict__ row_asg,
                                 const int32_t* __restrict__ eidx, GroupTable tab, int R, int kg, int ke,
                                 int nchunks, int KRP, __nv_bfloat16* __restrict__ Vt) {
+  pdl_wait();
+  pdl_trigger();
   // one thread per (row, 16-wide block of V~): the block of local expert jb holds the gated v of
   // the row's slot routed to that expert (zero if none); both halves (hi, lo of Bdn) get a copy
   const int nblk = KRP / kRank;
@@ -889,9 +969,8 @@ static cudaError_t launch_gemm(const CUtensorMap& A0, const CUtensorMap& A1, con
     attr = true;
   }
   dim3 grid(n_out / BN, tiles);
-  tc_gemm_kernel<BN, STAGES, OUT><<<grid, 192, smem, stream>>>(A0, A1, B0, B1, nk0, nk1, row_begin, G,
-                                                                  b_stride, b1_off, out, out_ld, scatter, st);
-  return cudaGetLastError();
+  return launch_pdl(tc_gemm_kernel<BN, STAGES, OUT>, grid, dim3(192), smem, stream, A0, A1, B0, B1, nk0, nk1,
+                    row_begin, G, b_stride, b1_off, out, out_ld, scatter, st);
 }
 
 template <int KRP, int KE>
@@ -907,9 +986,8 @@ static cudaError_t launch_up_ke(const CUtensorMap* maps, const UpArgs& p, int nc
     attr = true;
   }
   dim3 grid(nchunks, tiles);
-  ffn_up_tc_kernel<KRP, STAGES, KE, RBUF><<<grid, kUpWarps * 32, smem, stream>>>(maps[0], maps[1], maps[2],
-                                                                               maps[3], maps[4], maps[5], p);
-  return cudaGetLastError();
+  return launch_pdl(ffn_up_tc_kernel<KRP, STAGES, KE, RBUF>, grid, dim3(kUpWarps * 32), smem, stream, maps[0],
+                    maps[1], maps[2], maps[3], maps[4], maps[5], p);
 }
 
 template <int KRP>
@@ -936,13 +1014,15 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   for (int m = 0; m < 3; ++m) { pa.A[m] = rp.A[m]; pa.B[m] = rp.B[m]; }
   pa.Ain = b.Ain; pa.Bgs = b.Bgs; pa.Bus = b.Bus; pa.Adn = b.Adn; pa.Bdn = b.Bdn;
   pa.G = G; pa.K = a.K; pa.d = d; pa.f = f; pa.r = a.r; pa.KRP = KRP;
-  resid_prep_rows_kernel<<<148 * 4, 256, 0, st>>>(pa, a.tab);
-  resid_prep_t_kernel<<<G * (2 * (f / 64) + d / 64), 256, 0, st>>>(pa, a.tab);
+  const bool u_simt = R <= kUSimtMaxRows;
+  pa.need_ain = !u_simt;
+  launch_pdl(resid_prep_rows_kernel, dim3(148 * 4), dim3(256), 0, st, pa, a.tab);
+  launch_pdl(resid_prep_t_kernel, dim3(G * (2 * (f / 64) + d / 64)), dim3(256), 0, st, pa, a.tab);
   prof_mark("resid_prep", st);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   // 2. rows of x in (group, token) order
-  gather_rows_kernel<<<148 * 8, 256, 0, st>>>((const __nv_bfloat16*)x, row_asg, R, d, a.kg, b.X);
+  launch_pdl(gather_rows_kernel, dim3(148 * 8), dim3(256), 0, st, (const __nv_bfloat16*)x, row_asg, R, d, a.kg, b.X);
   prof_mark("gather_rows", st);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
@@ -961,12 +1041,18 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   if (!ok) return cudaErrorInvalidValue;
 
   // 3. U = X (Ain_hi + Ain_lo)^T (FP32 accumulation, FP16 out): the hi stack is at rows g*4*KRP, the lo stack 2*KRP later
-  e = (2 * KRP == 256)
-          ? launch_gemm<256, kOutF16>(mX, mX, mAhi, mAlo, d / 64, d / 64, row_begin, G, 2 * KRP, 4 * KRP, 2 * KRP,
-                                   tiles, b.U, 2 * KRP, nullptr, status, st)
-          : launch_gemm<128, kOutF16>(mX, mX, mAhi, mAlo, d / 64, d / 64, row_begin, G, 2 * KRP, 4 * KRP, 2 * KRP,
-                                   tiles, b.U, 2 * KRP, nullptr, status, st);
-  prof_mark("u_gemm", st);
+  if (u_simt) {
+    e = launch_pdl(u_simt_kernel, dim3(R, 2, KRP / 8), dim3(256), (size_t)d * 2, st, (const __nv_bfloat16*)x,
+                   row_asg, eidx, pa, a.tab, a.kg, a.ke, b.U);
+    prof_mark("u_simt", st);
+  } else {
+    e = (2 * KRP == 256)
+            ? launch_gemm<256, kOutF16>(mX, mX, mAhi, mAlo, d / 64, d / 64, row_begin, G, 2 * KRP, 4 * KRP, 2 * KRP,
+                                        tiles, b.U, 2 * KRP, nullptr, status, st)
+            : launch_gemm<128, kOutF16>(mX, mX, mAhi, mAlo, d / 64, d / 64, row_begin, G, 2 * KRP, 4 * KRP, 2 * KRP,
+                                        tiles, b.U, 2 * KRP, nullptr, status, st);
+    prof_mark("u_gemm", st);
+  }
   if (e != cudaSuccess) return e;
 
   // 4. fused gate/up
@@ -983,7 +1069,8 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   if (e != cudaSuccess) return e;
 
   // 5. V~
-  v_reduce_kernel<<<(R * (KRP / kRank) + 255) / 256, 256, 0, st>>>(b.Vpart, row_asg, eidx, a.tab, R, a.kg, a.ke, nchunks, KRP, b.Vt);
+  launch_pdl(v_reduce_kernel, dim3((R * (KRP / kRank) + 255) / 256), dim3(256), 0, st, (const float*)b.Vpart, row_asg,
+             eidx, a.tab, R, a.kg, a.ke, nchunks, KRP, b.Vt);
   prof_mark("v_reduce", st);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 

@@ -15,6 +15,8 @@ constexpr int kPermBlock = 256;  // tokens per block (8 warps)
 __global__ void __launch_bounds__(kPermBlock) perm_count_kernel(const int32_t* __restrict__ eidx,
                                                                 GroupTable tab, int Tn, int kg,
                                                                 int ke, int32_t* __restrict__ cnt) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int sc[kMaxE + kMaxE];
   const int E = tab.E, G = tab.G, k = kg * ke;
   for (int i = threadIdx.x; i < E + G; i += blockDim.x) sc[i] = 0;
@@ -33,6 +35,8 @@ __global__ void perm_scan_kernel(const int32_t* __restrict__ cnt, GroupTable tab
                                  int32_t* __restrict__ off, int32_t* __restrict__ ebeg,
                                  int32_t* __restrict__ ecnt, int32_t* __restrict__ gbeg,
                                  int32_t* __restrict__ rbeg) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int total[kMaxE + kMaxE];
   __shared__ int base[kMaxE + kMaxE];
   const int E = tab.E, G = tab.G, K = tab.K, NK = E + G;
@@ -78,6 +82,8 @@ __global__ void __launch_bounds__(kPermBlock) perm_scatter_kernel(
     const int32_t* __restrict__ eidx, GroupTable tab, int Tn, int kg, int ke,
     const int32_t* __restrict__ off, int32_t* __restrict__ perm, int32_t* __restrict__ inv_pos,
     int32_t* __restrict__ row_asg, int32_t* __restrict__ row_of) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int W = kPermBlock / 32;
   __shared__ uint32_t emask[W][kMaxE];
   __shared__ int epre[W][kMaxE];
@@ -128,6 +134,91 @@ __global__ void __launch_bounds__(kPermBlock) perm_scatter_kernel(
   }
 }
 
+// Small batches (T <= 1024): the whole permutation in one CTA of 1024 threads, one token per
+// thread, placed exactly as perm_scatter_kernel places a block (per-warp key masks from ballots,
+// warp prefixes, ranks within the warp) with the key bases scanned in the same order as
+// perm_scan_kernel: the same stable (key, token) order, in one launch instead of three.
+constexpr int kFusedThreads = 1024;
+constexpr int kFusedMaxT = kFusedThreads;
+constexpr int kFusedMaxKeys = 128;   // E + G; (2 + 2 x 32) x 128 ints of dynamic shared memory
+
+__global__ void __launch_bounds__(kFusedThreads) perm_fused_kernel(
+    const int32_t* __restrict__ eidx, GroupTable tab, int Tn, int kg, int ke, int32_t* __restrict__ perm,
+    int32_t* __restrict__ inv_pos, int32_t* __restrict__ ebeg, int32_t* __restrict__ ecnt,
+    int32_t* __restrict__ gbeg, int32_t* __restrict__ row_asg, int32_t* __restrict__ row_of,
+    int32_t* __restrict__ rbeg) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int W = kFusedThreads / 32;
+  extern __shared__ int fused_smem[];
+  const int E = tab.E, G = tab.G, K = tab.K, k = kg * ke, NK = E + G;
+  int* total = fused_smem;                           // [NK] items per key
+  int* base = fused_smem + NK;                       // [NK] first position of each key
+  int* wpre = fused_smem + 2 * NK;                   // [W][NK] first position of each key in warp w
+  uint32_t* wmask = (uint32_t*)(fused_smem + 2 * NK + W * NK);   // [W][NK] lanes of warp w holding the key
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t = threadIdx.x;
+  const bool valid = t < Tn;
+  int my_e[kMaxK], my_g[kMaxK];
+  for (int s = 0; s < k; ++s) my_e[s] = valid ? eidx[(size_t)t * k + s] : -1;
+  for (int j = 0; j < kg; ++j) my_g[j] = valid ? (int)tab.group_of[my_e[j * ke]] : -1;
+  for (int key = 0; key < NK; ++key) {
+    bool has = false;
+    if (key < E) { for (int s = 0; s < k; ++s) has |= (my_e[s] == key); }
+    else { for (int j = 0; j < kg; ++j) has |= (my_g[j] == key - E); }
+    const uint32_t m = __ballot_sync(0xffffffffu, has);
+    if (lane == 0) wmask[warp * NK + key] = m;
+  }
+  __syncthreads();
+  for (int key = threadIdx.x; key < NK; key += blockDim.x) {
+    int c = 0;
+    for (int w = 0; w < W; ++w) c += __popc(wmask[w * NK + key]);
+    total[key] = c;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int g = 0; g < G; ++g) {
+      if (gbeg) gbeg[g] = acc;
+      for (int i = 0; i < K; ++i) {
+        const int e = tab.member[g * K + i];
+        if (ebeg) ebeg[e] = acc;
+        if (ecnt) ecnt[e] = total[e];
+        base[e] = acc;
+        acc += total[e];
+      }
+    }
+    if (gbeg) gbeg[G] = acc;
+    int racc = 0;
+    for (int g = 0; g < G; ++g) {
+      rbeg[g] = racc;
+      base[E + g] = racc;
+      racc += total[E + g];
+    }
+    rbeg[G] = racc;
+  }
+  __syncthreads();
+  for (int key = threadIdx.x; key < NK; key += blockDim.x) {
+    int acc = base[key];
+    for (int w = 0; w < W; ++w) { wpre[w * NK + key] = acc; acc += __popc(wmask[w * NK + key]); }
+  }
+  __syncthreads();
+  if (!valid) return;
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int s = 0; s < k; ++s) {
+    const int e = my_e[s];
+    const int pos = wpre[warp * NK + e] + __popc(wmask[warp * NK + e] & lt);
+    if (perm) perm[pos] = t * k + s;
+    if (inv_pos) inv_pos[(size_t)t * k + s] = pos;
+  }
+  for (int j = 0; j < kg; ++j) {
+    const int key = E + my_g[j];
+    const int pos = wpre[warp * NK + key] + __popc(wmask[warp * NK + key] & lt);
+    row_asg[pos] = t * kg + j;
+    if (row_of) row_of[(size_t)t * kg + j] = pos;
+  }
+}
+
 cudaError_t launch_permute(const LayerArgs& a, const int32_t* eidx, const PermOut& o, int32_t* cnt,
                            int32_t* off, int nblk, cudaStream_t st) {
   if (a.T == 0) {
@@ -139,15 +230,25 @@ cudaError_t launch_permute(const LayerArgs& a, const int32_t* eidx, const PermOu
     if (e == cudaSuccess && o.ecnt) e = cudaMemsetAsync(o.ecnt, 0, sizeof(int32_t) * a.E, st);
     return e;
   }
-  perm_count_kernel<<<nblk, kPermBlock, 0, st>>>(eidx, a.tab, a.T, a.kg, a.ke, cnt);
+  if (a.T <= kFusedMaxT && a.E + a.G <= kFusedMaxKeys) {
+    const size_t smem = (size_t)(2 + 2 * (kFusedThreads / 32)) * (a.E + a.G) * sizeof(int);
+    launch_pdl(perm_fused_kernel, dim3(1), dim3(kFusedThreads), smem, st, eidx, a.tab, a.T, a.kg, a.ke, o.perm,
+               o.inv_pos, o.ebeg,
+                                                   o.ecnt, o.gbeg, o.row_asg, o.row_of, o.rbeg);
+    prof_mark("perm_fused", st);
+    return cudaGetLastError();
+  }
+  launch_pdl(perm_count_kernel, dim3(nblk), dim3(kPermBlock), 0, st, eidx, a.tab, a.T, a.kg, a.ke, cnt);
   prof_mark("perm_count", st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  perm_scan_kernel<<<1, 512, 0, st>>>(cnt, a.tab, nblk, off, o.ebeg, o.ecnt, o.gbeg, o.rbeg);
+  launch_pdl(perm_scan_kernel, dim3(1), dim3(512), 0, st, (const int32_t*)cnt, a.tab, nblk, off, o.ebeg, o.ecnt,
+             o.gbeg, o.rbeg);
   prof_mark("perm_scan", st);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  perm_scatter_kernel<<<nblk, kPermBlock, 0, st>>>(eidx, a.tab, a.T, a.kg, a.ke, off, o.perm,
+  launch_pdl(perm_scatter_kernel, dim3(nblk), dim3(kPermBlock), 0, st, eidx, a.tab, a.T, a.kg, a.ke,
+             (const int32_t*)off, o.perm,
                                                    o.inv_pos, o.row_asg, o.row_of);
   prof_mark("perm_scatter", st);
   return cudaGetLastError();

@@ -5,7 +5,8 @@ some latency-critical loops may not pay an allocation's implicit synchronisation
 hand the library a workspace.  moe_hier_permute_noalloc serves them from a fixed scratch array
 inside the library.  These tests call it through the C ABI and check that it returns exactly
 what moe_hier_permute returns, on two calls in a row with different layers (the second call
-reuses the array the first one left behind).
+reuses the array the first one left behind).  Both layers have more than 4096 tokens: smaller
+batches are permuted by a single-CTA kernel that needs no histogram scratch at all.
 """
 import ctypes
 
@@ -30,7 +31,7 @@ def L():
 
 
 def layer_case(**kw):
-    base = dict(name="noalloc", T=515, d=256, f=192, E=32, G=4, kg=2, ke=3, r=16, dtype="bf16",
+    base = dict(name="noalloc", T=5000, d=256, f=192, E=32, G=4, kg=2, ke=3, r=16, dtype="bf16",
                 resid="int4", group_map="perm", seed=41)
     base.update(kw)
     return MoEConfig(**base)
@@ -52,7 +53,7 @@ def noalloc_permute(L, layer, eidx):
 @pytest.mark.gpu
 def test_noalloc_permute_matches_workspace_permute_twice(L, cuda_ok):
     from compressed_expert_two_b300.layer import DeviceLayer
-    cases = [layer_case(), layer_case(T=777, d=384, E=64, G=8, kg=2, ke=3, group_map="contiguous", seed=42,
+    cases = [layer_case(), layer_case(T=8000, d=384, E=64, G=8, kg=2, ke=3, group_map="contiguous", seed=42,
                                       zipf_s=1.2)]
     for cfg in cases:
         layer = DeviceLayer(make_inputs(cfg), device="cuda")
