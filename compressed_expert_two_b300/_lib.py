@@ -33,12 +33,15 @@ class MoeHierResid(ctypes.Structure):
 
 EXPORTS = ["moe_hier_workspace_size", "moe_hier_route", "moe_hier_permute", "moe_hier_ffn",
            "moe_hier_combine", "moe_hier_forward", "moe_hier_get_status", "moe_hier_status_string",
-           "moe_hier_profile_begin", "moe_hier_profile_end"]
+           "moe_hier_last_cuda_error", "moe_hier_profile_begin", "moe_hier_profile_end"]
 
 
 class MoeError(RuntimeError):
     def __init__(self, fn: str, code: int):
-        super().__init__(f"{fn} failed: {code} ({status_string(code)})")
+        detail = status_string(code)
+        if code == MOE_ERR_CUDA:
+            detail += ": " + lib.moe_hier_last_cuda_error().decode()
+        super().__init__(f"{fn} failed: {code} ({detail})")
         self.code = code
 
 
@@ -61,8 +64,10 @@ def _load() -> ctypes.CDLL:
     lib.moe_hier_profile_end.argtypes = [ctypes.POINTER(ctypes.c_char_p), I]
     lib.moe_hier_status_string.argtypes = [I]
     lib.moe_hier_status_string.restype = ctypes.c_char_p
+    lib.moe_hier_last_cuda_error.argtypes = []
+    lib.moe_hier_last_cuda_error.restype = ctypes.c_char_p
     for name in EXPORTS:
-        if name not in ("moe_hier_workspace_size", "moe_hier_status_string"):
+        if name not in ("moe_hier_workspace_size", "moe_hier_status_string", "moe_hier_last_cuda_error"):
             getattr(lib, name).restype = I
     return lib
 

@@ -159,7 +159,14 @@ static cudaError_t run_ffn(const LayerArgs& a, const Plan& p, void* ws, const vo
   return launch_ffn_simt(a, x, wg, wu, wd, resid_ptrs(a, resid), eidx, gate, row_asg, row_begin, y_rows, b, s);
 }
 
-static int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+// The last CUDA error a call of this host thread returned as MOE_ERR_CUDA.
+static thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+static int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  g_last_cuda_error = e;
+  return MOE_ERR_CUDA;
+}
 
 }  // namespace moe
 
@@ -294,6 +301,10 @@ int moe_hier_profile_end(const char** names, int max_names) {
   g_prof_ev = nullptr;
   g_prof_n = g_prof_i = g_prof_launches = 0;
   return n;
+}
+
+const char* moe_hier_last_cuda_error(void) {
+  return g_last_cuda_error == cudaSuccess ? "no error" : cudaGetErrorString(g_last_cuda_error);
 }
 
 const char* moe_hier_status_string(int status) {

@@ -393,6 +393,150 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_kernel(
 }
 
 // ------------------------------------------------------------------------------------------
+// 3/6 (pairs). The same grouped GEMM on CTA pairs: the two CTAs of a cluster take two 128-row
+//      tiles of one group (pair P covers the group's tiles 2P and 2P + 1; the second may lie past
+//      the group's end and then only feeds the pair) and one MMA of M = 256 x N = BN, issued by
+//      rank 0, reads each CTA's A rows and B half (BN/2 rows) from its own shared memory.  Both
+//      CTAs' TMA loads complete on rank 0's stage barrier; rank 0's commits arrive on both CTAs'
+//      barriers.  Per SM a K step lands 16 KB of A and BN/2 x 128 B of B.
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ bool pair_tile_of(const int32_t* row_begin, int G, int P, int m, int& g, int& r0, int& r1) {
+  for (int gg = 0; gg < G; ++gg) {
+    const int b = row_begin[gg], e = row_begin[gg + 1];
+    const int np = ((e - b + kTile - 1) / kTile + 1) / 2;
+    if (P < np) {
+      g = gg;
+      r0 = b + (2 * P + m) * kTile;
+      r1 = e;
+      return true;
+    }
+    P -= np;
+  }
+  return false;
+}
+
+template <int BN, int STAGES, int OUT>
+__global__ void __launch_bounds__(192, 1) tc_gemm_pair_kernel(
+    const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
+    const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1, int nk0, int nk1,
+    const int32_t* __restrict__ row_begin, int G, int b_stride, int b1_off, void* __restrict__ out, int out_ld,
+    const int32_t* __restrict__ scatter, DevStatus* status) {
+  constexpr int BH = BN / 2;                                  // B rows held by each CTA
+  constexpr uint32_t A_BYTES = kTile * 128, B_BYTES = BH * 128, STAGE_BYTES = A_BYTES + B_BYTES;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full[STAGES], empty[STAGES], acc_full;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+  pdl_wait();
+  pdl_trigger();
+
+  const uint32_t rank = tc::cluster_rank();
+  int g, r0, r1;
+  if (!pair_tile_of(row_begin, G, blockIdx.x >> 1, (int)rank, g, r0, r1)) return;   // same for both CTAs
+  const int n0 = blockIdx.y * BN;
+  uint8_t* smem = align1024(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const tc::Abort ab{&abort_flag, status};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) { tc::bar_init(&full[s], 1); tc::bar_init(&empty[s], 1); }
+    tc::bar_init(&acc_full, 1);
+    abort_flag = 0;
+    tc::bar_fence_init();
+  }
+  if (warp == 1) tc::tmem_alloc_pair(&tmem_base, BN);
+  tc::fence_before();
+  // both CTAs' barriers are initialised before either CTA signals the other's
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  tc::fence_after();
+  const uint32_t tmem = tmem_base;
+  const int nk = nk0 + nk1;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer (both CTAs): own A rows and own half of B, counted on rank 0
+    tc::prefetch_map(&mA0); tc::prefetch_map(&mB0);
+    if (nk1) { tc::prefetch_map(&mA1); tc::prefetch_map(&mB1); }
+    const uint32_t full0 = tc::map_shared(tc::smem_u32(&full[0]), 0);
+    bool ok = true;
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % STAGES, it = kb / STAGES;
+      if (kb >= STAGES && !tc::bar_wait_cluster(&empty[s], (it - 1) & 1, ab, 41)) { ok = false; break; }
+      if (rank == 0) tc::bar_expect_tx(&full[s], 2 * STAGE_BYTES);
+      const bool first = kb < nk0;
+      const int kx = (first ? kb : kb - nk0) * 64;
+      uint8_t* st = smem + s * STAGE_BYTES;
+      tc::tma_load_2d_pair(st, first ? &mA0 : &mA1, full0 + 8 * s, kx, r0);
+      tc::tma_load_2d_pair(st + A_BYTES, first ? &mB0 : &mB1, full0 + 8 * s, kx,
+                           g * b_stride + (first ? 0 : b1_off) + n0 + (int)rank * BH);
+    }
+    // every commit rank 0 sends to this CTA's stage barriers has landed before the CTA exits
+    if (ok) {
+      for (int s = 0; s < STAGES && s < nk; ++s)
+        if (!tc::bar_wait_cluster(&empty[s], ((nk - 1 - s) / STAGES) & 1, ab, 42)) break;
+    }
+    if (abort_flag) tc::drain_copies();
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    // ---------------- MMA issuer (rank 0)
+    constexpr uint32_t idesc = tc::idesc_bf16(2 * kTile, BN);
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % STAGES, it = kb / STAGES;
+      if (!tc::bar_wait_cluster(&full[s], it & 1, ab, 43)) break;
+      tc::fence_after();
+      const uint32_t a0 = tc::smem_u32(smem + s * STAGE_BYTES), b0 = a0 + A_BYTES;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        tc::mma_bf16_pair(tmem, tc::sdesc(a0 + 32 * k), tc::sdesc(b0 + 32 * k), idesc, (kb | k) != 0);
+      tc::mma_commit_pair(&empty[s], 3);
+    }
+    tc::mma_commit_pair(&acc_full, 3);
+  } else if (warp >= 2) {
+    // ---------------- epilogue (both CTAs): this CTA's 128 rows, all BN columns
+    const int q = warp & 3, row = q * 32 + lane, i = r0 + row;
+    if (tc::bar_wait_cluster(&acc_full, 0, ab, 44) && !abort_flag) {
+      tc::fence_after();
+      const bool valid = i < r1;
+      const size_t orow = valid ? (size_t)(scatter ? scatter[i] : i) : 0;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 16) {
+        uint32_t v[16];
+        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c, v);
+        tc::tmem_ld_wait();
+        if (valid) {
+          if constexpr (OUT == kOutF32) {
+            uint4* d4 = reinterpret_cast<uint4*>((float*)out + orow * out_ld + n0 + c);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d4[e] = make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+          } else if constexpr (OUT == kOutF16) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              __half2 h2 = __floats2half2_rn(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+              pk[e] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            uint4* d4 = reinterpret_cast<uint4*>((__half*)out + orow * out_ld + n0 + c);
+            d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          } else {
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) pk[e] = tc::pack_bf16(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+            uint4* d4 = reinterpret_cast<uint4*>((__nv_bfloat16*)out + orow * out_ld + n0 + c);
+            d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
+        }
+      }
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after();
+    tc::tmem_dealloc_pair(tmem, BN);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
 // 4. Fused gate/up tile: base once, per-slot residual, SwiGLU, gated sum, down-residual partials
 //
 // One CTA owns a 128-row tile of one group and a chunk of 64-column d_ff tiles.  Warp roles
@@ -973,6 +1117,26 @@ static cudaError_t launch_gemm(const CUtensorMap& A0, const CUtensorMap& A1, con
                     row_begin, G, b_stride, b1_off, out, out_ld, scatter, st);
 }
 
+// CTA-pair version: grid.x = 2 x (an upper bound of the row-tile pairs), clusters of two CTAs
+// along x (the pair of a cta_group::2 MMA is formed along x), grid.y = N tiles of BN.
+template <int BN, int OUT>
+static cudaError_t launch_gemm_pair(const CUtensorMap& A0, const CUtensorMap& A1, const CUtensorMap& B0,
+                                    const CUtensorMap& B1, int nk0, int nk1, const int32_t* row_begin, int G,
+                                    int n_out, int b_stride, int b1_off, int pairs, void* out, int out_ld,
+                                    const int32_t* scatter, DevStatus* st, cudaStream_t stream) {
+  constexpr int STAGES = BN >= 256 ? 6 : 8;
+  const size_t smem = 1024 + (size_t)STAGES * (kTile * 128 + (BN / 2) * 128);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = set_smem(tc_gemm_pair_kernel<BN, STAGES, OUT>, smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  return launch_pdl_cluster(tc_gemm_pair_kernel<BN, STAGES, OUT>, dim3(2 * pairs, n_out / BN), dim3(192),
+                            dim3(2, 1, 1), smem, stream, A0, A1, B0, B1, nk0, nk1, row_begin, G, b_stride, b1_off,
+                            out, out_ld, scatter, st);
+}
+
 template <int KRP, int KE>
 static cudaError_t launch_up_ke(const CUtensorMap* maps, const UpArgs& p, int nchunks, int tiles, cudaStream_t stream) {
   constexpr int STAGES = KRP >= 128 ? 3 : 4;
@@ -1029,14 +1193,19 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   CUtensorMap mX, mAhi, mAlo, mWg, mWu, mBg, mBu, mAd, mH, mVt, mWd, mBd;
   const uint64_t Rp = R < kTile ? kTile : R;   // row buffers hold at least one full tile
   // Ain is [G][2 (hi, lo)][2*KRP][d]: rows g*4*KRP + n (hi) and g*4*KRP + 2*KRP + n (lo)
+  // pair GEMMs: each CTA of a pair holds half of the B tile
+  const int pairs = (R + 2 * kTile - 1) / (2 * kTile) + G;
+  // The pair form pays a cluster handshake per CTA; it gains only on long K loops over many rows
+  // (on short ones, or one-wave decode batches, the single-CTA form is faster).
+  const bool down_pair = d % 256 == 0 && f >= 4096 && R >= 2048;
   bool ok = make_map(&mX, b.X, Rp, d, kTile) &&
-            make_map(&mAhi, b.Ain, (uint64_t)G * 4 * KRP, d, 2 * KRP) &&
+            make_map(&mAhi, b.Ain, (uint64_t)G * 4 * KRP, d, KRP) &&
             make_map(&mWg, wg, (uint64_t)G * f, d, kNf) && make_map(&mWu, wu, (uint64_t)G * f, d, kNf) &&
             make_map(&mBg, b.Bgs, (uint64_t)G * f, KRP, kNf) && make_map(&mBu, b.Bus, (uint64_t)G * f, KRP, kNf) &&
             make_map(&mAd, b.Adn, (uint64_t)G * KRP, f, KRP) && make_map(&mH, b.hsum, Rp, f, kTile) &&
             make_map(&mVt, b.Vt, Rp, 2 * KRP, kTile);
   mAlo = mAhi;
-  const int BN2 = d % 256 == 0 ? 256 : 128;
+  const int BN2 = down_pair ? 128 : (d % 256 == 0 ? 256 : 128);   // B box rows: half of N = 256 for pairs
   ok = ok && make_map(&mWd, wd, (uint64_t)G * d, f, BN2) && make_map(&mBd, b.Bdn, (uint64_t)G * d, 2 * KRP, BN2);
   if (!ok) return cudaErrorInvalidValue;
 
@@ -1047,10 +1216,10 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
     prof_mark("u_simt", st);
   } else {
     e = (2 * KRP == 256)
-            ? launch_gemm<256, kOutF16>(mX, mX, mAhi, mAlo, d / 64, d / 64, row_begin, G, 2 * KRP, 4 * KRP, 2 * KRP,
-                                        tiles, b.U, 2 * KRP, nullptr, status, st)
-            : launch_gemm<128, kOutF16>(mX, mX, mAhi, mAlo, d / 64, d / 64, row_begin, G, 2 * KRP, 4 * KRP, 2 * KRP,
-                                        tiles, b.U, 2 * KRP, nullptr, status, st);
+            ? launch_gemm_pair<256, kOutF16>(mX, mX, mAhi, mAlo, d / 64, d / 64, row_begin, G, 2 * KRP, 4 * KRP,
+                                             2 * KRP, pairs, b.U, 2 * KRP, nullptr, status, st)
+            : launch_gemm_pair<128, kOutF16>(mX, mX, mAhi, mAlo, d / 64, d / 64, row_begin, G, 2 * KRP, 4 * KRP,
+                                             2 * KRP, pairs, b.U, 2 * KRP, nullptr, status, st);
     prof_mark("u_gemm", st);
   }
   if (e != cudaSuccess) return e;
@@ -1075,10 +1244,12 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   // 6. Y = [hsum | V~] [Wd | Bdn]^T, rows to their token slot
-  e = BN2 == 256 ? launch_gemm<256, kOutBf16>(mH, mVt, mWd, mBd, f / 64, 2 * KRP / 64, row_begin, G, d, d, 0,
-                                           tiles, y_rows, d, row_asg, status, st)
-                 : launch_gemm<128, kOutBf16>(mH, mVt, mWd, mBd, f / 64, 2 * KRP / 64, row_begin, G, d, d, 0,
-                                           tiles, y_rows, d, row_asg, status, st);
+  e = down_pair ? launch_gemm_pair<256, kOutBf16>(mH, mVt, mWd, mBd, f / 64, 2 * KRP / 64, row_begin, G, d, d, 0,
+                                                  pairs, y_rows, d, row_asg, status, st)
+                : (BN2 == 256 ? launch_gemm<256, kOutBf16>(mH, mVt, mWd, mBd, f / 64, 2 * KRP / 64, row_begin, G, d,
+                                                           d, 0, tiles, y_rows, d, row_asg, status, st)
+                              : launch_gemm<128, kOutBf16>(mH, mVt, mWd, mBd, f / 64, 2 * KRP / 64, row_begin, G, d,
+                                                           d, 0, tiles, y_rows, d, row_asg, status, st));
   prof_mark("ffn_down_tc", st);
   return e;
 }

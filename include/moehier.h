@@ -145,6 +145,10 @@ int moe_hier_get_status(const void* ws, void* stream);
 /* Static text for a moe_status value. */
 const char* moe_hier_status_string(int status);
 
+/* Static text of the last CUDA error that an entry point called on this host thread reported as
+ * MOE_ERR_CUDA ("no error" if none).  A diagnostic aid without a counterpart in the pages. */
+const char* moe_hier_last_cuda_error(void);
+
 /* Profiling aid (the pages have no counterpart; it changes no result).  After
  * moe_hier_profile_begin(events, n), the entry points called on this host thread record
  * events[0] on their stream before their first kernel and events[i] right after their i-th
