@@ -69,6 +69,7 @@ struct PrepArgs {
   __half *Bgs, *Bus;
   int G, K, d, f, r, KRP;
   bool need_ain;        // the U GEMM reads Ain (the CUDA-core U kernel reads the codes itself)
+  bool adn_f16;         // Adn holds FP16 dequantised values (else BF16 codes, scaled later)
 };
 
 // Eight consecutive elements c8..c8+7 of rank row k of expert e: their codes (u - 8) and the
@@ -127,7 +128,14 @@ __global__ void resid_prep_rows_kernel(PrepArgs p, GroupTable tab) {
         float cq[8], sc;
         codes8(p.A[2], e, k, c8, cq, sc);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) out[q] = tc::pack_bf16(cq[2 * q], cq[2 * q + 1]);
+        for (int q = 0; q < 4; ++q) {
+          if (p.adn_f16) {
+            __half2 h2 = __floats2half2_rn(cq[2 * q] * sc, cq[2 * q + 1] * sc);
+            out[q] = *reinterpret_cast<uint32_t*>(&h2);
+          } else {
+            out[q] = tc::pack_bf16(cq[2 * q], cq[2 * q + 1]);
+          }
+        }
       }
       *reinterpret_cast<uint4*>(p.Adn + rowg * f + c8) = make_uint4(out[0], out[1], out[2], out[3]);
     }
@@ -993,6 +1001,371 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
 }
 
 // ------------------------------------------------------------------------------------------
+// 4b. Fused gate/up on 256-column MMAs (one CTA per 128-row tile and chunk of 128-column d_ff
+//     tiles; for K r = 64 (KRP = 64) and at most two expert slots per row).
+//
+// The accumulator acc = [gate 128 | up 128] of one d_ff tile fills half of TMEM; V_s (the
+// A_down^T h_s of slot s, all K experts' blocks) has KRP columns per slot and accumulates over
+// every tile of the chunk; h_s goes to TMEM as FP16 (two per column, 64 columns, double
+// buffered) where the V MMA reads it as its A operand, with B = A_down^T dequantised to FP16,
+// so no scale is applied afterwards.  acc is single-buffered: the next tile's K loop starts when
+// the epilogue has read acc for the tile's last slot.  Residual deltas as in 4: acc += D_s
+// [B_gate | B_up]^T with D_0 = U~_0, D_s = U~_s - U~_{s-1}.
+// ------------------------------------------------------------------------------------------
+constexpr int kNf3 = 128;                 // d_ff columns per tile
+constexpr int kStages3 = 3;
+
+template <int KE>
+__global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up3_kernel(
+    const __grid_constant__ CUtensorMap mX, const __grid_constant__ CUtensorMap mWg,
+    const __grid_constant__ CUtensorMap mWu, const __grid_constant__ CUtensorMap mBg,
+    const __grid_constant__ CUtensorMap mBu, const __grid_constant__ CUtensorMap mAd, const UpArgs p) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int KRP = 64, NF = kNf3, STAGES = kStages3;
+  constexpr uint32_t X_BYTES = kTile * 128, W_BYTES = 2 * NF * 128, STAGE_BYTES = X_BYTES + W_BYTES;
+  constexpr uint32_t BRES_BYTES = NF * KRP * 2;            // B_gate or B_up tile: 128 rows x KRP
+  constexpr uint32_t AD_BYTES = KRP * NF * 2;              // A_down^T tile: KRP rows x 128 (two 64-column atoms)
+  constexpr uint32_t UT_BYTES = kTile * KRP * 2;
+  constexpr uint32_t COL_V = 2 * NF;                       // V_s at COL_V + s * KRP
+  constexpr uint32_t COL_H = COL_V + KE * KRP;             // h buffers at COL_H + 64 b
+  static_assert(KE >= 1 && KE <= 2 && COL_H + 128 <= 512, "TMEM budget");
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full[STAGES], empty[STAGES];
+  __shared__ uint64_t base_full, acc_empty, rb_full, rb_empty, ad_full, ad_empty;
+  __shared__ uint64_t acc_full, acc_read, u_ready, h_ready, v_done[2], fin1, fin2;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+
+  int g, r0, r1;
+  if (!tile_of(p.row_begin, p.G, blockIdx.y, g, r0, r1)) return;
+  const int chunk = blockIdx.x;
+  const int ft0 = chunk * p.ftiles_per_chunk;
+  const int ft1 = min(ft0 + p.ftiles_per_chunk, p.n_ftiles);
+  if (ft0 >= ft1) return;
+  const int nft = ft1 - ft0;
+  const int nkb = p.d / 64;
+  const int f = p.f;
+
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sStage = smem;
+  uint8_t* sBg = sStage + STAGES * STAGE_BYTES;
+  uint8_t* sBu = sBg + BRES_BYTES;
+  uint8_t* sAd = sBu + BRES_BYTES;
+  uint8_t* sUg = sAd + AD_BYTES;
+  uint8_t* sUu = sUg + UT_BYTES;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const tc::Abort ab{&abort_flag, p.status};
+  constexpr int kEpiArrive = kUpEpi / 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) { tc::bar_init(&full[s], 1); tc::bar_init(&empty[s], 1); }
+    tc::bar_init(&base_full, 1); tc::bar_init(&acc_empty, kEpiArrive);
+    tc::bar_init(&rb_full, 1); tc::bar_init(&rb_empty, 1); tc::bar_init(&ad_full, 1); tc::bar_init(&ad_empty, 1);
+    tc::bar_init(&acc_full, 1);
+    tc::bar_init(&acc_read, kEpiArrive);
+    tc::bar_init(&u_ready, kEpiArrive);
+    tc::bar_init(&h_ready, kEpiArrive);
+    tc::bar_init(&v_done[0], 1); tc::bar_init(&v_done[1], 1);
+    tc::bar_init(&fin1, 1); tc::bar_init(&fin2, 1);
+    abort_flag = 0;
+    tc::bar_fence_init();
+  }
+  if (warp == 1) tc::tmem_alloc(&tmem_base, 512);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = tmem_base;
+  auto warp_arrive = [&](uint64_t* b) {
+    __syncwarp();
+    if (lane == 0) tc::bar_arrive(b);
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer of the base stages (X, W_gate, W_up of one 128-column tile)
+      tc::prefetch_map(&mX); tc::prefetch_map(&mWg); tc::prefetch_map(&mWu);
+      int kc = 0;
+      bool ok = true;
+      for (int lt = 0; lt < nft && ok; ++lt) {
+        const int n0 = (ft0 + lt) * NF;
+        for (int kb = 0; kb < nkb; ++kb, ++kc) {
+          const int s = kc % STAGES, it = kc / STAGES;
+          if (kc >= STAGES && !tc::bar_wait(&empty[s], (it - 1) & 1, ab, 51)) { ok = false; break; }
+          uint8_t* st = sStage + s * STAGE_BYTES;
+          tc::bar_expect_tx(&full[s], STAGE_BYTES);
+          tc::tma_load_2d(st, &mX, &full[s], kb * 64, r0);
+          tc::tma_load_2d(st + X_BYTES, &mWg, &full[s], kb * 64, g * f + n0);
+          tc::tma_load_2d(st + X_BYTES + NF * 128, &mWu, &full[s], kb * 64, g * f + n0);
+        }
+      }
+      if (abort_flag) tc::drain_copies();
+    }
+  } else if (warp == 3) {
+    if (lane == 0) {
+      // ---------------- TMA producer of the residual tiles of each d_ff tile
+      tc::prefetch_map(&mBg); tc::prefetch_map(&mBu); tc::prefetch_map(&mAd);
+      for (int lt = 0; lt < nft; ++lt) {
+        const int n0 = (ft0 + lt) * NF;
+        if (lt > 0 && !tc::bar_wait(&rb_empty, (lt - 1) & 1, ab, 52)) break;
+        tc::bar_expect_tx(&rb_full, 2 * BRES_BYTES);
+        tc::tma_load_2d(sBg, &mBg, &rb_full, 0, g * f + n0);
+        tc::tma_load_2d(sBu, &mBu, &rb_full, 0, g * f + n0);
+        if (lt > 0 && !tc::bar_wait(&ad_empty, (lt - 1) & 1, ab, 53)) break;
+        tc::bar_expect_tx(&ad_full, AD_BYTES);
+        tc::tma_load_2d(sAd, &mAd, &ad_full, n0, g * KRP);
+        tc::tma_load_2d(sAd + KRP * 128, &mAd, &ad_full, n0 + 64, g * KRP);
+      }
+      if (abort_flag) tc::drain_copies();
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- base MMA issuer: acc = X [Wg | Wu]^T, N = 256
+      constexpr uint32_t id_base = tc::idesc_bf16(kTile, 2 * NF);
+      int kc = 0;
+      bool ok = true;
+      for (int lt = 0; lt < nft && ok; ++lt) {
+        if (lt >= 1 && !tc::bar_wait(&acc_empty, (lt - 1) & 1, ab, 54)) break;
+        tc::fence_after();
+        for (int kb = 0; kb < nkb; ++kb, ++kc) {
+          const int s = kc % STAGES, it = kc / STAGES;
+          if (!tc::bar_wait(&full[s], it & 1, ab, 55)) { ok = false; break; }
+          tc::fence_after();
+          const uint32_t a0 = tc::smem_u32(sStage + s * STAGE_BYTES);
+          const uint32_t b0 = a0 + X_BYTES;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tc::mma_bf16(tmem, tc::sdesc(a0 + 32 * k), tc::sdesc(b0 + 32 * k), id_base, (kb | k) != 0);
+          tc::mma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        tc::mma_commit(&base_full);
+      }
+      tc::mma_commit(&fin1);
+      const uint64_t t0 = tc::now_ns();
+      while (!tc::bar_test(&fin1, 0) && tc::now_ns() - t0 < tc::kWaitNs) {}
+    }
+  } else if (warp == 2) {
+    if (lane == 0) {
+      // ---------------- residual issuer: acc += D_s [Bg | Bu]^T; V_s += h_s Adn^T (one slot behind)
+      constexpr uint32_t id_res = tc::idesc_f16(kTile, NF);
+      constexpr uint32_t id_v = tc::idesc_f16(kTile, KRP);
+      const uint32_t ug = tc::smem_u32(sUg), uu = tc::smem_u32(sUu);
+      const uint32_t bg = tc::smem_u32(sBg), bu = tc::smem_u32(sBu), ad = tc::smem_u32(sAd);
+      const int n_slots = nft * KE;
+      auto issue_v = [&](int tau) -> bool {
+        const int lt = tau / KE, s = tau % KE;
+        if (s == 0 && !tc::bar_wait(&ad_full, lt & 1, ab, 56)) return false;
+        if (!tc::bar_wait(&h_ready, tau & 1, ab, 57)) return false;
+        tc::fence_after();
+        const uint32_t hcol = tmem + COL_H + 64 * (tau & 1);
+#pragma unroll
+        for (int kk = 0; kk < NF / 16; ++kk)
+          tc::mma_f16_tmem_a(tmem + COL_V + s * KRP, hcol + 8 * kk,
+                             tc::sdesc(ad + (kk >> 2) * (KRP * 128) + (kk & 3) * 32), id_v, (lt | kk) != 0);
+        tc::mma_commit(&v_done[tau & 1]);
+        if (s == KE - 1) tc::mma_commit(&ad_empty);
+        return true;
+      };
+      bool ok = true;
+      for (int sig = 0; sig < n_slots && ok; ++sig) {
+        const int lt = sig / KE, s = sig % KE;
+        if (sig >= 1 && !issue_v(sig - 1)) { ok = false; break; }
+        if (s == 0) {
+          if (!tc::bar_wait(&base_full, lt & 1, ab, 58)) { ok = false; break; }
+          if (!tc::bar_wait(&rb_full, lt & 1, ab, 59)) { ok = false; break; }
+        }
+        if (!tc::bar_wait(&u_ready, sig & 1, ab, 60)) { ok = false; break; }
+        if (s > 0 && !tc::bar_wait(&acc_read, (sig - 1) & 1, ab, 61)) { ok = false; break; }
+        tc::fence_after();
+#pragma unroll
+        for (int kk = 0; kk < KRP / 16; ++kk) {
+          const uint32_t off_u = (kk & 3) * 32, off_b = (kk & 3) * 32;
+          tc::mma_bf16(tmem, tc::sdesc(ug + off_u), tc::sdesc(bg + off_b), id_res, 1u);
+          tc::mma_bf16(tmem + NF, tc::sdesc(uu + off_u), tc::sdesc(bu + off_b), id_res, 1u);
+        }
+        tc::mma_commit(&acc_full);
+        if (s == KE - 1) tc::mma_commit(&rb_empty);
+      }
+      if (ok && n_slots > 0) issue_v(n_slots - 1);
+      tc::mma_commit(&fin2);
+      const uint64_t t0 = tc::now_ns();
+      while (!tc::bar_test(&fin2, 0) && tc::now_ns() - t0 < tc::kWaitNs) {}
+    }
+  } else {
+    // ---------------- epilogue: one thread per (tile row, column half of 64 d_ff columns)
+    const int q = warp & 3, half = (warp - kUpEpiWarp0) >> 2, row = q * 32 + lane, i = r0 + row;
+    auto ewait = [&](uint64_t* b, uint32_t par, int where) -> bool {
+      const bool r = tc::bar_wait(b, par, ab, where);
+      return __all_sync(0xffffffffu, r);
+    };
+    const bool valid = i < r1;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const int c0 = half * 64;
+    uint8_t* sU = half == 0 ? sUg : sUu;
+    int le[KE], eid[KE];
+    float gt[KE];
+#pragma unroll
+    for (int s = 0; s < KE; ++s) { le[s] = 0; eid[s] = 0; gt[s] = 0.f; }
+    const __half* urow = p.U;
+    if (valid) {
+      const int b = p.row_asg[i], t = b / p.kg, j = b % p.kg, k = p.kg * KE;
+#pragma unroll
+      for (int s = 0; s < KE; ++s) {
+        const int e = p.eidx[(size_t)t * k + j * KE + s];
+        le[s] = p.tab.local_of[e];
+        eid[s] = e;
+        gt[s] = p.gate[(size_t)t * k + j * KE + s];
+      }
+      urow = p.U + (size_t)i * 2 * KRP + half * KRP;
+    }
+    {
+      uint4* z = reinterpret_cast<uint4*>(sU + (row >> 3) * 1024 + (row & 7) * 128);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) z[c] = make_uint4(0, 0, 0, 0);
+    }
+    auto load_u = [&](int s, uint32_t (&pk)[8]) {
+      if (!valid) return;
+      const uint4* u4 = reinterpret_cast<const uint4*>(urow + le[s] * kRank);
+      const uint4 a = u4[0], b = u4[1];
+      pk[0] = a.x; pk[1] = a.y; pk[2] = a.z; pk[3] = a.w;
+      pk[4] = b.x; pk[5] = b.y; pk[6] = b.z; pk[7] = b.w;
+    };
+    auto zero_block = [&](int blk) {
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, blk * kRank, kTile)) = z;
+      *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, blk * kRank + 8, kTile)) = z;
+    };
+    int nz_pos = -1, nz_neg = -1;
+    uint32_t unext[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) unext[c] = 0u;
+    auto build_delta = [&](int s) {
+      if (!valid) return;
+      const int pos = le[s], neg = s > 0 ? le[s - 1] : -1;
+      if (neg >= 0) {
+        uint4* b0 = reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, neg * kRank, kTile));
+        uint4* b1 = reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, neg * kRank + 8, kTile));
+        const uint4 v0 = *b0, v1 = *b1;
+        constexpr uint32_t F = 0x80008000u;          // exact FP16 negation
+        *b0 = make_uint4(v0.x ^ F, v0.y ^ F, v0.z ^ F, v0.w ^ F);
+        *b1 = make_uint4(v1.x ^ F, v1.y ^ F, v1.z ^ F, v1.w ^ F);
+      }
+      if (nz_neg >= 0 && nz_neg != pos && nz_neg != neg) zero_block(nz_neg);
+      if (nz_pos >= 0 && nz_pos != pos && nz_pos != neg) zero_block(nz_pos);
+      *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, pos * kRank, kTile)) =
+          make_uint4(unext[0], unext[1], unext[2], unext[3]);
+      *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, pos * kRank + 8, kTile)) =
+          make_uint4(unext[4], unext[5], unext[6], unext[7]);
+      nz_pos = pos; nz_neg = neg;
+    };
+
+    load_u(0, unext);
+    build_delta(0);
+    tc::fence_async_smem();
+    warp_arrive(&u_ready);
+    if (KE > 1) load_u(KE > 1 ? 1 : 0, unext);
+    else if (nft > 1) load_u(0, unext);
+
+    bool ok = true;
+    int sig = 0;
+    for (int lt = 0; lt < nft && ok; ++lt) {
+      float hs[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) hs[c] = 0.f;
+#pragma unroll
+      for (int s = 0; s < KE; ++s, ++sig) {
+        if (!ewait(&acc_full, sig & 1, 62)) { ok = false; break; }
+        // the h buffer of this slot is free once the V MMA of slot sig - 2 has completed
+        if (sig >= 2 && !ewait(&v_done[sig & 1], ((sig - 2) >> 1) & 1, 63)) { ok = false; break; }
+        tc::fence_after();
+        const uint32_t hbuf = tmem + lane_off + COL_H + 64 * (sig & 1) + c0 / 2;
+#pragma unroll
+        for (int c = 0; c < 64; c += 8) {
+          uint32_t av[8], bv[8];
+          tmem_ld8(tmem + lane_off + c0 + c, av);
+          tmem_ld8(tmem + lane_off + NF + c0 + c, bv);
+          tc::tmem_ld_wait();
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            float h2[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              h2[u] = silu_fast(__uint_as_float(av[e + u])) * __uint_as_float(bv[e + u]);
+              hs[c + e + u] += gt[s] * h2[u];
+            }
+            __half2 hh = __floats2half2_rn(h2[0], h2[1]);
+            pk[e / 2] = *reinterpret_cast<uint32_t*>(&hh);
+          }
+          tc::tmem_st4(hbuf + c / 2, pk[0], pk[1], pk[2], pk[3]);
+        }
+        tc::tmem_st_wait();
+        tc::fence_before();
+        warp_arrive(&acc_read);
+        if (s == KE - 1) warp_arrive(&acc_empty);
+        warp_arrive(&h_ready);
+        const bool more = s + 1 < KE || lt + 1 < nft;
+        if (more) {
+          build_delta(s + 1 < KE ? s + 1 : 0);
+          tc::fence_async_smem();
+          warp_arrive(&u_ready);
+          const int s2 = (s + 2) % KE;
+          const int lt2 = lt + (s + 2) / KE;
+          if (lt2 < nft) load_u(s2, unext);
+        }
+      }
+      if (!ok) break;
+      if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(p.hsum + (size_t)i * f + (ft0 + lt) * NF + c0);
+#pragma unroll
+        for (int c = 0; c < 64; c += 8)
+          dst[c / 8] = make_uint4(tc::pack_bf16(hs[c], hs[c + 1]), tc::pack_bf16(hs[c + 2], hs[c + 3]),
+                                  tc::pack_bf16(hs[c + 4], hs[c + 5]), tc::pack_bf16(hs[c + 6], hs[c + 7]));
+      }
+    }
+    // every V MMA has completed: the last two commits of v_done
+    if (ok && sig >= 1) ok = ewait(&v_done[(sig - 1) & 1], ((sig - 1) >> 1) & 1, 64);
+    if (ok && sig >= 2) ok = ewait(&v_done[(sig - 2) & 1], ((sig - 2) >> 1) & 1, 65);
+    if (ok) {
+      tc::fence_after();
+      // V_s of slot s is read by the half h = s % 2; the row's expert block le[s] of the KRP columns
+#pragma unroll
+      for (int s = 0; s < KE; ++s) {
+        if (half != (s & 1)) continue;
+        float v[kRank];
+#pragma unroll
+        for (int k = 0; k < kRank; ++k) v[k] = 0.f;
+#pragma unroll
+        for (int jb = 0; jb < KRP / 16; ++jb) {
+          uint32_t vv[16];
+          tc::tmem_ld16(tmem + lane_off + COL_V + s * KRP + jb * 16, vv);
+          tc::tmem_ld_wait();
+          if (jb == le[s]) {
+#pragma unroll
+            for (int k = 0; k < kRank; ++k) v[k] = __uint_as_float(vv[k]);
+          }
+        }
+        if (valid) {
+          float* vp = p.Vpart + ((size_t)chunk * p.R + i) * KE * kRank + s * kRank;
+#pragma unroll
+          for (int k = 0; k < kRank; k += 4)
+            *reinterpret_cast<float4*>(vp + k) =
+                make_float4(gt[s] * v[k], gt[s] * v[k + 1], gt[s] * v[k + 2], gt[s] * v[k + 3]);
+        }
+      }
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
 // 5. V~[i][j*16 + k] = sum over column chunks of the gated v of the slot whose expert is local j
 // ------------------------------------------------------------------------------------------
 __global__ void v_reduce_kernel(const float* __restrict__ Vpart, const int32_t* __restrict__ row_asg,
@@ -1081,8 +1454,12 @@ int tc_krp(const LayerArgs& a) { return ((a.K * a.r + 63) / 64) * 64; }
 // estimates them (full tiles plus about half a partial tile per group, or one tile per group
 // when groups hold fewer than 128 rows) and picks the chunk count whose waves of one CTA per SM
 // cost least: ceil(CTAs / SMs) x (tiles per chunk + a fixed per-CTA overhead of half a tile).
+// Which fused gate/up kernel runs: the 256-column one (4b) when K r fits 64 columns, at most
+// two slots and d_ff is a multiple of 128; otherwise the 128-column one (4).
+static bool up3_ok(const LayerArgs& a) { return tc_krp(a) == 64 && a.ke <= 2 && a.f % kNf3 == 0; }
+
 int tc_up_chunks(const LayerArgs& a) {
-  const int n_ft = a.f / kNf;
+  const int n_ft = a.f / (up3_ok(a) ? kNf3 : kNf);
   const int full = (a.R + kTile - 1) / kTile;
   int tiles = a.R >= kTile * a.G ? full + (a.G + 1) / 2 : (a.R < a.G ? a.R : a.G);
   if (tiles < 1) tiles = 1;
@@ -1154,6 +1531,20 @@ static cudaError_t launch_up_ke(const CUtensorMap* maps, const UpArgs& p, int nc
                     maps[1], maps[2], maps[3], maps[4], maps[5], p);
 }
 
+template <int KE>
+static cudaError_t launch_up3(const CUtensorMap* maps, const UpArgs& p, int nchunks, int tiles, cudaStream_t stream) {
+  const size_t smem = 1024 + (size_t)kStages3 * (kTile * 128 + 2 * kNf3 * 128) + 2 * (size_t)(kNf3 * 64 * 2) +
+                      (size_t)64 * kNf3 * 2 + 2 * (size_t)(kTile * 64 * 2);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = set_smem(ffn_up3_kernel<KE>, smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  return launch_pdl(ffn_up3_kernel<KE>, dim3(nchunks, tiles), dim3(kUpWarps * 32), smem, stream, maps[0], maps[1],
+                    maps[2], maps[3], maps[4], maps[5], p);
+}
+
 template <int KRP>
 static cudaError_t launch_up(const CUtensorMap* maps, const UpArgs& p, int nchunks, int tiles, cudaStream_t stream) {
   switch (p.ke) {
@@ -1180,6 +1571,8 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   pa.G = G; pa.K = a.K; pa.d = d; pa.f = f; pa.r = a.r; pa.KRP = KRP;
   const bool u_simt = R <= kUSimtMaxRows;
   pa.need_ain = !u_simt;
+  const bool up3 = up3_ok(a);
+  pa.adn_f16 = up3;
   launch_pdl(resid_prep_rows_kernel, dim3(148 * 4), dim3(256), 0, st, pa, a.tab);
   launch_pdl(resid_prep_t_kernel, dim3(G * (2 * (f / 64) + d / 64)), dim3(256), 0, st, pa, a.tab);
   prof_mark("resid_prep", st);
@@ -1195,13 +1588,14 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   // Ain is [G][2 (hi, lo)][2*KRP][d]: rows g*4*KRP + n (hi) and g*4*KRP + 2*KRP + n (lo)
   // pair GEMMs: each CTA of a pair holds half of the B tile
   const int pairs = (R + 2 * kTile - 1) / (2 * kTile) + G;
+  const int nf_up = up3 ? kNf3 : kNf;
   // The pair form pays a cluster handshake per CTA; it gains only on long K loops over many rows
   // (on short ones, or one-wave decode batches, the single-CTA form is faster).
   const bool down_pair = d % 256 == 0 && f >= 4096 && R >= 2048;
   bool ok = make_map(&mX, b.X, Rp, d, kTile) &&
             make_map(&mAhi, b.Ain, (uint64_t)G * 4 * KRP, d, KRP) &&
-            make_map(&mWg, wg, (uint64_t)G * f, d, kNf) && make_map(&mWu, wu, (uint64_t)G * f, d, kNf) &&
-            make_map(&mBg, b.Bgs, (uint64_t)G * f, KRP, kNf) && make_map(&mBu, b.Bus, (uint64_t)G * f, KRP, kNf) &&
+            make_map(&mWg, wg, (uint64_t)G * f, d, nf_up) && make_map(&mWu, wu, (uint64_t)G * f, d, nf_up) &&
+            make_map(&mBg, b.Bgs, (uint64_t)G * f, KRP, nf_up) && make_map(&mBu, b.Bus, (uint64_t)G * f, KRP, nf_up) &&
             make_map(&mAd, b.Adn, (uint64_t)G * KRP, f, KRP) && make_map(&mH, b.hsum, Rp, f, kTile) &&
             make_map(&mVt, b.Vt, Rp, 2 * KRP, kTile);
   mAlo = mAhi;
@@ -1229,11 +1623,14 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   p.row_begin = row_begin; p.row_asg = row_asg; p.eidx = eidx; p.gate = gate; p.U = b.U; p.hsum = b.hsum;
   p.sAd = rp.A[2].scales;
   p.Vpart = b.Vpart; p.status = status; p.tab = a.tab; p.G = G; p.d = d; p.f = f; p.kg = a.kg; p.ke = a.ke;
-  p.R = R; p.n_ftiles = f / kNf;
+  p.R = R; p.n_ftiles = f / nf_up;
   const int nchunks = tc_up_chunks(a);
   p.ftiles_per_chunk = (p.n_ftiles + nchunks - 1) / nchunks;
   const CUtensorMap maps[6] = {mX, mWg, mWu, mBg, mBu, mAd};
-  e = KRP == 128 ? launch_up<128>(maps, p, nchunks, tiles, st) : launch_up<64>(maps, p, nchunks, tiles, st);
+  if (up3)
+    e = a.ke == 1 ? launch_up3<1>(maps, p, nchunks, tiles, st) : launch_up3<2>(maps, p, nchunks, tiles, st);
+  else
+    e = KRP == 128 ? launch_up<128>(maps, p, nchunks, tiles, st) : launch_up<64>(maps, p, nchunks, tiles, st);
   prof_mark("ffn_up_tc", st);
   if (e != cudaSuccess) return e;
 
