@@ -18,7 +18,7 @@ struct LayerArgs {
 
 // Workspace carving (offsets in bytes from ws; every region 256-byte aligned).
 struct Plan {
-  size_t status, logits, wpair, gidx, eidx, gate;
+  size_t status, logits, gidx, eidx, gate;
   size_t perm, inv_pos, ebeg, ecnt, gbeg, row_asg, row_of, rbeg;
   size_t cnt, off;   // per-block histograms and their exclusive offsets
   int nblk;          // permutation blocks
@@ -37,7 +37,7 @@ void prof_start(cudaStream_t st);
 void prof_mark(const char* kernel_name, cudaStream_t st);
 
 cudaError_t launch_route(const LayerArgs& a, const void* x, const void* wg, const float* bg,
-                         const void* we, float2* wpair, float* logits, int32_t* gidx, int32_t* eidx, float* gate,
+                         const void* we, float* logits, int32_t* gidx, int32_t* eidx, float* gate,
                          cudaStream_t st);
 
 struct PermOut {

@@ -103,105 +103,110 @@ __global__ void __launch_bounds__(WT * WR * 32, MINB) router_logits_bf16_kernel(
     }
 }
 
-// The router rows as FP32 pairs for the paired FMA: wpair[q][c] = (row 2q, row 2q + 1) at element c
-// (rows: the G group rows, then the E expert rows; a missing last row is zero).  BF16 -> FP32 is
-// exact, so the logits below are the same numbers as from the BF16 rows.
-__global__ void router_wpair_kernel(const __nv_bfloat16* __restrict__ wg, const __nv_bfloat16* __restrict__ we,
-                                    float2* __restrict__ wpair, int d, int G, int E) {
-  pdl_wait();
-  pdl_trigger();
-  const int R = G + E, NP = (R + 1) / 2;
-  const size_t n = (size_t)NP * d;
-  for (size_t w = blockIdx.x * (size_t)blockDim.x + threadIdx.x; w < n; w += (size_t)gridDim.x * blockDim.x) {
-    const int q = (int)(w / d), c = (int)(w % d);
-    const int r0 = 2 * q, r1 = 2 * q + 1;
-    const float a = __bfloat162float(r0 < G ? wg[(size_t)r0 * d + c] : we[(size_t)(r0 - G) * d + c]);
-    const float b = r1 < R ? __bfloat162float(r1 < G ? wg[(size_t)r1 * d + c] : we[(size_t)(r1 - G) * d + c]) : 0.f;
-    wpair[w] = make_float2(a, b);
-  }
-}
+// BF16 router logits with the operands staged in shared memory.  A CTA of 8 warps computes 32
+// tokens x 16 router rows (warp (tg, rg): tokens 8 tg.., rows 8 rg..); d streams through a
+// three-stage cp.async pipeline in chunks of 256 elements.  Canonical order as above: lane l adds
+// the products of its elements 128*j + 4*l + u in ascending index (one rounding per product --
+// exact for BF16 x BF16 -- and per add), then the xor butterfly 16, 8, 4, 2, 1.
+constexpr int kRtTok = 32, kRtRows = 16, kRtDC = 256, kRtStages = 3;
 
-// BF16 router logits from row pairs.  Warp (tg, rg) owns TPW tokens x RP row pairs; the CTA is
-// WT x WR warps.  Canonical order as above: lane l adds the products of its elements
-// 128*j + 4*l + u in ascending index (one rounding per product -- exact for BF16 x BF16 -- and per
-// add), then the xor butterfly 16, 8, 4, 2, 1; each paired FMA performs the steps of two rows.
-template <int TPW, int RP, int WT, int WR, int MINB>
-__global__ void __launch_bounds__(WT * WR * 32, MINB) router_logits_pair_kernel(
-    const __nv_bfloat16* __restrict__ x, const float2* __restrict__ wpair, const float* __restrict__ bg,
-    float* __restrict__ logits, int Tn, int d, int G, int E) {
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem)), "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N> __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__global__ void __launch_bounds__(256, 2) router_logits_smem_kernel(
+    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ wg, const float* __restrict__ bg,
+    const __nv_bfloat16* __restrict__ we, float* __restrict__ logits, int Tn, int d, int G, int E) {
   pdl_wait();
   pdl_trigger();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int tg = warp % WT, rg = warp / WT;
-  const int R = G + E, NP = (R + 1) / 2;
-  const int t0 = (blockIdx.x * WT + tg) * TPW;
-  const int q0 = (blockIdx.y * WR + rg) * RP;
-  if (t0 >= Tn || q0 >= NP) return;
-  const uint2* xp[TPW];
-#pragma unroll
-  for (int i = 0; i < TPW; ++i) xp[i] = reinterpret_cast<const uint2*>(x + (size_t)min(t0 + i, Tn - 1) * d) + lane;
-  const float4* wp[RP];
-#pragma unroll
-  for (int q = 0; q < RP; ++q) wp[q] = reinterpret_cast<const float4*>(wpair + (size_t)min(q0 + q, NP - 1) * d) + 2 * lane;
-  float2 acc[TPW][RP];
-#pragma unroll
-  for (int i = 0; i < TPW; ++i)
-#pragma unroll
-    for (int q = 0; q < RP; ++q) acc[i][q] = make_float2(0.f, 0.f);
-  const int nb = d / 128;
-#pragma unroll 2
-  for (int jb = 0; jb < nb; ++jb) {
-    float2 xd[TPW][4];                               // (x, x) for each token and element u
-#pragma unroll
-    for (int i = 0; i < TPW; ++i) {
-      const uint2 v = __ldg(xp[i] + jb * 32);
-      const float e0 = __uint_as_float(v.x << 16), e1 = __uint_as_float(v.x & 0xFFFF0000u);
-      const float e2 = __uint_as_float(v.y << 16), e3 = __uint_as_float(v.y & 0xFFFF0000u);
-      xd[i][0] = make_float2(e0, e0); xd[i][1] = make_float2(e1, e1);
-      xd[i][2] = make_float2(e2, e2); xd[i][3] = make_float2(e3, e3);
+  extern __shared__ __align__(16) uint8_t rt_smem[];   // [stages][32][256] x, then [stages][16][256] w
+  auto xs = reinterpret_cast<__nv_bfloat16 (*)[kRtTok][kRtDC]>(rt_smem);
+  auto ws = reinterpret_cast<__nv_bfloat16 (*)[kRtRows][kRtDC]>(rt_smem + sizeof(__nv_bfloat16) * kRtStages * kRtTok * kRtDC);
+  const int R = G + E;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tg = warp & 3, rg = warp >> 2;
+  const int t_base = blockIdx.x * kRtTok, r_base = blockIdx.y * kRtRows;
+  const int nchunk = (d + kRtDC - 1) / kRtDC;
+  // loader: 16-byte pieces; rows past the batch or the router repeat the last one (results unused)
+  auto load_chunk = [&](int c, int st) {
+    const int cb = c * kRtDC, width = min(kRtDC, d - cb), pieces = width / 8;
+    for (int w = threadIdx.x; w < kRtTok * pieces; w += blockDim.x) {
+      const int rr = w / pieces, pc = (w % pieces) * 8;
+      const int t = min(t_base + rr, Tn - 1);
+      cp_async16(&xs[st][rr][pc], x + (size_t)t * d + cb + pc);
     }
-#pragma unroll
-    for (int q = 0; q < RP; ++q) {
-      const float4 wa = __ldg(wp[q] + jb * 64), wb = __ldg(wp[q] + jb * 64 + 1);
-      const float2 w2[4] = {make_float2(wa.x, wa.y), make_float2(wa.z, wa.w), make_float2(wb.x, wb.y),
-                            make_float2(wb.z, wb.w)};
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int i = 0; i < TPW; ++i) acc[i][q] = fma2(xd[i][u], w2[u], acc[i][q]);
+    for (int w = threadIdx.x; w < kRtRows * pieces; w += blockDim.x) {
+      const int rr = w / pieces, pc = (w % pieces) * 8;
+      const int r = min(r_base + rr, R - 1);
+      const __nv_bfloat16* src = r < G ? wg + (size_t)r * d : we + (size_t)(r - G) * d;
+      cp_async16(&ws[st][rr][pc], src + cb + pc);
     }
+  };
+  float acc[8][8];                                   // [token][row]
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[i][q] = 0.f;
+#pragma unroll
+  for (int c = 0; c < kRtStages - 1; ++c) {
+    if (c < nchunk) load_chunk(c, c);
+    cp_async_commit();
   }
+  for (int c = 0; c < nchunk; ++c) {
+    cp_async_wait<kRtStages - 2>();
+    __syncthreads();
+    const int st = c % kRtStages;
+    const int nj = min(kRtDC, d - c * kRtDC) / 128;
+    for (int jj = 0; jj < nj; ++jj) {
+      uint2 xr[8], wr[8];
 #pragma unroll
-  for (int i = 0; i < TPW; ++i)
+      for (int i = 0; i < 8; ++i) xr[i] = *reinterpret_cast<const uint2*>(&xs[st][tg * 8 + i][jj * 128 + 4 * lane]);
 #pragma unroll
-    for (int q = 0; q < RP; ++q)
+      for (int q = 0; q < 8; ++q) wr[q] = *reinterpret_cast<const uint2*>(&ws[st][rg * 8 + q][jj * 128 + 4 * lane]);
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        acc[i][q].x = __fadd_rn(acc[i][q].x, __shfl_xor_sync(0xffffffffu, acc[i][q].x, o));
-        acc[i][q].y = __fadd_rn(acc[i][q].y, __shfl_xor_sync(0xffffffffu, acc[i][q].y, o));
-      }
+      for (int u = 0; u < 4; ++u) {
+        float xv[8], wv[8];
 #pragma unroll
-  for (int i = 0; i < TPW; ++i)
-#pragma unroll
-    for (int q = 0; q < RP; ++q)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int t = t0 + i, rr = 2 * (q0 + q) + h;
-        if (((i * RP * 2 + q * 2 + h) & 31) == lane && t < Tn && rr < R) {
-          float v = h ? acc[i][q].y : acc[i][q].x;
-          if (rr < G && bg != nullptr) v = __fadd_rn(v, bg[rr]);
-          logits[(size_t)t * R + rr] = v;
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t a = u < 2 ? xr[i].x : xr[i].y;
+          xv[i] = (u & 1) ? __uint_as_float(a & 0xFFFF0000u) : __uint_as_float(a << 16);
         }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t w = u < 2 ? wr[q].x : wr[q].y;
+          wv[q] = (u & 1) ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
+        }
+        // BF16 x BF16 is exact in FP32, so the fused multiply-add rounds once, like mul + add
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[i][q] = __fmaf_rn(xv[i], wv[q], acc[i][q]);
       }
-}
-
-template <int TPW, int RP, int WT, int WR, int MINB>
-static void launch_pair_logits(const void* x, const float2* wpair, const float* bg, float* logits, int Tn, int d,
-                               int G, int E, cudaStream_t st) {
-  const int NP = (G + E + 1) / 2;
-  dim3 grid((Tn + WT * TPW - 1) / (WT * TPW), (NP + WR * RP - 1) / (WR * RP));
-  launch_pdl(router_logits_pair_kernel<TPW, RP, WT, WR, MINB>, grid, dim3(WT * WR * 32), 0, st,
-             (const __nv_bfloat16*)x, (const float2*)wpair, bg, logits, Tn, d, G, E);
+    }
+    // refill the stage computed in the previous iteration (every warp has passed the barrier above)
+    const int cn = c + kRtStages - 1;
+    if (cn < nchunk) load_chunk(cn, cn % kRtStages);
+    cp_async_commit();
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) acc[i][q] = __fadd_rn(acc[i][q], __shfl_xor_sync(0xffffffffu, acc[i][q], o));
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int t = t_base + tg * 8 + i, rr = r_base + rg * 8 + q;
+      if (((i * 8 + q) & 31) == lane && t < Tn && rr < R) {
+        float v = acc[i][q];
+        if (rr < G && bg != nullptr) v = __fadd_rn(v, bg[rr]);
+        logits[(size_t)t * R + rr] = v;
+      }
+    }
 }
 
 // FP32 router logits (same canonical order; products rounded before the add, no contraction).
@@ -335,18 +340,19 @@ static void launch_bf16_logits(const void* x, const void* wg, const float* bg, c
 }
 
 static cudaError_t launch_logits(bool bf16, const void* x, const void* wg, const float* bg, const void* we,
-                                 float2* wpair, float* logits, int Tn, int d, int G, int E, cudaStream_t st) {
-  if (bf16 && Tn >= 1024 && wpair) {
-    // many tokens: FP32 row pairs, 4 tokens x RP row pairs per warp; RP picked to waste the
-    // fewest pairs for this router height
-    const int NP = (G + E + 1) / 2;
-    launch_pdl(router_wpair_kernel, dim3(148 * 2), dim3(256), 0, st, (const __nv_bfloat16*)wg,
-               (const __nv_bfloat16*)we, wpair, d, G, E);
-    prof_mark("router_wpair", st);
-    const int w4 = (NP + 7) / 8 * 8 - NP, w6 = (NP + 11) / 12 * 12 - NP, w8 = (NP + 15) / 16 * 16 - NP;
-    if (w6 < w4 && w6 <= w8) launch_pair_logits<4, 6, 4, 2, 2>(x, wpair, bg, logits, Tn, d, G, E, st);
-    else if (w8 < w4) launch_pair_logits<4, 8, 4, 2, 2>(x, wpair, bg, logits, Tn, d, G, E, st);
-    else launch_pair_logits<4, 4, 4, 2, 2>(x, wpair, bg, logits, Tn, d, G, E, st);
+                                 float* logits, int Tn, int d, int G, int E, cudaStream_t st) {
+  if (bf16 && Tn >= 1024) {
+    dim3 grid((Tn + kRtTok - 1) / kRtTok, (G + E + kRtRows - 1) / kRtRows);
+    constexpr size_t smem = sizeof(__nv_bfloat16) * kRtStages * (kRtTok + kRtRows) * kRtDC;   // 72 KB
+    static bool attr = false;
+    if (!attr) {
+      const cudaError_t e = cudaFuncSetAttribute(router_logits_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+      if (e != cudaSuccess) return e;
+      attr = true;
+    }
+    launch_pdl(router_logits_smem_kernel, grid, dim3(256), smem, st, (const __nv_bfloat16*)x, (const __nv_bfloat16*)wg,
+               bg, (const __nv_bfloat16*)we, logits, Tn, d, G, E);
   } else if (bf16) {
     // few tokens: small warp blocks and a deep unroll so that the loads of many j blocks are in
     // flight at once
@@ -362,10 +368,10 @@ static cudaError_t launch_logits(bool bf16, const void* x, const void* wg, const
 }
 
 cudaError_t launch_route(const LayerArgs& a, const void* x, const void* wg, const float* bg,
-                         const void* we, float2* wpair, float* logits, int32_t* gidx, int32_t* eidx, float* gate,
+                         const void* we, float* logits, int32_t* gidx, int32_t* eidx, float* gate,
                          cudaStream_t st) {
   if (a.T == 0) return cudaSuccess;
-  cudaError_t err = launch_logits(a.bf16, x, wg, bg, we, wpair, logits, a.T, a.d, a.G, a.E, st);
+  cudaError_t err = launch_logits(a.bf16, x, wg, bg, we, logits, a.T, a.d, a.G, a.E, st);
   if (err != cudaSuccess) return err;
   launch_pdl(router_select_kernel, dim3((a.T + 127) / 128), dim3(128), 0, st, (const float*)logits, a.tab, a.T, a.kg,
              a.ke, gidx, eidx, gate);
