@@ -1455,8 +1455,9 @@ int tc_krp(const LayerArgs& a) { return ((a.K * a.r + 63) / 64) * 64; }
 // when groups hold fewer than 128 rows) and picks the chunk count whose waves of one CTA per SM
 // cost least: ceil(CTAs / SMs) x (tiles per chunk + a fixed per-CTA overhead of half a tile).
 // Which fused gate/up kernel runs: the 256-column one (4b) when K r fits 64 columns, at most
-// two slots and d_ff is a multiple of 128; otherwise the 128-column one (4).
-static bool up3_ok(const LayerArgs& a) { return tc_krp(a) == 64 && a.ke <= 2 && a.f % kNf3 == 0; }
+// two slots, d_ff is a multiple of 128 and the K loop (d_model) is long enough to hide its
+// serialised epilogue; otherwise the 128-column one (4), whose epilogue overlaps the next tile.
+static bool up3_ok(const LayerArgs& a) { return tc_krp(a) == 64 && a.ke <= 2 && a.f % kNf3 == 0 && a.d >= 2048; }
 
 int tc_up_chunks(const LayerArgs& a) {
   const int n_ft = a.f / (up3_ok(a) ? kNf3 : kNf);
