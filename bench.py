@@ -83,28 +83,75 @@ def workload_name(cfg) -> str:
 
 # ------------------------------------------------------------------ clocks during the timed region
 class Clocks:
+    """SM clock and clock-event reasons sampled while the timed steps run.
+
+    NVML is polled from a thread (about every 0.5 ms: the timed region can be a few ms); the GPU is
+    found by its UUID because NVML does not follow CUDA_VISIBLE_DEVICES.  Without NVML the
+    nvidia-smi sampler (200 ms) is used instead."""
+    REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40}
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+    def __init__(self, device):
+        import threading
+        self.device = device
+        self.samples = []
+        self.stop_flag = threading.Event()
+        self.thread = None
+        self.handle = None
         self.proc = None
         self.file = None
+        try:
+            import pynvml
+            import torch
+            pynvml.nvmlInit()
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            self.handle = pynvml.nvmlDeviceGetHandleByUUID(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+            self.nvml = pynvml
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.handle, pynvml.NVML_CLOCK_SM)
+        except Exception:
+            self.handle = None
+
+    def _poll(self):
+        nv = self.nvml
+        while not self.stop_flag.is_set():
+            try:
+                mhz = nv.nvmlDeviceGetClockInfo(self.handle, nv.NVML_CLOCK_SM)
+                try:
+                    rs = nv.nvmlDeviceGetCurrentClocksEventReasons(self.handle)
+                except AttributeError:
+                    rs = nv.nvmlDeviceGetCurrentClocksThrottleReasons(self.handle)
+                self.samples.append((mhz, rs))
+            except Exception:
+                pass
+            time.sleep(0.0005)
 
     def start(self):
+        import threading
+        if self.handle is not None:
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
         try:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                ["nvidia-smi", "-i", str(self.device.index or 0), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=self.file, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
     def stop(self):
+        if self.thread is not None:
+            self.stop_flag.set()
+            self.thread.join()
+            sm = [m for m, _ in self.samples]
+            reasons = sorted(n for n, bit in self.REASONS.items() if any(r & bit for _, r in self.samples))
+            return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                    "samples": len(sm), "source": "nvml, polled during the timed steps", "reasons": reasons}
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock source"]}
         time.sleep(0.25)
         self.proc.terminate()
         try:
@@ -130,8 +177,8 @@ class Clocks:
                 if v.lower() == "active":
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "sm_max_mhz": max(smax) if smax else None, "samples": len(sm),
+                "source": "nvidia-smi, 200 ms", "reasons": sorted(reasons)}
 
 
 # ------------------------------------------------------------------ CPU oracle timing (rank 0 only)
@@ -246,17 +293,12 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    gpu_index = local_rank
-    if os.environ.get("CUDA_VISIBLE_DEVICES"):
-        ids = os.environ["CUDA_VISIBLE_DEVICES"].split(",")
-        gpu_index = int(ids[local_rank]) if ids[local_rank].isdigit() else local_rank
-    clocks = Clocks(gpu_index) if rank == 0 else None
+    clocks = Clocks(dev) if rank == 0 else None
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
     if clocks:
         clocks.start()
-        time.sleep(0.3)
     wall0 = time.perf_counter()
     for i in range(K):
         flush.fill_(i & 0xFF)                      # evict the weights from L2 between steps

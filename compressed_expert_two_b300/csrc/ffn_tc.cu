@@ -1014,9 +1014,11 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
 // ------------------------------------------------------------------------------------------
 constexpr int kNf3 = 128;                 // d_ff columns per tile
 constexpr int kStages3 = 3;
+constexpr int kUp3EpiWarps = 16;          // four warps per TMEM lane quarter, 32 d_ff columns each
+constexpr int kUp3Warps = kUpEpiWarp0 + kUp3EpiWarps;
 
 template <int KE>
-__global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up3_kernel(
+__global__ void __launch_bounds__(kUp3Warps * 32, 1) ffn_up3_kernel(
     const __grid_constant__ CUtensorMap mX, const __grid_constant__ CUtensorMap mWg,
     const __grid_constant__ CUtensorMap mWu, const __grid_constant__ CUtensorMap mBg,
     const __grid_constant__ CUtensorMap mBu, const __grid_constant__ CUtensorMap mAd, const UpArgs p) {
@@ -1058,7 +1060,7 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up3_kernel(
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const tc::Abort ab{&abort_flag, p.status};
-  constexpr int kEpiArrive = kUpEpi / 32;
+  constexpr int kEpiArrive = kUp3EpiWarps;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { tc::bar_init(&full[s], 1); tc::bar_init(&empty[s], 1); }
     tc::bar_init(&base_full, 1); tc::bar_init(&acc_empty, kEpiArrive);
@@ -1194,16 +1196,18 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up3_kernel(
       while (!tc::bar_test(&fin2, 0) && tc::now_ns() - t0 < tc::kWaitNs) {}
     }
   } else {
-    // ---------------- epilogue: one thread per (tile row, column half of 64 d_ff columns)
-    const int q = warp & 3, half = (warp - kUpEpiWarp0) >> 2, row = q * 32 + lane, i = r0 + row;
+    // ---------------- epilogue: one thread per (tile row, quarter of 32 d_ff columns)
+    const int q = warp & 3, part = (warp - kUpEpiWarp0) >> 2, row = q * 32 + lane, i = r0 + row;
     auto ewait = [&](uint64_t* b, uint32_t par, int where) -> bool {
       const bool r = tc::bar_wait(b, par, ab, where);
       return __all_sync(0xffffffffu, r);
     };
     const bool valid = i < r1;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    const int c0 = half * 64;
-    uint8_t* sU = half == 0 ? sUg : sUu;
+    const int c0 = part * 32;
+    // parts 0 and 1 keep this row's U~ blocks (gate, up); parts 2 and 3 only compute
+    const bool builds = part < 2;
+    uint8_t* sU = part == 0 ? sUg : sUu;
     int le[KE], eid[KE];
     float gt[KE];
 #pragma unroll
@@ -1218,15 +1222,15 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up3_kernel(
         eid[s] = e;
         gt[s] = p.gate[(size_t)t * k + j * KE + s];
       }
-      urow = p.U + (size_t)i * 2 * KRP + half * KRP;
+      urow = p.U + (size_t)i * 2 * KRP + (part & 1) * KRP;
     }
-    {
+    if (builds) {
       uint4* z = reinterpret_cast<uint4*>(sU + (row >> 3) * 1024 + (row & 7) * 128);
 #pragma unroll
       for (int c = 0; c < 8; ++c) z[c] = make_uint4(0, 0, 0, 0);
     }
     auto load_u = [&](int s, uint32_t (&pk)[8]) {
-      if (!valid) return;
+      if (!valid || !builds) return;
       const uint4* u4 = reinterpret_cast<const uint4*>(urow + le[s] * kRank);
       const uint4 a = u4[0], b = u4[1];
       pk[0] = a.x; pk[1] = a.y; pk[2] = a.z; pk[3] = a.w;
@@ -1242,7 +1246,7 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up3_kernel(
 #pragma unroll
     for (int c = 0; c < 8; ++c) unext[c] = 0u;
     auto build_delta = [&](int s) {
-      if (!valid) return;
+      if (!valid || !builds) return;
       const int pos = le[s], neg = s > 0 ? le[s - 1] : -1;
       if (neg >= 0) {
         uint4* b0 = reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, neg * kRank, kTile));
@@ -1271,9 +1275,9 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up3_kernel(
     bool ok = true;
     int sig = 0;
     for (int lt = 0; lt < nft && ok; ++lt) {
-      float hs[64];
+      float hs[32];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) hs[c] = 0.f;
+      for (int c = 0; c < 32; ++c) hs[c] = 0.f;
 #pragma unroll
       for (int s = 0; s < KE; ++s, ++sig) {
         if (!ewait(&acc_full, sig & 1, 62)) { ok = false; break; }
@@ -1281,30 +1285,36 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up3_kernel(
         if (sig >= 2 && !ewait(&v_done[sig & 1], ((sig - 2) >> 1) & 1, 63)) { ok = false; break; }
         tc::fence_after();
         const uint32_t hbuf = tmem + lane_off + COL_H + 64 * (sig & 1) + c0 / 2;
+        // two batches of 16 columns, one TMEM round trip each; acc is released as soon as the
+        // second batch has been read, so the next slot's residual MMA overlaps the arithmetic
 #pragma unroll
-        for (int c = 0; c < 64; c += 8) {
-          uint32_t av[8], bv[8];
-          tmem_ld8(tmem + lane_off + c0 + c, av);
-          tmem_ld8(tmem + lane_off + NF + c0 + c, bv);
+        for (int bt = 0; bt < 2; ++bt) {
+          uint32_t av[16], bv[16];
+          tc::tmem_ld16(tmem + lane_off + c0 + 16 * bt, av);
+          tc::tmem_ld16(tmem + lane_off + NF + c0 + 16 * bt, bv);
           tc::tmem_ld_wait();
-          uint32_t pk[4];
+          if (bt == 1) {
+            tc::fence_before();
+            warp_arrive(&acc_read);
+            if (s == KE - 1) warp_arrive(&acc_empty);
+          }
+          uint32_t pk[8];
 #pragma unroll
-          for (int e = 0; e < 8; e += 2) {
+          for (int e = 0; e < 16; e += 2) {
             float h2[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
               h2[u] = silu_fast(__uint_as_float(av[e + u])) * __uint_as_float(bv[e + u]);
-              hs[c + e + u] += gt[s] * h2[u];
+              hs[16 * bt + e + u] += gt[s] * h2[u];
             }
             __half2 hh = __floats2half2_rn(h2[0], h2[1]);
             pk[e / 2] = *reinterpret_cast<uint32_t*>(&hh);
           }
-          tc::tmem_st4(hbuf + c / 2, pk[0], pk[1], pk[2], pk[3]);
+          tc::tmem_st4(hbuf + 8 * bt, pk[0], pk[1], pk[2], pk[3]);
+          tc::tmem_st4(hbuf + 8 * bt + 4, pk[4], pk[5], pk[6], pk[7]);
         }
         tc::tmem_st_wait();
         tc::fence_before();
-        warp_arrive(&acc_read);
-        if (s == KE - 1) warp_arrive(&acc_empty);
         warp_arrive(&h_ready);
         const bool more = s + 1 < KE || lt + 1 < nft;
         if (more) {
@@ -1320,7 +1330,7 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up3_kernel(
       if (valid) {
         uint4* dst = reinterpret_cast<uint4*>(p.hsum + (size_t)i * f + (ft0 + lt) * NF + c0);
 #pragma unroll
-        for (int c = 0; c < 64; c += 8)
+        for (int c = 0; c < 32; c += 8)
           dst[c / 8] = make_uint4(tc::pack_bf16(hs[c], hs[c + 1]), tc::pack_bf16(hs[c + 2], hs[c + 3]),
                                   tc::pack_bf16(hs[c + 4], hs[c + 5]), tc::pack_bf16(hs[c + 6], hs[c + 7]));
       }
@@ -1330,10 +1340,10 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up3_kernel(
     if (ok && sig >= 2) ok = ewait(&v_done[(sig - 2) & 1], ((sig - 2) >> 1) & 1, 65);
     if (ok) {
       tc::fence_after();
-      // V_s of slot s is read by the half h = s % 2; the row's expert block le[s] of the KRP columns
+      // V_s of slot s is read by part s; the row's expert block le[s] of the KRP columns
 #pragma unroll
       for (int s = 0; s < KE; ++s) {
-        if (half != (s & 1)) continue;
+        if (part != s) continue;
         float v[kRank];
 #pragma unroll
         for (int k = 0; k < kRank; ++k) v[k] = 0.f;
@@ -1455,9 +1465,8 @@ int tc_krp(const LayerArgs& a) { return ((a.K * a.r + 63) / 64) * 64; }
 // when groups hold fewer than 128 rows) and picks the chunk count whose waves of one CTA per SM
 // cost least: ceil(CTAs / SMs) x (tiles per chunk + a fixed per-CTA overhead of half a tile).
 // Which fused gate/up kernel runs: the 256-column one (4b) when K r fits 64 columns, at most
-// two slots, d_ff is a multiple of 128 and the K loop (d_model) is long enough to hide its
-// serialised epilogue; otherwise the 128-column one (4), whose epilogue overlaps the next tile.
-static bool up3_ok(const LayerArgs& a) { return tc_krp(a) == 64 && a.ke <= 2 && a.f % kNf3 == 0 && a.d >= 2048; }
+// two slots and d_ff is a multiple of 128; otherwise the 128-column one (4).
+static bool up3_ok(const LayerArgs& a) { return tc_krp(a) == 64 && a.ke <= 2 && a.f % kNf3 == 0; }
 
 int tc_up_chunks(const LayerArgs& a) {
   const int n_ft = a.f / (up3_ok(a) ? kNf3 : kNf);
@@ -1542,7 +1551,7 @@ static cudaError_t launch_up3(const CUtensorMap* maps, const UpArgs& p, int nchu
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return launch_pdl(ffn_up3_kernel<KE>, dim3(nchunks, tiles), dim3(kUpWarps * 32), smem, stream, maps[0], maps[1],
+  return launch_pdl(ffn_up3_kernel<KE>, dim3(nchunks, tiles), dim3(kUp3Warps * 32), smem, stream, maps[0], maps[1],
                     maps[2], maps[3], maps[4], maps[5], p);
 }
 

@@ -166,7 +166,8 @@ int moe_hier_profile_end(const char** names, int max_names);
  * without ws/ws_bytes.  The scratch (per-block histograms and offsets) is a fixed array of
  * 65,536 int32 (256 KiB) inside the library, held by every GPU that loads the library until the
  * process exits; a layer needs 2 * ceil(T/256) * (E + G) of them, and larger layers are rejected
- * with MOE_ERR_WORKSPACE before anything is enqueued.  The call allocates nothing.  The first
+ * with MOE_ERR_WORKSPACE before anything is enqueued (batches of at most 1024 tokens are
+ * permuted by a single-CTA kernel that uses no scratch).  The call allocates nothing.  The first
  * call on a device looks up the array's device address (with that device current); make that
  * first call before any stream capture.  All calls share the one array and each kernel
  * overwrites every entry it later reads, so nothing needs clearing between calls, but calls
