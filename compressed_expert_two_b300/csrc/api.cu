@@ -59,11 +59,12 @@ Plan make_plan(const LayerArgs& a) {
     p.Ain = take(G * 4 * KRP * d * 2);
     p.Bgs = take(G * f * KRP * 2);
     p.Bus = take(G * f * KRP * 2);
+    p.Adt = take(G * f * KRP * 2);
     p.Adn = take(G * KRP * f * 2);
     p.Bdn = take(G * d * 2 * KRP * 2);
     p.Ubf = take(Rp * 2 * KRP * 2);
     p.hsum_bf = take(Rp * f * 2);
-    p.Vpart = take((size_t)p.nchunks * R * a.ke * a.r * 4);
+    p.Vpart = take((size_t)p.nchunks * 2 * R * a.ke * a.r * 4);   // up to two partials per chunk
     p.Vt = take(Rp * 2 * KRP * 2);
   } else {
     p.U = take(R * a.ke * 2 * a.r * 4);
@@ -148,7 +149,8 @@ static cudaError_t run_ffn(const LayerArgs& a, const Plan& p, void* ws, const vo
                            cudaStream_t s) {
   if (p.tc) {
     TcBufs b{at<__nv_bfloat16>(ws, p.X),   at<__nv_bfloat16>(ws, p.Ain),    at<__half>(ws, p.Bgs),
-             at<__half>(ws, p.Bus),        at<__nv_bfloat16>(ws, p.Adn),    at<__nv_bfloat16>(ws, p.Bdn),
+             at<__half>(ws, p.Bus),        at<__half>(ws, p.Adt),           at<__nv_bfloat16>(ws, p.Adn),
+             at<__nv_bfloat16>(ws, p.Bdn),
              at<__half>(ws, p.Ubf), at<__nv_bfloat16>(ws, p.hsum_bf), at<__nv_bfloat16>(ws, p.Vt),
              at<float>(ws, p.Vpart)};
     return launch_ffn_tc(a, x, wg, wu, wd, resid_ptrs(a, resid), eidx, gate, row_asg, row_begin, y_rows, b,

@@ -96,6 +96,16 @@ struct ResidView {
   }
 };
 
+// Two independent IEEE round-to-nearest FMAs in one instruction: (a.x*b.x + c.x, a.y*b.y + c.y).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  unsigned long long ra = *reinterpret_cast<unsigned long long*>(&a);
+  unsigned long long rb = *reinterpret_cast<unsigned long long*>(&b);
+  unsigned long long rc = *reinterpret_cast<unsigned long long*>(&c);
+  unsigned long long rd;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+  return *reinterpret_cast<float2*>(&rd);
+}
+
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 // SiLU from the fast exponential and reciprocal intrinsics (relative error ~1e-6); for z << 0
 // the denominator overflows to +inf and the result is -0.

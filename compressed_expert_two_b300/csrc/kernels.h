@@ -26,7 +26,7 @@ struct Plan {
   // tensor-core path
   bool tc;
   int krp, nchunks;
-  size_t X, Ain, Bgs, Bus, Adn, Bdn, Ubf, hsum_bf, Vpart, Vt;
+  size_t X, Ain, Bgs, Bus, Adt, Adn, Bdn, Ubf, hsum_bf, Vpart, Vt;
   size_t total;
 };
 
@@ -62,7 +62,7 @@ cudaError_t launch_ffn_simt(const LayerArgs& a, const void* x, const void* wg, c
 
 struct TcBufs {
   __nv_bfloat16 *X, *Ain;
-  __half *Bgs, *Bus;
+  __half *Bgs, *Bus, *Adt;
   __nv_bfloat16 *Adn, *Bdn;
   __half* U;
   __nv_bfloat16 *hsum, *Vt;

@@ -9,16 +9,6 @@
 
 namespace moe {
 
-// Two independent IEEE round-to-nearest FMAs in one instruction: (a.x*b.x + c.x, a.y*b.y + c.y).
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  unsigned long long ra = *reinterpret_cast<unsigned long long*>(&a);
-  unsigned long long rb = *reinterpret_cast<unsigned long long*>(&b);
-  unsigned long long rc = *reinterpret_cast<unsigned long long*>(&c);
-  unsigned long long rd;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
-  return *reinterpret_cast<float2*>(&rd);
-}
-
 // BF16 router logits.  Warp (tg, rg) of the CTA owns TPW tokens x RPW router rows; the CTA is
 // WT x WR warps.  Canonical order: lane l owns elements 128*j + 4*l + u (u = 0..3) and adds them
 // in ascending index, one rounding per product (exact: BF16 x BF16 fits FP32) and per add; then
