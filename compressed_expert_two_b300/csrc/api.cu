@@ -133,31 +133,65 @@ static ResidPtrs resid_ptrs(const LayerArgs& a, const moe_hier_resid* r) {
   return rp;
 }
 
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
 static bool resid_ok(const LayerArgs& a, const moe_hier_resid* r) {
   if (a.r == 0) return true;
   if (!r) return false;
   for (int m = 0; m < 3; ++m) {
-    if (!r->A[m] || !r->B[m]) return false;
+    if (!r->A[m] || !r->B[m] || !aligned16(r->A[m]) || !aligned16(r->B[m])) return false;
     if (a.int4 && (!r->sA[m] || !r->sB[m])) return false;
   }
   return true;
 }
 
+static TcBufs tc_bufs(const Plan& p, void* ws) {
+  return TcBufs{at<__nv_bfloat16>(ws, p.X),   at<__nv_bfloat16>(ws, p.Ain),    at<__half>(ws, p.Bgs),
+                at<__half>(ws, p.Bus),        at<__half>(ws, p.Adt),           at<__nv_bfloat16>(ws, p.Adn),
+                at<__nv_bfloat16>(ws, p.Bdn),
+                at<__half>(ws, p.Ubf), at<__nv_bfloat16>(ws, p.hsum_bf), at<__nv_bfloat16>(ws, p.Vt),
+                at<float>(ws, p.Vpart)};
+}
+
 static cudaError_t run_ffn(const LayerArgs& a, const Plan& p, void* ws, const void* x, const void* wg,
                            const void* wu, const void* wd, const moe_hier_resid* resid, const int32_t* eidx,
                            const float* gate, const int32_t* row_asg, const int32_t* row_begin, void* y_rows,
-                           cudaStream_t s) {
-  if (p.tc) {
-    TcBufs b{at<__nv_bfloat16>(ws, p.X),   at<__nv_bfloat16>(ws, p.Ain),    at<__half>(ws, p.Bgs),
-             at<__half>(ws, p.Bus),        at<__half>(ws, p.Adt),           at<__nv_bfloat16>(ws, p.Adn),
-             at<__nv_bfloat16>(ws, p.Bdn),
-             at<__half>(ws, p.Ubf), at<__nv_bfloat16>(ws, p.hsum_bf), at<__nv_bfloat16>(ws, p.Vt),
-             at<float>(ws, p.Vpart)};
-    return launch_ffn_tc(a, x, wg, wu, wd, resid_ptrs(a, resid), eidx, gate, row_asg, row_begin, y_rows, b,
-                         at<DevStatus>(ws, p.status), s);
-  }
+                           cudaEvent_t prep_done, cudaStream_t s) {
+  if (p.tc)
+    return launch_ffn_tc(a, x, wg, wu, wd, resid_ptrs(a, resid), eidx, gate, row_asg, row_begin, y_rows,
+                         tc_bufs(p, ws), at<DevStatus>(ws, p.status), prep_done, s);
   FfnBufs b{at<float>(ws, p.U), at<float>(ws, p.H), at<float>(ws, p.hsum), at<float>(ws, p.V)};
   return launch_ffn_simt(a, x, wg, wu, wd, resid_ptrs(a, resid), eidx, gate, row_asg, row_begin, y_rows, b, s);
+}
+
+// moe_hier_forward enqueues the weight-only residual preparation on a second stream, so that it
+// runs while the tokens are routed and permuted.  One such stream and two events per host thread
+// and device, created on first use and kept until the thread exits (no device memory).
+struct SideStream {
+  int dev = -1;
+  cudaStream_t st = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  ~SideStream() {
+    if (join) cudaEventDestroy(join);
+    if (fork) cudaEventDestroy(fork);
+    if (st) cudaStreamDestroy(st);
+  }
+};
+static thread_local SideStream g_side;
+
+static SideStream* side_stream() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  if (g_side.st && g_side.dev == dev) return &g_side;
+  if (g_side.st) return nullptr;                    // created for another device: run serially
+  if (cudaStreamCreateWithFlags(&g_side.st, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&g_side.fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&g_side.join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  g_side.dev = dev;
+  return &g_side;
 }
 
 // The last CUDA error a call of this host thread returned as MOE_ERR_CUDA.
@@ -192,6 +226,7 @@ int moe_hier_route(const moe_hier_desc* desc, const void* x, const void* w_group
   int st = validate(desc, group_map_host, &a);
   if (st != MOE_OK) return st;
   if (a.T > 0 && (!x || !w_group || !w_expert || !gidx || !eidx || !gate)) return MOE_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(w_group) || !aligned16(w_expert)) return MOE_ERR_INVALID;
   const Plan p = make_plan(a);
   if ((st = check_ws(p, ws, ws_bytes)) != MOE_OK) return st;
   prof_start((cudaStream_t)stream);
@@ -213,7 +248,7 @@ int moe_hier_permute(const moe_hier_desc* desc, const int32_t* group_map_host, c
   PermOut o{perm, inv_pos, expert_begin, expert_count, group_begin, row_asg, row_of, row_begin};
   prof_start((cudaStream_t)stream);
   return cuda_status(launch_permute(a, eidx, o, at<int32_t>(ws, p.cnt), at<int32_t>(ws, p.off),
-                                    p.nblk, (cudaStream_t)stream));
+                                    p.nblk, at<DevStatus>(ws, p.status), false, (cudaStream_t)stream));
 }
 
 int moe_hier_ffn(const moe_hier_desc* desc, const void* x, const int32_t* group_map_host,
@@ -228,11 +263,13 @@ int moe_hier_ffn(const moe_hier_desc* desc, const void* x, const int32_t* group_
   if (a.T > 0 && (!x || !w_gate || !w_up || !w_down || !eidx || !gate || !row_asg || !row_begin ||
                   !y_rows || !resid_ok(a, resid)))
     return MOE_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) || !aligned16(y_rows))
+    return MOE_ERR_INVALID;
   const Plan p = make_plan(a);
   if ((st = check_ws(p, ws, ws_bytes)) != MOE_OK) return st;
   prof_start((cudaStream_t)stream);
   return cuda_status(run_ffn(a, p, ws, x, w_gate, w_up, w_down, resid, eidx, gate, row_asg, row_begin, y_rows,
-                             (cudaStream_t)stream));
+                             nullptr, (cudaStream_t)stream));
 }
 
 int moe_hier_combine(const moe_hier_desc* desc, const void* y_rows, void* y, void* stream) {
@@ -256,6 +293,9 @@ int moe_hier_forward(const moe_hier_desc* desc, const void* x, const void* w_gro
   if (a.T > 0 && (!x || !w_group || !w_expert || !w_gate || !w_up || !w_down || !y ||
                   !resid_ok(a, resid)))
     return MOE_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(w_group) || !aligned16(w_expert) || !aligned16(w_gate) || !aligned16(w_up) ||
+      !aligned16(w_down) || !aligned16(y))
+    return MOE_ERR_INVALID;
   const Plan p = make_plan(a);
   if ((st = check_ws(p, ws, ws_bytes)) != MOE_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
@@ -265,17 +305,34 @@ int moe_hier_forward(const moe_hier_desc* desc, const void* x, const void* w_gro
   int32_t* perm = perm_opt ? perm_opt : at<int32_t>(ws, p.perm);
   prof_start(s);
   cudaError_t e = cudaMemsetAsync(at<DevStatus>(ws, p.status), 0, sizeof(DevStatus), s);
+  // residual stacks on the side stream, concurrently with routing and permutation (in order,
+  // on `s`, when profiling per kernel)
+  cudaEvent_t prep_done = nullptr;
+  SideStream* side = (p.tc && a.T > 0 && !g_prof_ev) ? side_stream() : nullptr;
+  if (e == cudaSuccess && side) {
+    e = cudaEventRecord(side->fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side->st, side->fork, 0);
+    if (e == cudaSuccess) e = launch_resid_prep(a, resid_ptrs(a, resid), tc_bufs(p, ws), side->st);
+    if (e == cudaSuccess) e = cudaEventRecord(side->join, side->st);
+    prep_done = side->join;
+  }
   if (e == cudaSuccess)
     e = launch_route(a, x, w_group, b_group, w_expert, at<float>(ws, p.logits), gidx, eidx, gate, s);
   PermOut o{perm, at<int32_t>(ws, p.inv_pos), at<int32_t>(ws, p.ebeg), at<int32_t>(ws, p.ecnt),
             at<int32_t>(ws, p.gbeg), at<int32_t>(ws, p.row_asg), at<int32_t>(ws, p.row_of),
             at<int32_t>(ws, p.rbeg)};
   if (e == cudaSuccess)
-    e = launch_permute(a, eidx, o, at<int32_t>(ws, p.cnt), at<int32_t>(ws, p.off), p.nblk, s);
+    e = launch_permute(a, eidx, o, at<int32_t>(ws, p.cnt), at<int32_t>(ws, p.off), p.nblk,
+                       at<DevStatus>(ws, p.status), true, s);
   void* yrows = a.kg > 1 ? at<void>(ws, p.yrows) : y;
   if (e == cudaSuccess)
-    e = run_ffn(a, p, ws, x, w_gate, w_up, w_down, resid, eidx, gate, o.row_asg, o.rbeg, yrows, s);
+    e = run_ffn(a, p, ws, x, w_gate, w_up, w_down, resid, eidx, gate, o.row_asg, o.rbeg, yrows, prep_done, s);
   if (e == cudaSuccess) e = launch_combine(a, yrows, y, s);
+  // the side stream's work rejoins `s` on every path (a capture must not end with it forked)
+  if (prep_done) {
+    const cudaError_t j = cudaStreamWaitEvent(s, prep_done, 0);
+    if (e == cudaSuccess) e = j;
+  }
   return cuda_status(e);
 }
 
@@ -381,5 +438,5 @@ extern "C" int moe_hier_permute_noalloc(const moe_hier_desc* desc, const int32_t
   int32_t* off = scratch + (size_t)nblk * (a.E + a.G);
   PermOut o{perm, inv_pos, expert_begin, expert_count, group_begin, row_asg, row_of, row_begin};
   prof_start((cudaStream_t)stream);
-  return cuda_status(launch_permute(a, eidx, o, cnt, off, nblk, (cudaStream_t)stream));
+  return cuda_status(launch_permute(a, eidx, o, cnt, off, nblk, nullptr, false, (cudaStream_t)stream));
 }

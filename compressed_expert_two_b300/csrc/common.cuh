@@ -66,6 +66,8 @@ struct GroupTable {
 struct DevStatus {
   int code;
   int where;
+  unsigned int grid_bar;   // arrivals at the permutation's grid-wide barrier (zeroed before it)
+  int pad;
 };
 
 __device__ __forceinline__ float to_f32(float v) { return v; }
@@ -104,6 +106,21 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
   unsigned long long rd;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
   return *reinterpret_cast<float2*>(&rd);
+}
+
+// a.lo * b.lo + c and a.hi * b.hi + c for two BF16 values packed in a 32-bit word (low half =
+// lower address), one rounding: the mixed-precision FMA of sm_100 and later.
+__device__ __forceinline__ float fma_bf16_lo(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n .reg .b16 al, ah, bl, bh;\n mov.b32 {al, ah}, %1;\n mov.b32 {bl, bh}, %2;\n"
+      " fma.rn.f32.bf16 %0, al, bl, %3;\n}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fma_bf16_hi(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n .reg .b16 al, ah, bl, bh;\n mov.b32 {al, ah}, %1;\n mov.b32 {bl, bh}, %2;\n"
+      " fma.rn.f32.bf16 %0, ah, bh, %3;\n}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  return d;
 }
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }

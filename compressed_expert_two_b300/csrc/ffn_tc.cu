@@ -227,58 +227,135 @@ __global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ x, const in
 }
 
 // ------------------------------------------------------------------------------------------
-// 3'. U on the CUDA cores, for batches of few rows (decode): warp w of block (row i, matrix m,
-//     z) computes U[i][m*KRP + o], o = 8z + w, = sum_c x[t(i)][c] A_m,e_j^T[k][c] (o = j*r + k)
-//     for the K experts of the row's group straight from the INT4 codes, lanes striding over c
-//     in 8-element chunks (FP32 accumulation, FP16 out; padding columns zero).
+// 3'. U on the CUDA cores, for batches of few rows (decode): block (row i, matrix m) computes
+//     (blocks m = 0 also write the gathered row X[i] of step 2)
+//     U[i][m*KRP + o] = sum_c x[t(i)][c] A_m,e_j^T[k][c] (o = j*r + k) for the K experts of the
+//     row's group straight from the INT4 codes; warp w takes 8 outputs at a time, lanes stride
+//     over c in 32-element chunks (one 16-byte load of codes per output and chunk), FP32
+//     accumulation, FP16 out, padding columns zero.
+//     Codes become BF16 values without a per-element conversion: a nibble q or'ed into the
+//     mantissa of the BF16 number 128 (bits 0x4300) is the BF16 number 128 + q, and subtracting
+//     136 leaves q - 8 exactly (the exponent-bias conversion used by weight-only quantised GEMM
+//     kernels, e.g. Kim et al., "Who Says Elephants Can't Run", 2022); the mixed-precision FMA
+//     then multiplies BF16 x by it exactly and rounds once into the FP32 sum.
 // ------------------------------------------------------------------------------------------
-constexpr int kUSimtUnroll = 8;
+template <bool AH, bool BH>
+__device__ __forceinline__ float fma_bf16_sel(uint32_t a, uint32_t b, float c) {
+  float d;
+  if (AH && BH)
+    asm("{\n .reg .b16 al, ah, bl, bh;\n mov.b32 {al, ah}, %1;\n mov.b32 {bl, bh}, %2;\n"
+        " fma.rn.f32.bf16 %0, ah, bh, %3;\n}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  else if (AH)
+    asm("{\n .reg .b16 al, ah, bl, bh;\n mov.b32 {al, ah}, %1;\n mov.b32 {bl, bh}, %2;\n"
+        " fma.rn.f32.bf16 %0, ah, bl, %3;\n}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  else if (BH)
+    asm("{\n .reg .b16 al, ah, bl, bh;\n mov.b32 {al, ah}, %1;\n mov.b32 {bl, bh}, %2;\n"
+        " fma.rn.f32.bf16 %0, al, bh, %3;\n}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  else
+    asm("{\n .reg .b16 al, ah, bl, bh;\n mov.b32 {al, ah}, %1;\n mov.b32 {bl, bh}, %2;\n"
+        " fma.rn.f32.bf16 %0, al, bl, %3;\n}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+
+// Two BF16 pairs (q - 8) from two code bytes: for bytes (b_lo, b_hi) of w selected by `sel`,
+// P = (hi nibble of b_lo, hi nibble of b_hi), Q = (lo nibble of b_lo, lo nibble of b_hi).
+__device__ __forceinline__ void code_pairs(uint32_t w, uint32_t sel, uint32_t& P, uint32_t& Q) {
+  const uint32_t r = __byte_perm(w, 0u, sel);               // [b_lo, 0, b_hi, 0]
+  const uint32_t p = ((r >> 4) & 0x000F000Fu) | 0x43004300u;
+  const uint32_t q = (r & 0x000F000Fu) | 0x43004300u;
+  const __nv_bfloat162 off = __floats2bfloat162_rn(136.f, 136.f);
+  __nv_bfloat162 pp = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&p), off);
+  __nv_bfloat162 qq = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&q), off);
+  P = *reinterpret_cast<uint32_t*>(&pp);
+  Q = *reinterpret_cast<uint32_t*>(&qq);
+}
+
+// sum over 8 elements: x pairs X0 = (x0, x1) .. X3 = (x6, x7), code word w (element 2b = high
+// nibble of byte b, element 2b + 1 = low nibble)
+__device__ __forceinline__ float dot8_int4(uint32_t w, uint32_t X0, uint32_t X1, uint32_t X2, uint32_t X3, float acc) {
+  uint32_t P0, Q0, P1, Q1;
+  code_pairs(w, 0x4140u, P0, Q0);                          // (e0, e2), (e1, e3)
+  code_pairs(w, 0x4342u, P1, Q1);                          // (e4, e6), (e5, e7)
+  acc = fma_bf16_sel<false, false>(X0, P0, acc);
+  acc = fma_bf16_sel<true, false>(X0, Q0, acc);
+  acc = fma_bf16_sel<false, true>(X1, P0, acc);
+  acc = fma_bf16_sel<true, true>(X1, Q0, acc);
+  acc = fma_bf16_sel<false, false>(X2, P1, acc);
+  acc = fma_bf16_sel<true, false>(X2, Q1, acc);
+  acc = fma_bf16_sel<false, true>(X3, P1, acc);
+  acc = fma_bf16_sel<true, true>(X3, Q1, acc);
+  return acc;
+}
+
+constexpr int kUSimtOut = 8;    // outputs per warp pass
 
 __global__ void __launch_bounds__(256) u_simt_kernel(const __nv_bfloat16* __restrict__ x,
                                                      const int32_t* __restrict__ row_asg,
                                                      const int32_t* __restrict__ eidx, PrepArgs p, GroupTable tab,
-                                                     int kg, int ke, __half* __restrict__ U) {
+                                                     int kg, int ke, __half* __restrict__ U,
+                                                     __nv_bfloat16* __restrict__ X) {
   pdl_wait();
   pdl_trigger();
-  extern __shared__ __nv_bfloat16 xs[];              // the row's x (d values)
+  extern __shared__ __align__(16) __nv_bfloat16 xs[];      // the row's x (d values)
   const int i = blockIdx.x, m = blockIdx.y, d = p.d, KRP = p.KRP, r = p.r, K = p.K;
-  const int lane = threadIdx.x & 31, o = blockIdx.z * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int b = row_asg[i], t = b / kg, jg = b % kg;
   const int g = tab.group_of[eidx[(size_t)t * kg * ke + jg * ke]];
-  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8)
-    *reinterpret_cast<uint4*>(xs + c) = *reinterpret_cast<const uint4*>(x + (size_t)t * d + c);
+  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)t * d + c);
+    *reinterpret_cast<uint4*>(xs + c) = v;
+    if (m == 0) *reinterpret_cast<uint4*>(X + (size_t)i * d + c) = v;   // the row in (group, token) order
+  }
   __syncthreads();
-  const int j = o / r, k = o % r;
-  float acc = 0.f;
-  if (j < K) {
-    const int e = tab.member[g * K + j];
-    const int nch = d / 8;                           // 8-element chunks; lane takes chunks lane + 32 n
-    for (int c0 = lane; c0 < nch; c0 += 32 * kUSimtUnroll) {
-      float cq[kUSimtUnroll][8], sc[kUSimtUnroll];
+  const ResidView& v = p.A[m];
+  const uint8_t* codes = (const uint8_t*)v.vals;
+  const int nchunk = d / 32;                                  // 32-element chunks of a rank row
+  for (int ob = warp * kUSimtOut; ob < KRP; ob += nwarps * kUSimtOut) {
+    const uint8_t* crow[kUSimtOut];
+    const __half* srow[kUSimtOut];
+    bool live[kUSimtOut];
 #pragma unroll
-      for (int u = 0; u < kUSimtUnroll; ++u) {
-        const int ch = c0 + 32 * u;
-        if (ch < nch) codes8(p.A[m], e, k, ch * 8, cq[u], sc[u]);
-        else { sc[u] = 0.f; for (int q = 0; q < 8; ++q) cq[u][q] = 0.f; }
+    for (int q = 0; q < kUSimtOut; ++q) {
+      const int o = ob + q, j = o / r, k = o % r;
+      live[q] = o < KRP && j < K;
+      const size_t row = live[q] ? (size_t)tab.member[g * K + j] * r + k : 0;
+      crow[q] = codes + row * (d / 2);
+      srow[q] = v.scales + row * (d / kQGroup);
+    }
+    float acc[kUSimtOut];
+#pragma unroll
+    for (int q = 0; q < kUSimtOut; ++q) acc[q] = 0.f;
+    for (int c = lane; c < nchunk; c += 32) {
+      uint4 cw[kUSimtOut];
+      float sc[kUSimtOut];
+#pragma unroll
+      for (int q = 0; q < kUSimtOut; ++q) {
+        cw[q] = live[q] ? __ldg(reinterpret_cast<const uint4*>(crow[q] + (size_t)c * 16)) : make_uint4(0, 0, 0, 0);
+        sc[q] = live[q] ? __half2float(srow[q][c >> 1]) : 0.f;
       }
+      const uint4* xp = reinterpret_cast<const uint4*>(xs + c * 32);
+      const uint4 x0 = xp[0], x1 = xp[1], x2 = xp[2], x3 = xp[3];
 #pragma unroll
-      for (int u = 0; u < kUSimtUnroll; ++u) {
-        const int ch = c0 + 32 * u;
-        if (ch >= nch) continue;
-        const uint4 xv = *reinterpret_cast<const uint4*>(xs + ch * 8);
-        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-        float s8 = 0.f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          s8 = fmaf(__uint_as_float(xw[q] << 16), cq[u][2 * q], s8);
-          s8 = fmaf(__uint_as_float(xw[q] & 0xFFFF0000u), cq[u][2 * q + 1], s8);
-        }
-        acc = fmaf(s8, sc[u], acc);
+      for (int q = 0; q < kUSimtOut; ++q) {
+        float s = 0.f;
+        s = dot8_int4(cw[q].x, x0.x, x0.y, x0.z, x0.w, s);
+        s = dot8_int4(cw[q].y, x1.x, x1.y, x1.z, x1.w, s);
+        s = dot8_int4(cw[q].z, x2.x, x2.y, x2.z, x2.w, s);
+        s = dot8_int4(cw[q].w, x3.x, x3.y, x3.z, x3.w, s);
+        acc[q] = fmaf(s, sc[q], acc[q]);
       }
     }
+#pragma unroll
+    for (int q = 0; q < kUSimtOut; ++q)
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], off);
+    if (lane < kUSimtOut && ob + lane < KRP) {
+      float val = acc[0];
+#pragma unroll
+      for (int q = 1; q < kUSimtOut; ++q) val = lane == q ? acc[q] : val;
+      U[(size_t)i * 2 * KRP + m * KRP + ob + lane] = __float2half_rn(val);
+    }
   }
-  for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) U[(size_t)i * 2 * KRP + m * KRP + o] = __float2half_rn(acc);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -1039,7 +1116,7 @@ __global__ void __launch_bounds__(kUp3Warps * 32, 1) ffn_up3_kernel(
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full[STAGES], empty[STAGES];
   __shared__ uint64_t base_full, acc_empty, rb_full, rb_empty, ad_full, ad_empty;
-  __shared__ uint64_t acc_full, acc_read, u_ready, h_ready, v_done[2], fin1, fin2;
+  __shared__ uint64_t acc_full, acc_read, u_ready, h_ready[2], v_done[2], fin1, fin2;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
@@ -1071,7 +1148,7 @@ __global__ void __launch_bounds__(kUp3Warps * 32, 1) ffn_up3_kernel(
     tc::bar_init(&acc_full, 1);
     tc::bar_init(&acc_read, kEpiArrive);
     tc::bar_init(&u_ready, kEpiArrive);
-    tc::bar_init(&h_ready, kEpiArrive);
+    tc::bar_init(&h_ready[0], kEpiArrive); tc::bar_init(&h_ready[1], kEpiArrive);
     tc::bar_init(&v_done[0], 1); tc::bar_init(&v_done[1], 1);
     tc::bar_init(&fin1, 1); tc::bar_init(&fin2, 1);
     abort_flag = 0;
@@ -1162,7 +1239,7 @@ __global__ void __launch_bounds__(kUp3Warps * 32, 1) ffn_up3_kernel(
       auto issue_v = [&](int tau) -> bool {
         const int lt = tau / KE, s = tau % KE;
         if (s == 0 && !tc::bar_wait(&ad_full, lt & 1, ab, 56)) return false;
-        if (!tc::bar_wait(&h_ready, tau & 1, ab, 57)) return false;
+        if (!tc::bar_wait(&h_ready[tau & 1], (tau >> 1) & 1, ab, 57)) return false;
         tc::fence_after();
         const uint32_t hcol = tmem + COL_H + 64 * (tau & 1);
 #pragma unroll
@@ -1176,7 +1253,9 @@ __global__ void __launch_bounds__(kUp3Warps * 32, 1) ffn_up3_kernel(
       bool ok = true;
       for (int sig = 0; sig < n_slots && ok; ++sig) {
         const int lt = sig / KE, s = sig % KE;
-        if (sig >= 1 && !issue_v(sig - 1)) { ok = false; break; }
+        // V of the previous tile's last slot goes first (the new tile's base K loop is long);
+        // inside a tile, V of slot s - 1 follows R_s so that R_s does not wait for h_{s-1}
+        if (s == 0 && sig >= 1 && !issue_v(sig - 1)) { ok = false; break; }
         if (s == 0) {
           if (!tc::bar_wait(&base_full, lt & 1, ab, 58)) { ok = false; break; }
           if (!tc::bar_wait(&rb_full, lt & 1, ab, 59)) { ok = false; break; }
@@ -1192,6 +1271,7 @@ __global__ void __launch_bounds__(kUp3Warps * 32, 1) ffn_up3_kernel(
         }
         tc::mma_commit(&acc_full);
         if (s == KE - 1) tc::mma_commit(&rb_empty);
+        if (s > 0 && !issue_v(sig - 1)) { ok = false; break; }
       }
       if (ok && n_slots > 0) issue_v(n_slots - 1);
       tc::mma_commit(&fin2);
@@ -1284,6 +1364,18 @@ __global__ void __launch_bounds__(kUp3Warps * 32, 1) ffn_up3_kernel(
 #pragma unroll
       for (int s = 0; s < KE; ++s, ++sig) {
         if (!ewait(&acc_full, sig & 1, 62)) { ok = false; break; }
+        // R_s has finished reading the U~ tile.  Inside a tile the next delta is built now, so
+        // that the next residual MMA waits only for acc to be read; the next tile's first delta
+        // is built after acc is released (its MMA follows the next base K loop)
+        auto next_delta = [&]() {
+          build_delta(s + 1 < KE ? s + 1 : 0);
+          tc::fence_async_smem();
+          warp_arrive(&u_ready);
+          const int s2 = (s + 2) % KE;
+          const int lt2 = lt + (s + 2) / KE;
+          if (lt2 < nft) load_u(s2, unext);
+        };
+        if (s + 1 < KE) next_delta();
         // the h buffer of this slot is free once the V MMA of slot sig - 2 has completed
         if (sig >= 2 && !ewait(&v_done[sig & 1], ((sig - 2) >> 1) & 1, 63)) { ok = false; break; }
         tc::fence_after();
@@ -1299,7 +1391,10 @@ __global__ void __launch_bounds__(kUp3Warps * 32, 1) ffn_up3_kernel(
           if (bt == 1) {
             tc::fence_before();
             warp_arrive(&acc_read);
-            if (s == KE - 1) warp_arrive(&acc_empty);
+            if (s == KE - 1) {
+              warp_arrive(&acc_empty);
+              if (lt + 1 < nft) next_delta();
+            }
           }
           uint32_t pk[8];
 #pragma unroll
@@ -1318,16 +1413,7 @@ __global__ void __launch_bounds__(kUp3Warps * 32, 1) ffn_up3_kernel(
         }
         tc::tmem_st_wait();
         tc::fence_before();
-        warp_arrive(&h_ready);
-        const bool more = s + 1 < KE || lt + 1 < nft;
-        if (more) {
-          build_delta(s + 1 < KE ? s + 1 : 0);
-          tc::fence_async_smem();
-          warp_arrive(&u_ready);
-          const int s2 = (s + 2) % KE;
-          const int lt2 = lt + (s + 2) / KE;
-          if (lt2 < nft) load_u(s2, unext);
-        }
+        warp_arrive(&h_ready[sig & 1]);
       }
       if (!ok) break;
       if (valid) {
@@ -1724,40 +1810,38 @@ __global__ void v_reduce_kernel(const float* __restrict__ Vpart, const int32_t* 
                                 int nchunks, int KRP, __nv_bfloat16* __restrict__ Vt) {
   pdl_wait();
   pdl_trigger();
-  // one thread per (row, 16-wide block of V~): the block of local expert jb holds the gated v of
-  // the row's slot routed to that expert (zero if none); both halves (hi, lo of Bdn) get a copy
+  // one thread per (row, 16-wide block of V~, quarter of the block): the block of local expert jb
+  // holds the gated v of the row's slot routed to that expert (zero if none); both halves (hi,
+  // lo of Bdn) get a copy
   const int nblk = KRP / kRank;
   const int w = blockIdx.x * blockDim.x + threadIdx.x;
-  if (w >= R * nblk) return;
-  const int i = w / nblk, jb = w % nblk;
+  if (w >= R * nblk * 4) return;
+  const int qt = w & 3, i = (w >> 2) / nblk, jb = (w >> 2) % nblk;
   const int b = row_asg[i], t = b / kg, j = b % kg;
   int slot = -1;
   for (int s = 0; s < ke; ++s)
     if (jb < tab.K && tab.local_of[eidx[(size_t)t * kg * ke + j * ke + s]] == jb) slot = s;
-  float acc[kRank];
-#pragma unroll
-  for (int k = 0; k < kRank; ++k) acc[k] = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (slot >= 0) {
-    const float4* src = reinterpret_cast<const float4*>(Vpart + ((size_t)i * ke + slot) * kRank);
+    const float4* src = reinterpret_cast<const float4*>(Vpart + ((size_t)i * ke + slot) * kRank) + qt;
     const size_t cstride = (size_t)R * ke * kRank / 4;   // float4s per chunk
-#pragma unroll 4
-    for (int c = 0; c < nchunks; ++c) {
+    int c = 0;
+    for (; c + 8 <= nchunks; c += 8) {
+      float4 v[8];
 #pragma unroll
-      for (int q = 0; q < kRank / 4; ++q) {
-        const float4 v4 = src[c * cstride + q];
-        acc[4 * q] += v4.x; acc[4 * q + 1] += v4.y; acc[4 * q + 2] += v4.z; acc[4 * q + 3] += v4.w;
-      }
+      for (int u = 0; u < 8; ++u) v[u] = src[(c + u) * cstride];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) { acc.x += v[u].x; acc.y += v[u].y; acc.z += v[u].z; acc.w += v[u].w; }
+    }
+    for (; c < nchunks; ++c) {
+      const float4 v = src[c * cstride];
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
   }
-  uint32_t pk[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) pk[k] = tc::pack_bf16(acc[2 * k], acc[2 * k + 1]);
-  const uint4 lo4 = make_uint4(pk[0], pk[1], pk[2], pk[3]), hi4 = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-  uint4* row = reinterpret_cast<uint4*>(Vt + (size_t)i * 2 * KRP);
-  row[(jb * kRank) / 8] = lo4;
-  row[(jb * kRank) / 8 + 1] = hi4;
-  row[(KRP + jb * kRank) / 8] = lo4;
-  row[(KRP + jb * kRank) / 8 + 1] = hi4;
+  const uint2 pk = make_uint2(tc::pack_bf16(acc.x, acc.y), tc::pack_bf16(acc.z, acc.w));
+  uint2* row = reinterpret_cast<uint2*>(Vt + (size_t)i * 2 * KRP);
+  row[(jb * kRank) / 4 + qt] = pk;
+  row[(KRP + jb * kRank) / 4 + qt] = pk;
 }
 
 // ------------------------------------------------------------------------------------------
@@ -1934,38 +2018,56 @@ static cudaError_t launch_up(const CUtensorMap* maps, const UpArgs& p, int nchun
   }
 }
 
+// The double-buffered form (4c) hides its heavier epilogue (V on the CUDA cores) only behind
+// long K loops over many rows; shorter ones run the single-buffered form (4b).
+static bool up4_ok(const LayerArgs& a) { return up3_ok(a) && a.d >= 4096 && a.R >= 2048; }
+
+static PrepArgs prep_args(const LayerArgs& a, const ResidPtrs& rp, const TcBufs& b) {
+  PrepArgs pa;
+  for (int m = 0; m < 3; ++m) { pa.A[m] = rp.A[m]; pa.B[m] = rp.B[m]; }
+  pa.Ain = b.Ain; pa.Bgs = b.Bgs; pa.Bus = b.Bus; pa.Adn = b.Adn; pa.Bdn = b.Bdn;
+  pa.G = a.G; pa.K = a.K; pa.d = a.d; pa.f = a.f; pa.r = a.r; pa.KRP = tc_krp(a);
+  pa.need_ain = a.R > kUSimtMaxRows;             // the CUDA-core U kernel reads the codes itself
+  const bool up4 = up4_ok(a);
+  pa.adn_f16 = up3_ok(a) && !up4;
+  pa.Adt = up4 ? b.Adt : nullptr;
+  return pa;
+}
+
+// 1. residual stacks (weights only: may run on another stream, concurrently with the routing)
+cudaError_t launch_resid_prep(const LayerArgs& a, const ResidPtrs& rp, const TcBufs& b, cudaStream_t st) {
+  if (a.R == 0) return cudaSuccess;
+  const PrepArgs pa = prep_args(a, rp, b);
+  const int G = a.G, d = a.d, f = a.f;
+  launch_pdl(resid_prep_rows_kernel, dim3(148 * 4), dim3(256), 0, st, pa, a.tab);
+  launch_pdl(resid_prep_t_kernel, dim3(G * (2 * (f / 64) + d / 64 + (pa.Adt ? f / 64 : 0))), dim3(256), 0, st, pa,
+             a.tab);
+  prof_mark("resid_prep", st);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, const void* wu, const void* wd,
                           const ResidPtrs& rp, const int32_t* eidx, const float* gate, const int32_t* row_asg,
                           const int32_t* row_begin, void* y_rows, const TcBufs& b, DevStatus* status,
-                          cudaStream_t st) {
+                          cudaEvent_t prep_done, cudaStream_t st) {
   if (a.R == 0) return cudaSuccess;
   const int KRP = tc_krp(a), G = a.G, d = a.d, f = a.f, R = a.R;
   const int tiles = (R + kTile - 1) / kTile + G;
   cudaError_t e;
 
-  // 1. residual stacks
-  PrepArgs pa;
-  for (int m = 0; m < 3; ++m) { pa.A[m] = rp.A[m]; pa.B[m] = rp.B[m]; }
-  pa.Ain = b.Ain; pa.Bgs = b.Bgs; pa.Bus = b.Bus; pa.Adn = b.Adn; pa.Bdn = b.Bdn;
-  pa.G = G; pa.K = a.K; pa.d = d; pa.f = f; pa.r = a.r; pa.KRP = KRP;
+  // 1. residual stacks, unless already enqueued elsewhere (prep_done: recorded after them)
+  const PrepArgs pa = prep_args(a, rp, b);
   const bool u_simt = R <= kUSimtMaxRows;
-  pa.need_ain = !u_simt;
-  const bool up3 = up3_ok(a);
-  // the double-buffered form (4c) hides its heavier epilogue (V on the CUDA cores) only behind
-  // long K loops over many rows; shorter ones run the single-buffered form (4b)
-  const bool up4 = up3 && d >= 4096 && R >= 2048;
-  pa.adn_f16 = up3 && !up4;
-  pa.Adt = up4 ? b.Adt : nullptr;
-  launch_pdl(resid_prep_rows_kernel, dim3(148 * 4), dim3(256), 0, st, pa, a.tab);
-  launch_pdl(resid_prep_t_kernel, dim3(G * (2 * (f / 64) + d / 64 + (pa.Adt ? f / 64 : 0))), dim3(256), 0, st, pa,
-             a.tab);
-  prof_mark("resid_prep", st);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const bool up3 = up3_ok(a), up4 = up4_ok(a);
+  if (!prep_done && (e = launch_resid_prep(a, rp, b, st)) != cudaSuccess) return e;
 
-  // 2. rows of x in (group, token) order
-  launch_pdl(gather_rows_kernel, dim3(148 * 8), dim3(256), 0, st, (const __nv_bfloat16*)x, row_asg, R, d, a.kg, b.X);
-  prof_mark("gather_rows", st);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // 2. rows of x in (group, token) order (the CUDA-core U kernel writes them itself)
+  if (!u_simt) {
+    launch_pdl(gather_rows_kernel, dim3(148 * 8), dim3(256), 0, st, (const __nv_bfloat16*)x, row_asg, R, d, a.kg,
+               b.X);
+    prof_mark("gather_rows", st);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
 
   CUtensorMap mX, mAhi, mAlo, mWg, mWu, mBg, mBu, mAd, mH, mVt, mWd, mBd, mAdt;
   const uint64_t Rp = R < kTile ? kTile : R;   // row buffers hold at least one full tile
@@ -1989,9 +2091,10 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   if (!ok) return cudaErrorInvalidValue;
 
   // 3. U = X (Ain_hi + Ain_lo)^T (FP32 accumulation, FP16 out): the hi stack is at rows g*4*KRP, the lo stack 2*KRP later
+  if (prep_done && !u_simt && (e = cudaStreamWaitEvent(st, prep_done, 0)) != cudaSuccess) return e;
   if (u_simt) {
-    e = launch_pdl(u_simt_kernel, dim3(R, 2, KRP / 8), dim3(256), (size_t)d * 2, st, (const __nv_bfloat16*)x,
-                   row_asg, eidx, pa, a.tab, a.kg, a.ke, b.U);
+    e = launch_pdl(u_simt_kernel, dim3(R, 2), dim3(256), (size_t)d * 2, st, (const __nv_bfloat16*)x,
+                   row_asg, eidx, pa, a.tab, a.kg, a.ke, b.U, b.X);
     prof_mark("u_simt", st);
   } else {
     e = (2 * KRP == 256)
@@ -2004,6 +2107,7 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   if (e != cudaSuccess) return e;
 
   // 4. fused gate/up
+  if (prep_done && u_simt && (e = cudaStreamWaitEvent(st, prep_done, 0)) != cudaSuccess) return e;
   UpArgs p;
   p.row_begin = row_begin; p.row_asg = row_asg; p.eidx = eidx; p.gate = gate; p.U = b.U; p.hsum = b.hsum;
   p.sAd = rp.A[2].scales;
@@ -2022,7 +2126,7 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   if (e != cudaSuccess) return e;
 
   // 5. V~
-  launch_pdl(v_reduce_kernel, dim3((R * (KRP / kRank) + 255) / 256), dim3(256), 0, st, (const float*)b.Vpart, row_asg,
+  launch_pdl(v_reduce_kernel, dim3((R * (KRP / kRank) * 4 + 255) / 256), dim3(256), 0, st, (const float*)b.Vpart, row_asg,
              eidx, a.tab, R, a.kg, a.ke, up4 ? 2 * nchunks : nchunks, KRP, b.Vt);
   prof_mark("v_reduce", st);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -44,7 +44,7 @@ struct PermOut {
   int32_t *perm, *inv_pos, *ebeg, *ecnt, *gbeg, *row_asg, *row_of, *rbeg;
 };
 cudaError_t launch_permute(const LayerArgs& a, const int32_t* eidx, const PermOut& o, int32_t* cnt,
-                           int32_t* off, int nblk, cudaStream_t st);
+                           int32_t* off, int nblk, DevStatus* status, bool bar_zeroed, cudaStream_t st);
 
 struct ResidPtrs {
   ResidView A[3], B[3];
@@ -74,7 +74,10 @@ int tc_up_chunks(const LayerArgs& a);
 cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, const void* wu, const void* wd,
                           const ResidPtrs& rp, const int32_t* eidx, const float* gate, const int32_t* row_asg,
                           const int32_t* row_begin, void* y_rows, const TcBufs& b, DevStatus* status,
-                          cudaStream_t st);
+                          cudaEvent_t prep_done, cudaStream_t st);
+// The weight-only first step of launch_ffn_tc (residual stacks); launch_ffn_tc skips it when
+// given prep_done, an event recorded after this call's work (it then waits for the event).
+cudaError_t launch_resid_prep(const LayerArgs& a, const ResidPtrs& rp, const TcBufs& b, cudaStream_t st);
 
 cudaError_t launch_combine(const LayerArgs& a, const void* y_rows, void* y, cudaStream_t st);
 

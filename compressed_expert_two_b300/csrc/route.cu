@@ -155,24 +155,19 @@ __global__ void __launch_bounds__(256, 2) router_logits_smem_kernel(
       for (int i = 0; i < 8; ++i) xr[i] = *reinterpret_cast<const uint2*>(&xs[st][tg * 8 + i][jj * 128 + 4 * lane]);
 #pragma unroll
       for (int q = 0; q < 8; ++q) wr[q] = *reinterpret_cast<const uint2*>(&ws[st][rg * 8 + q][jj * 128 + 4 * lane]);
+      // element u of the lane's 4-element chunk: the mixed-precision FMA takes the BF16 halves
+      // as they are (BF16 x BF16 is exact in FP32, so it rounds once, like mul + add)
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        float xv[8], wv[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const uint32_t a = u < 2 ? xr[i].x : xr[i].y;
-          xv[i] = (u & 1) ? __uint_as_float(a & 0xFFFF0000u) : __uint_as_float(a << 16);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t w = u < 2 ? wr[q].x : wr[q].y;
+            acc[i][q] = (u & 1) ? fma_bf16_hi(a, w, acc[i][q]) : fma_bf16_lo(a, w, acc[i][q]);
+          }
         }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint32_t w = u < 2 ? wr[q].x : wr[q].y;
-          wv[q] = (u & 1) ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
-        }
-        // BF16 x BF16 is exact in FP32, so the fused multiply-add rounds once, like mul + add
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-          for (int q = 0; q < 8; ++q) acc[i][q] = __fmaf_rn(xv[i], wv[q], acc[i][q]);
       }
     }
     // refill the stage computed in the previous iteration (every warp has passed the barrier above)
@@ -261,63 +256,96 @@ __global__ void __launch_bounds__(256) router_logits_f32_kernel(
     }
 }
 
-// One thread per token: top-k_g groups, softmax p; inside each chosen group top-k_e experts,
-// softmax q; gate = p * q.  Higher logit first, equal logits -> lower index first.
-__global__ void router_select_kernel(const float* __restrict__ logits, GroupTable tab, int Tn,
-                                     int kg, int ke, int32_t* __restrict__ gidx,
-                                     int32_t* __restrict__ eidx, float* __restrict__ gate) {
+// L lanes per token (L = the power of two >= max(G, K), at most 32): top-k_g groups, softmax p;
+// inside each chosen group top-k_e experts, softmax q; gate = p * q.  Higher logit first, equal
+// logits -> lower index first.  Lane l of a token holds groups l, l + L, ... and, per chosen
+// group, its member l; each pick is an argmax over the token's lanes; lane j keeps the j-th pick.
+// The softmax sums run over the picks in order.
+constexpr int kSelGroupsPerLane = kMaxE / 32;
+
+template <int L>
+__device__ __forceinline__ void seg_argmax(float& v, int& idx) {
+  // idx < 0: nothing to offer; ties go to the lower index
+#pragma unroll
+  for (int o = L / 2; o >= 1; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o, L);
+    const int oi = __shfl_xor_sync(0xffffffffu, idx, o, L);
+    if (oi >= 0 && (idx < 0 || ov > v || (ov == v && oi < idx))) { v = ov; idx = oi; }
+  }
+}
+
+template <int L>
+__global__ void __launch_bounds__(256) router_select_kernel(const float* __restrict__ logits, GroupTable tab,
+                                                            int Tn, int kg, int ke, int32_t* __restrict__ gidx,
+                                                            int32_t* __restrict__ eidx, float* __restrict__ gate) {
   pdl_wait();
   pdl_trigger();
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= Tn) return;
+  const int li = threadIdx.x & (L - 1);
+  const int t_raw = (blockIdx.x * blockDim.x + threadIdx.x) / L;
+  if ((int)((blockIdx.x * blockDim.x + (threadIdx.x & ~31u)) / L) >= Tn) return;   // the whole warp is past the batch
+  const bool valid = t_raw < Tn;
+  const int t = valid ? t_raw : Tn - 1;
   const int G = tab.G, E = tab.E, K = tab.K, k = kg * ke;
   const float* sg = logits + (size_t)t * (G + E);
   const float* se = sg + G;
-  uint32_t taken[kMaxE / 32];
+  float gv[kSelGroupsPerLane];
+  uint32_t avail = 0u;
 #pragma unroll
-  for (int i = 0; i < kMaxE / 32; ++i) taken[i] = 0u;
-  int gsel[kMaxK];
-  float gval[kMaxK];
+  for (int u = 0; u < kSelGroupsPerLane; ++u) {
+    const int g = li + L * u;
+    gv[u] = g < G ? sg[g] : 0.f;
+    if (g < G) avail |= 1u << u;
+  }
+  // group picks: lane j keeps pick j
+  int my_g = -1;
+  float my_gv = 0.f;
   for (int j = 0; j < kg; ++j) {
-    int best = -1;
     float bv = 0.f;
-    for (int g = 0; g < G; ++g) {
-      if (taken[g >> 5] & (1u << (g & 31))) continue;
-      const float v = sg[g];
-      if (best < 0 || v > bv) { best = g; bv = v; }
-    }
-    taken[best >> 5] |= 1u << (best & 31);
-    gsel[j] = best;
-    gval[j] = bv;
+    int bi = -1;
+#pragma unroll
+    for (int u = 0; u < kSelGroupsPerLane; ++u)
+      if (((avail >> u) & 1u) && (bi < 0 || gv[u] > bv)) { bv = gv[u]; bi = li + L * u; }
+    seg_argmax<L>(bv, bi);
+    if (bi % L == li) avail &= ~(1u << (bi / L));
+    if (li == j) { my_g = bi; my_gv = bv; }
   }
-  float pden = 0.f, pe[kMaxK];
-  for (int j = 0; j < kg; ++j) { pe[j] = expf(gval[j] - gval[0]); pden += pe[j]; }
+  const float g0 = __shfl_sync(0xffffffffu, my_gv, 0, L);
+  const float my_pe = expf(my_gv - g0);
+  float pden = 0.f;
+  for (int j = 0; j < kg; ++j) pden += __shfl_sync(0xffffffffu, my_pe, j, L);
+  const float my_p = my_pe / pden;
   for (int j = 0; j < kg; ++j) {
-    const int g = gsel[j];
-    gidx[(size_t)t * kg + j] = g;
-    const float p = pe[j] / pden;
-    uint32_t used = 0u;  // bit i: i-th member of g already chosen (K <= 32 enforced on host)
-    int esel[kMaxK];
-    float ev[kMaxK];
-    for (int s = 0; s < ke; ++s) {
-      int bi = -1;
-      float bv = 0.f;
-      for (int i = 0; i < K; ++i) {
-        if (used & (1u << i)) continue;
-        const float v = se[tab.member[g * K + i]];
-        if (bi < 0 || v > bv) { bi = i; bv = v; }
-      }
-      used |= 1u << bi;
-      esel[s] = tab.member[g * K + bi];
-      ev[s] = bv;
+    const int g = __shfl_sync(0xffffffffu, my_g, j, L);
+    const float p = __shfl_sync(0xffffffffu, my_p, j, L);
+    if (valid && li == 0) gidx[(size_t)t * kg + j] = g;
+    const float v_l = li < K ? se[tab.member[g * K + li]] : 0.f;
+    bool open = li < K;
+    int my_e = -1;
+    float my_ev = 0.f;
+    for (int s2 = 0; s2 < ke; ++s2) {
+      float bv = open ? v_l : 0.f;
+      int bi = open ? li : -1;
+      seg_argmax<L>(bv, bi);
+      if (bi == li) open = false;
+      if (li == s2) { my_e = (int)tab.member[g * K + bi]; my_ev = bv; }
     }
-    float qden = 0.f, qe[kMaxK];
-    for (int s = 0; s < ke; ++s) { qe[s] = expf(ev[s] - ev[0]); qden += qe[s]; }
-    for (int s = 0; s < ke; ++s) {
-      eidx[(size_t)t * k + j * ke + s] = esel[s];
-      gate[(size_t)t * k + j * ke + s] = p * (qe[s] / qden);
+    const float e0 = __shfl_sync(0xffffffffu, my_ev, 0, L);
+    const float my_qe = expf(my_ev - e0);
+    float qden = 0.f;
+    for (int s2 = 0; s2 < ke; ++s2) qden += __shfl_sync(0xffffffffu, my_qe, s2, L);
+    if (valid && li < ke) {
+      eidx[(size_t)t * k + j * ke + li] = my_e;
+      gate[(size_t)t * k + j * ke + li] = p * (my_qe / qden);
     }
   }
+}
+
+template <int L>
+static void launch_select(const LayerArgs& a, const float* logits, int32_t* gidx, int32_t* eidx, float* gate,
+                          cudaStream_t st) {
+  const int per_block = 256 / L;
+  launch_pdl(router_select_kernel<L>, dim3((a.T + per_block - 1) / per_block), dim3(256), 0, st, logits, a.tab, a.T,
+             a.kg, a.ke, gidx, eidx, gate);
 }
 
 template <int TPW, int RPW, int WT, int WR, int MINB, int UNR>
@@ -363,8 +391,11 @@ cudaError_t launch_route(const LayerArgs& a, const void* x, const void* wg, cons
   if (a.T == 0) return cudaSuccess;
   cudaError_t err = launch_logits(a.bf16, x, wg, bg, we, logits, a.T, a.d, a.G, a.E, st);
   if (err != cudaSuccess) return err;
-  launch_pdl(router_select_kernel, dim3((a.T + 127) / 128), dim3(128), 0, st, (const float*)logits, a.tab, a.T, a.kg,
-             a.ke, gidx, eidx, gate);
+  const int need = a.G > a.K ? a.G : a.K;
+  if (need <= 4) launch_select<4>(a, logits, gidx, eidx, gate, st);
+  else if (need <= 8) launch_select<8>(a, logits, gidx, eidx, gate, st);
+  else if (need <= 16) launch_select<16>(a, logits, gidx, eidx, gate, st);
+  else launch_select<32>(a, logits, gidx, eidx, gate, st);
   prof_mark("router_select", st);
   return cudaGetLastError();
 }

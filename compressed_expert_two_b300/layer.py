@@ -49,7 +49,7 @@ class DeviceLayer:
                 self.resid.A[m_i], self.resid.B[m_i] = t["A"].data_ptr(), t["B"].data_ptr()
             self._resid_t[m] = t
         self.ws_bytes = L.moe_hier_workspace_size(self.desc)
-        self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
+        self.ws = torch.zeros(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
         self.act_dtype = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
 
     @property

@@ -18,17 +18,25 @@
  * Conventions for every entry point
  *   - All tensor pointers are DEVICE pointers owned by the caller, except group_map_host (host
  *     memory, read during the call only).  Row-major, nn.Linear layout (W is [d_out][d_in]).
- *   - The library never allocates, frees or synchronises (except moe_hier_get_status, which
- *     synchronises the given stream).  Work is enqueued on `stream` (a cudaStream_t; NULL = the
- *     legacy default stream) and the call returns.  Scratch memory is the caller's workspace
+ *   - The library never allocates device memory, frees or synchronises (except
+ *     moe_hier_get_status, which synchronises the given stream).  Work is enqueued on `stream`
+ *     (a cudaStream_t; NULL = the legacy default stream) and the call returns.  moe_hier_forward
+ *     also runs its weight-only step (the residual stacks) on a second stream that it creates,
+ *     with two events, on its first call in a host thread (per device); the work forks from and
+ *     rejoins `stream` through those events, so it is also captured by a CUDA graph capture of
+ *     `stream`.  Scratch memory is the caller's workspace
  *     `ws` of `ws_bytes` bytes (>= moe_hier_workspace_size), 256-byte aligned.  Calls that share
  *     a workspace must be ordered on one stream; distinct workspaces may run concurrently.
  *   - Return value: MOE_OK, or a negative moe_status.  MOE_ERR_INVALID / _UNSUPPORTED /
  *     _WORKSPACE are detected on the host before anything is enqueued.  MOE_ERR_CUDA means a
  *     launch failed (cudaGetLastError); earlier steps of the call may already be enqueued.
  *     Conditions found on the device (a bounded wait that ran out) are written to a status word
- *     in the workspace and reported by moe_hier_get_status.
+ *     in the workspace and reported by moe_hier_get_status.  moe_hier_forward clears the word
+ *     when it starts; the stand-alone calls only set it, so a caller that uses them alone
+ *     clears it by zeroing the first 16 bytes of `ws` (a zero-filled workspace starts clear).
  *   - Inputs must be finite; NaN logits give unspecified routing.
+ *   - Device arrays start on 16-byte boundaries (as cudaMalloc and PyTorch allocations do);
+ *     x, y, the weights and the residual codes are checked (MOE_ERR_INVALID otherwise).
  *
  * Shapes (T tokens, d = d_model, f = d_ff, k = k_g * k_e routed experts per token)
  *   x         [T][d]            act dtype          y [T][d] act dtype

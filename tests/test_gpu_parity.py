@@ -64,6 +64,8 @@ CASES = {
     "bf16_zipf": small(T=777, d=384, E=64, G=8, kg=2, ke=3, group_map="contiguous", seed=26,
                        zipf_s=1.2, resid_std=0.2),
     "bf16_one_token": small(T=1, seed=27),
+    "bf16_K32": small(T=300, E=128, G=4, kg=2, ke=3, group_map="perm", seed=36, resid_std=0.2),
+    "bf16_G64": small(T=200, E=128, G=64, kg=3, ke=2, group_map="perm", seed=37, resid_std=0.2),
     "bf16_K1": small(T=200, E=4, G=4, kg=2, ke=1, seed=28),
     "f32_kg2": small(T=130, dtype="f32", resid="f32", r=4, kg=2, ke=1, E=8, G=4, seed=29, resid_std=0.2),
 }
@@ -115,6 +117,43 @@ def test_all_tokens_one_group_and_empty_experts():
     for key in ("expert_begin", "expert_count", "group_begin", "row_begin"):
         assert np.array_equal(p[key].cpu().numpy(), ref[key]), key
     check_y(out["y"], ref["y"])
+
+
+def synthetic_eidx(T, group_map, G, kg, ke, seed, skew=0.0):
+    """Seeded routing decisions: kg distinct groups per token (weights ~ (g+1)^-skew), then ke
+    distinct experts of each chosen group."""
+    rng = np.random.default_rng(seed)
+    members = [np.flatnonzero(group_map == g) for g in range(G)]
+    w = (np.arange(G) + 1.0) ** -skew
+    w /= w.sum()
+    eidx = np.empty((T, kg * ke), dtype=np.int32)
+    for t in range(T):
+        gs = rng.choice(G, size=kg, replace=False, p=w)
+        for j, g in enumerate(gs):
+            eidx[t, j * ke:(j + 1) * ke] = rng.choice(members[g], size=ke, replace=False)
+    return eidx
+
+
+@pytest.mark.parametrize("T,E,G,kg,ke,skew", [(20, 64, 8, 2, 3, 0.0), (64, 32, 8, 1, 2, 0.0),
+                                              (1000, 256, 8, 2, 4, 1.0), (1024, 16, 4, 1, 2, 0.0),
+                                              (1025, 16, 4, 1, 2, 0.0), (3000, 64, 8, 2, 3, 1.2),
+                                              (9000, 8, 2, 1, 2, 0.0), (16384, 64, 8, 2, 3, 2.5)])
+def test_permute_batches(T, E, G, kg, ke, skew):
+    """One-CTA batches (up to 1024 tokens, down to a single warp) and multi-block batches, called
+    twice in a row through the stand-alone entry point: every output bit-exact both times."""
+    cfg = small(T=T, E=E, G=G, kg=kg, ke=ke, seed=40 + T % 97)
+    inp = make_inputs(cfg)
+    layer = device_layer(inp)
+    gm = inp["group_map"].numpy()
+    eidx = synthetic_eidx(T, gm, G, kg, ke, seed=T, skew=skew)
+    ref = oracle.permute(eidx, gm, G, ke)
+    e_dev = torch.from_numpy(eidx).cuda()
+    for _ in range(2):
+        p = layer.permute(e_dev)
+        torch.cuda.synchronize()
+        assert layer.status() == 0
+        for key, want in ref.items():
+            assert np.array_equal(p[key].cpu().numpy(), want), key
 
 
 def test_empty_batch():
