@@ -178,8 +178,8 @@ def test_repeat_calls_are_deterministic():
 
 
 # ------------------------------------------------------------------ the full-size workloads
-def full_size_check(name, n_sample):
-    cfg = CONFIGS[name]
+def full_size_check(name, n_sample, cfg=None):
+    cfg = cfg or CONFIGS[name]
     inp = make_inputs(cfg)
     layer = device_layer(inp)
     out = layer.forward()
@@ -203,3 +203,11 @@ def full_size_check(name, n_sample):
 @pytest.mark.parametrize("name,n", [("mixtral_prefill", 24), ("finegrained_skewed", 64), ("decode", 8)])
 def test_full_size_sampled(name, n):
     full_size_check(name, n)
+
+
+@pytest.mark.parametrize("T,ke,seed", [(2304, 2, 41), (2100, 1, 42)])
+def test_long_k_gate_up_sampled(T, ke, seed):
+    """d_model = 4096 with more than 2048 rows: the CTA-pair double-buffered gate/up kernel, with
+    a ragged last pair (T not a multiple of 256 rows per group); sampled tokens against the oracle."""
+    cfg = small(T=T, d=4096, f=1024, E=8, G=2, kg=1, ke=ke, seed=seed, resid_std=0.2)
+    full_size_check("long_k", 40, cfg)
