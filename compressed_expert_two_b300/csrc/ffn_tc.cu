@@ -2446,9 +2446,9 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   // pair GEMMs: each CTA of a pair holds half of the B tile
   const int pairs = (R + 2 * kTile - 1) / (2 * kTile) + G;
   const int nf_up = up3 ? kNf3 : kNf;
-  // The pair form pays a cluster handshake per CTA; it gains only on long K loops over many rows
-  // (on short ones, or one-wave decode batches, the single-CTA form is faster).
-  const bool down_pair = d % 256 == 0 && f >= 4096 && R >= 2048;
+  // The pair form pays a cluster handshake per CTA; it gains on K loops of d_ff >= 2048 over many
+  // rows (on shorter ones, or one-wave decode batches, the single-CTA form is faster).
+  const bool down_pair = d % 256 == 0 && f >= 2048 && R >= 2048;
   bool ok = make_map(&mX, b.X, Rp, d, kTile) &&
             make_map(&mAhi, b.Ain, (uint64_t)G * 4 * KRP, d, KRP) &&
             make_map(&mWg, wg, (uint64_t)G * f, d, nf_up) && make_map(&mWu, wu, (uint64_t)G * f, d, nf_up) &&
