@@ -38,7 +38,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -58,21 +58,24 @@ def load_peaks():
 
 def recorded_traffic(config: str, kernel: str):
     """DRAM bytes (read + write) per launch of `kernel` on `config` from the committed ncu summary
-    profiles/dram_traffic.json, or None when the kernel sources changed since it was captured."""
+    profiles/dram_traffic.json, or None when the source file that defines the kernel changed since
+    the counters were taken (each entry records that file and its SHA-256)."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as fh:
         rec = json.load(fh)
-    h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "compressed_expert_two_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as fh:
-            h.update(fh.read())
-    if rec.get("csrc_sha256") != h.hexdigest():
+    ent = rec.get("traffic", {}).get(config, {}).get(kernel)
+    if not isinstance(ent, dict):
         return None
-    return rec.get("traffic", {}).get(config, {}).get(kernel)
+    src = os.path.join(ROOT, "compressed_expert_two_b300", "csrc", ent.get("source", ""))
+    if not os.path.isfile(src):
+        return None
+    with open(src, "rb") as fh:
+        if hashlib.sha256(fh.read()).hexdigest() != ent.get("sha256"):
+            return None
+    return ent.get("bytes")
 
 
 def workload_name(cfg) -> str:
@@ -82,6 +85,63 @@ def workload_name(cfg) -> str:
 
 
 # ------------------------------------------------------------------ clocks during the timed region
+class _Nvml:
+    """The few read-only NVML calls the clock sampler needs: the pynvml module when installed,
+    else the driver's libnvidia-ml through ctypes."""
+    SM = 1                                                  # NVML_CLOCK_SM
+
+    def __init__(self):
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.py = pynvml
+            return
+        except Exception:
+            self.py = None
+        import ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        self.ct = ctypes
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def handle_by_uuid(self, uuid):
+        if self.py:
+            return self.py.nvmlDeviceGetHandleByUUID(uuid)
+        h = self.ct.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByUUID(self.ct.c_char_p(uuid.encode()), self.ct.byref(h)) != 0:
+            raise RuntimeError("nvmlDeviceGetHandleByUUID failed")
+        return h
+
+    def _uint(self, fn, h, kind):
+        v = self.ct.c_uint()
+        if fn(h, self.ct.c_int(kind), self.ct.byref(v)) != 0:
+            raise RuntimeError("NVML clock query failed")
+        return v.value
+
+    def max_sm_mhz(self, h):
+        if self.py:
+            return self.py.nvmlDeviceGetMaxClockInfo(h, self.py.NVML_CLOCK_SM)
+        return self._uint(self.lib.nvmlDeviceGetMaxClockInfo, h, self.SM)
+
+    def sm_mhz(self, h):
+        if self.py:
+            return self.py.nvmlDeviceGetClockInfo(h, self.py.NVML_CLOCK_SM)
+        return self._uint(self.lib.nvmlDeviceGetClockInfo, h, self.SM)
+
+    def reasons(self, h):
+        if self.py:
+            try:
+                return self.py.nvmlDeviceGetCurrentClocksEventReasons(h)
+            except AttributeError:
+                return self.py.nvmlDeviceGetCurrentClocksThrottleReasons(h)
+        v = self.ct.c_ulonglong()
+        if self.reasons_fn(h, self.ct.byref(v)) != 0:
+            raise RuntimeError("NVML reasons query failed")
+        return v.value
+
+
 class Clocks:
     """SM clock and clock-event reasons sampled while the timed steps run.
 
@@ -103,26 +163,20 @@ class Clocks:
         self.proc = None
         self.file = None
         try:
-            import pynvml
             import torch
-            pynvml.nvmlInit()
             uuid = str(torch.cuda.get_device_properties(device).uuid)
-            self.handle = pynvml.nvmlDeviceGetHandleByUUID(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
-            self.nvml = pynvml
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.handle, pynvml.NVML_CLOCK_SM)
-        except Exception:
+            self.nvml = _Nvml()
+            self.handle = self.nvml.handle_by_uuid(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+            self.max_mhz = self.nvml.max_sm_mhz(self.handle)
+        except Exception as exc:                      # no NVML: the nvidia-smi sampler below
             self.handle = None
+            self.nvml_error = str(exc)[:120]
 
     def _poll(self):
         nv = self.nvml
         while not self.stop_flag.is_set():
             try:
-                mhz = nv.nvmlDeviceGetClockInfo(self.handle, nv.NVML_CLOCK_SM)
-                try:
-                    rs = nv.nvmlDeviceGetCurrentClocksEventReasons(self.handle)
-                except AttributeError:
-                    rs = nv.nvmlDeviceGetCurrentClocksThrottleReasons(self.handle)
-                self.samples.append((mhz, rs))
+                self.samples.append((nv.sm_mhz(self.handle), nv.reasons(self.handle)))
             except Exception:
                 pass
             time.sleep(0.0005)

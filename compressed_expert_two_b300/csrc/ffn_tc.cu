@@ -1465,8 +1465,8 @@ __global__ void __launch_bounds__(kUp3Warps * 32, 1) ffn_up3_kernel(
 }
 
 // ------------------------------------------------------------------------------------------
-// 4c. Fused gate/up on 256-column MMAs with a double-buffered accumulator (K r = 64 columns,
-//     at most two slots per row).
+// 4c. Fused gate/up on 256-column MMAs with a double-buffered accumulator, on CTA pairs (K r = 64
+//     columns, at most two slots per row).
 //
 // As 4b, but TMEM holds two accumulators acc[b] = [gate 128 | up 128] (512 columns) so that the
 // next tile's K loop runs during this tile's slots, and V_s = A_down^T h_s is accumulated on the
@@ -1474,345 +1474,18 @@ __global__ void __launch_bounds__(kUp3Warps * 32, 1) ffn_up3_kernel(
 // sums of each slot, reading the row's expert block of A_down^T from a transposed FP16 tile in
 // shared memory.  12 warps: base TMA, base MMA, residual MMA, residual TMA, 8 epilogue warps
 // (two per TMEM lane quarter, 64 d_ff columns each).
+//
+// The two CTAs of a cluster take two 128-row tiles of one group (pair tiles as in the pair GEMM)
+// and the same chunk of d_ff tiles; rank 0 issues every MMA with M = 256 (cta_group::2).  For the
+// base product rank 0 holds the W_gate tile and rank 1 the W_up tile of B (N = 256 = gate | up),
+// so a K step lands 16 KB of X and 16 KB of W per SM instead of 16 + 32 KB: the shared-memory
+// fill rate, not the tensor pipe, bounds a single CTA here.  The residual MMAs (N = 128 each)
+// split B_gate / B_up by rows (64 per CTA); each CTA keeps its own U~ tiles, A_down^T tile and
+// epilogue.  Both CTAs' loads of a stage complete on rank 0's barrier; rank 0's commits arrive on
+// the barriers of the CTAs that wait on them; the epilogues of both CTAs arrive on rank 0's
+// barriers.
 // ------------------------------------------------------------------------------------------
 constexpr int kUp4EpiWarps = 8;
-
-template <int KE>
-__global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up4_kernel(
-    const __grid_constant__ CUtensorMap mX, const __grid_constant__ CUtensorMap mWg,
-    const __grid_constant__ CUtensorMap mWu, const __grid_constant__ CUtensorMap mBg,
-    const __grid_constant__ CUtensorMap mBu, const __grid_constant__ CUtensorMap mAdt, const UpArgs p) {
-  pdl_wait();
-  pdl_trigger();
-  constexpr int KRP = 64, NF = kNf3, STAGES = kStages3;
-  constexpr uint32_t X_BYTES = kTile * 128, W_BYTES = 2 * NF * 128, STAGE_BYTES = X_BYTES + W_BYTES;
-  constexpr uint32_t BRES_BYTES = NF * KRP * 2;            // B_gate or B_up tile: 128 rows x KRP (FP16)
-  constexpr uint32_t ADT_BYTES = NF * KRP * 2;             // A_down^T transposed: 128 d_ff columns x KRP (FP16)
-  constexpr uint32_t UT_BYTES = kTile * KRP * 2;
-  static_assert(KE >= 1 && KE <= 2, "slots");
-
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full[STAGES], empty[STAGES];
-  __shared__ uint64_t base_full[2], acc_empty[2];
-  __shared__ uint64_t rb_full, rb_empty, ad_full, ad_empty;
-  __shared__ uint64_t acc_full, acc_read, u_ready, fin1, fin2;
-  __shared__ uint32_t tmem_base;
-  __shared__ int abort_flag;
-
-  int g, r0, r1;
-  if (!tile_of(p.row_begin, p.G, blockIdx.y, g, r0, r1)) return;
-  const int chunk = blockIdx.x;
-  const int ft0 = chunk * p.ftiles_per_chunk;
-  const int ft1 = min(ft0 + p.ftiles_per_chunk, p.n_ftiles);
-  if (ft0 >= ft1) return;
-  const int nft = ft1 - ft0;
-  const int nkb = p.d / 64;
-  const int f = p.f;
-
-  uint8_t* smem = align1024(smem_raw);
-  uint8_t* sStage = smem;
-  uint8_t* sBg = sStage + STAGES * STAGE_BYTES;
-  uint8_t* sBu = sBg + BRES_BYTES;
-  uint8_t* sAdt = sBu + BRES_BYTES;
-  uint8_t* sUg = sAdt + ADT_BYTES;
-  uint8_t* sUu = sUg + UT_BYTES;
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const tc::Abort ab{&abort_flag, p.status};
-  constexpr int kEpiArrive = kUp4EpiWarps;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) { tc::bar_init(&full[s], 1); tc::bar_init(&empty[s], 1); }
-    for (int b = 0; b < 2; ++b) { tc::bar_init(&base_full[b], 1); tc::bar_init(&acc_empty[b], kEpiArrive); }
-    tc::bar_init(&rb_full, 1); tc::bar_init(&rb_empty, 1);
-    tc::bar_init(&ad_full, 1); tc::bar_init(&ad_empty, kEpiArrive);
-    tc::bar_init(&acc_full, 1);
-    tc::bar_init(&acc_read, kEpiArrive);
-    tc::bar_init(&u_ready, kEpiArrive);
-    tc::bar_init(&fin1, 1); tc::bar_init(&fin2, 1);
-    abort_flag = 0;
-    tc::bar_fence_init();
-  }
-  if (warp == 1) tc::tmem_alloc(&tmem_base, 512);
-  tc::fence_before();
-  __syncthreads();
-  tc::fence_after();
-  const uint32_t tmem = tmem_base;
-  auto warp_arrive = [&](uint64_t* b) {
-    __syncwarp();
-    if (lane == 0) tc::bar_arrive(b);
-  };
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer of the base stages (X, W_gate, W_up of one 128-column tile)
-      tc::prefetch_map(&mX); tc::prefetch_map(&mWg); tc::prefetch_map(&mWu);
-      int kc = 0;
-      bool ok = true;
-      for (int lt = 0; lt < nft && ok; ++lt) {
-        const int n0 = (ft0 + lt) * NF;
-        for (int kb = 0; kb < nkb; ++kb, ++kc) {
-          const int s = kc % STAGES, it = kc / STAGES;
-          if (kc >= STAGES && !tc::bar_wait(&empty[s], (it - 1) & 1, ab, 71)) { ok = false; break; }
-          uint8_t* st = sStage + s * STAGE_BYTES;
-          tc::bar_expect_tx(&full[s], STAGE_BYTES);
-          tc::tma_load_2d(st, &mX, &full[s], kb * 64, r0);
-          tc::tma_load_2d(st + X_BYTES, &mWg, &full[s], kb * 64, g * f + n0);
-          tc::tma_load_2d(st + X_BYTES + NF * 128, &mWu, &full[s], kb * 64, g * f + n0);
-        }
-      }
-      if (abort_flag) tc::drain_copies();
-    }
-  } else if (warp == 3) {
-    if (lane == 0) {
-      // ---------------- TMA producer of the residual tiles of each d_ff tile
-      tc::prefetch_map(&mBg); tc::prefetch_map(&mBu); tc::prefetch_map(&mAdt);
-      for (int lt = 0; lt < nft; ++lt) {
-        const int n0 = (ft0 + lt) * NF;
-        if (lt > 0 && !tc::bar_wait(&rb_empty, (lt - 1) & 1, ab, 72)) break;
-        tc::bar_expect_tx(&rb_full, 2 * BRES_BYTES);
-        tc::tma_load_2d(sBg, &mBg, &rb_full, 0, g * f + n0);
-        tc::tma_load_2d(sBu, &mBu, &rb_full, 0, g * f + n0);
-        if (lt > 0 && !tc::bar_wait(&ad_empty, (lt - 1) & 1, ab, 73)) break;
-        tc::bar_expect_tx(&ad_full, ADT_BYTES);
-        tc::tma_load_2d(sAdt, &mAdt, &ad_full, 0, g * f + n0);
-      }
-      if (abort_flag) tc::drain_copies();
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- base MMA issuer: acc[lt & 1] = X [Wg | Wu]^T, N = 256
-      constexpr uint32_t id_base = tc::idesc_bf16(kTile, 2 * NF);
-      int kc = 0;
-      bool ok = true;
-      for (int lt = 0; lt < nft && ok; ++lt) {
-        const int b = lt & 1;
-        if (lt >= 2 && !tc::bar_wait(&acc_empty[b], ((lt >> 1) - 1) & 1, ab, 74)) break;
-        tc::fence_after();
-        const uint32_t dcol = tmem + b * 2 * NF;
-        for (int kb = 0; kb < nkb; ++kb, ++kc) {
-          const int s = kc % STAGES, it = kc / STAGES;
-          if (!tc::bar_wait(&full[s], it & 1, ab, 75)) { ok = false; break; }
-          tc::fence_after();
-          const uint32_t a0 = tc::smem_u32(sStage + s * STAGE_BYTES);
-          const uint32_t b0 = a0 + X_BYTES;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            tc::mma_bf16(dcol, tc::sdesc(a0 + 32 * k), tc::sdesc(b0 + 32 * k), id_base, (kb | k) != 0);
-          tc::mma_commit(&empty[s]);
-        }
-        if (!ok) break;
-        tc::mma_commit(&base_full[b]);
-      }
-      tc::mma_commit(&fin1);
-      const uint64_t t0 = tc::now_ns();
-      while (!tc::bar_test(&fin1, 0) && tc::now_ns() - t0 < tc::kWaitNs) {}
-    }
-  } else if (warp == 2) {
-    if (lane == 0) {
-      // ---------------- residual issuer: acc[b] += D_s [Bg | Bu]^T
-      constexpr uint32_t id_res = tc::idesc_f16(kTile, NF);
-      const uint32_t ug = tc::smem_u32(sUg), uu = tc::smem_u32(sUu);
-      const uint32_t bg = tc::smem_u32(sBg), bu = tc::smem_u32(sBu);
-      const int n_slots = nft * KE;
-      bool ok = true;
-      for (int sig = 0; sig < n_slots && ok; ++sig) {
-        const int lt = sig / KE, s = sig % KE, b = lt & 1;
-        if (s == 0) {
-          if (!tc::bar_wait(&base_full[b], (lt >> 1) & 1, ab, 76)) { ok = false; break; }
-          if (!tc::bar_wait(&rb_full, lt & 1, ab, 77)) { ok = false; break; }
-        }
-        if (!tc::bar_wait(&u_ready, sig & 1, ab, 78)) { ok = false; break; }
-        if (s > 0 && !tc::bar_wait(&acc_read, (sig - 1) & 1, ab, 79)) { ok = false; break; }
-        tc::fence_after();
-        const uint32_t dcol = tmem + b * 2 * NF;
-#pragma unroll
-        for (int kk = 0; kk < KRP / 16; ++kk) {
-          const uint32_t off = (kk & 3) * 32;
-          tc::mma_bf16(dcol, tc::sdesc(ug + off), tc::sdesc(bg + off), id_res, 1u);
-          tc::mma_bf16(dcol + NF, tc::sdesc(uu + off), tc::sdesc(bu + off), id_res, 1u);
-        }
-        tc::mma_commit(&acc_full);
-        if (s == KE - 1) tc::mma_commit(&rb_empty);
-      }
-      tc::mma_commit(&fin2);
-      const uint64_t t0 = tc::now_ns();
-      while (!tc::bar_test(&fin2, 0) && tc::now_ns() - t0 < tc::kWaitNs) {}
-    }
-  } else {
-    // ---------------- epilogue: one thread per (tile row, half of 64 d_ff columns)
-    const int q = warp & 3, half = (warp - kUpEpiWarp0) >> 2, row = q * 32 + lane, i = r0 + row;
-    auto ewait = [&](uint64_t* b, uint32_t par, int where) -> bool {
-      const bool r = tc::bar_wait(b, par, ab, where);
-      return __all_sync(0xffffffffu, r);
-    };
-    const bool valid = i < r1;
-    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    const int c0 = half * 64;
-    uint8_t* sU = half == 0 ? sUg : sUu;
-    int le[KE];
-    float gt[KE];
-#pragma unroll
-    for (int s = 0; s < KE; ++s) { le[s] = 0; gt[s] = 0.f; }
-    const __half* urow = p.U;
-    if (valid) {
-      const int b = p.row_asg[i], t = b / p.kg, j = b % p.kg, k = p.kg * KE;
-#pragma unroll
-      for (int s = 0; s < KE; ++s) {
-        const int e = p.eidx[(size_t)t * k + j * KE + s];
-        le[s] = p.tab.local_of[e];
-        gt[s] = p.gate[(size_t)t * k + j * KE + s];
-      }
-      urow = p.U + (size_t)i * 2 * KRP + half * KRP;
-    }
-    {
-      uint4* z = reinterpret_cast<uint4*>(sU + (row >> 3) * 1024 + (row & 7) * 128);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) z[c] = make_uint4(0, 0, 0, 0);
-    }
-    auto load_u = [&](int s, uint32_t (&pk)[8]) {
-      if (!valid) return;
-      const uint4* u4 = reinterpret_cast<const uint4*>(urow + le[s] * kRank);
-      const uint4 a = u4[0], b = u4[1];
-      pk[0] = a.x; pk[1] = a.y; pk[2] = a.z; pk[3] = a.w;
-      pk[4] = b.x; pk[5] = b.y; pk[6] = b.z; pk[7] = b.w;
-    };
-    auto zero_block = [&](int blk) {
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, blk * kRank, kTile)) = z;
-      *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, blk * kRank + 8, kTile)) = z;
-    };
-    int nz_pos = -1, nz_neg = -1;
-    uint32_t unext[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) unext[c] = 0u;
-    auto build_delta = [&](int s) {
-      if (!valid) return;
-      const int pos = le[s], neg = s > 0 ? le[s - 1] : -1;
-      if (neg >= 0) {
-        uint4* b0 = reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, neg * kRank, kTile));
-        uint4* b1 = reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, neg * kRank + 8, kTile));
-        const uint4 v0 = *b0, v1 = *b1;
-        constexpr uint32_t F = 0x80008000u;          // exact FP16 negation
-        *b0 = make_uint4(v0.x ^ F, v0.y ^ F, v0.z ^ F, v0.w ^ F);
-        *b1 = make_uint4(v1.x ^ F, v1.y ^ F, v1.z ^ F, v1.w ^ F);
-      }
-      if (nz_neg >= 0 && nz_neg != pos && nz_neg != neg) zero_block(nz_neg);
-      if (nz_pos >= 0 && nz_pos != pos && nz_pos != neg) zero_block(nz_pos);
-      *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, pos * kRank, kTile)) =
-          make_uint4(unext[0], unext[1], unext[2], unext[3]);
-      *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, pos * kRank + 8, kTile)) =
-          make_uint4(unext[4], unext[5], unext[6], unext[7]);
-      nz_pos = pos; nz_neg = neg;
-    };
-
-    load_u(0, unext);
-    build_delta(0);
-    tc::fence_async_smem();
-    warp_arrive(&u_ready);
-    if (KE > 1) load_u(KE > 1 ? 1 : 0, unext);
-    else if (nft > 1) load_u(0, unext);
-
-    // V partials of this row over this thread's columns, per slot, as FP32 pairs (k, k + 1)
-    float2 vacc[KE][kRank / 2];
-#pragma unroll
-    for (int s = 0; s < KE; ++s)
-#pragma unroll
-      for (int k = 0; k < kRank / 2; ++k) vacc[s][k] = make_float2(0.f, 0.f);
-
-    bool ok = true;
-    int sig = 0;
-    for (int lt = 0; lt < nft && ok; ++lt) {
-      const int bsel = lt & 1;
-      const uint32_t acc_col = bsel * 2 * NF;
-      if (!ewait(&ad_full, lt & 1, 80)) { ok = false; break; }
-      float hs[64];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) hs[c] = 0.f;
-#pragma unroll
-      for (int s = 0; s < KE; ++s, ++sig) {
-        if (!ewait(&acc_full, sig & 1, 81)) { ok = false; break; }
-        tc::fence_after();
-        const uint8_t* arow = sAdt + le[s] * kRank * 2;       // this row's expert block, column stride KRP
-#pragma unroll
-        for (int bt = 0; bt < 4; ++bt) {
-          uint32_t av[16], bv[16];
-          tc::tmem_ld16(tmem + lane_off + acc_col + c0 + 16 * bt, av);
-          tc::tmem_ld16(tmem + lane_off + acc_col + NF + c0 + 16 * bt, bv);
-          tc::tmem_ld_wait();
-          if (bt == 3) {
-            // this thread has read acc for this slot: the next slot's residual may land
-            tc::fence_before();
-            warp_arrive(&acc_read);
-            if (s == KE - 1) warp_arrive(&acc_empty[bsel]);
-          }
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float h = silu_fast(__uint_as_float(av[e])) * __uint_as_float(bv[e]);
-            hs[16 * bt + e] += gt[s] * h;
-            // v_k += h * A_down^T[k][c] for the 16 ranks of the row's expert
-            const int c = c0 + 16 * bt + e;
-            const uint4* ap = reinterpret_cast<const uint4*>(arow + (size_t)c * KRP * 2);
-            const uint4 w0 = ap[0], w1 = ap[1];
-            const uint32_t ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-            const float2 h2 = make_float2(h, h);
-#pragma unroll
-            for (int k2 = 0; k2 < 8; ++k2) {
-              const float2 a2 = __half22float2(*reinterpret_cast<const __half2*>(&ww[k2]));
-              vacc[s][k2] = fma2(h2, a2, vacc[s][k2]);
-            }
-          }
-        }
-        const bool more = s + 1 < KE || lt + 1 < nft;
-        if (more) {
-          build_delta(s + 1 < KE ? s + 1 : 0);
-          tc::fence_async_smem();
-          warp_arrive(&u_ready);
-          const int s2 = (s + 2) % KE;
-          const int lt2 = lt + (s + 2) / KE;
-          if (lt2 < nft) load_u(s2, unext);
-        }
-      }
-      if (!ok) break;
-      warp_arrive(&ad_empty);                        // done with this tile's A_down^T
-      if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(p.hsum + (size_t)i * f + (ft0 + lt) * NF + c0);
-#pragma unroll
-        for (int c = 0; c < 64; c += 8)
-          dst[c / 8] = make_uint4(tc::pack_bf16(hs[c], hs[c + 1]), tc::pack_bf16(hs[c + 2], hs[c + 3]),
-                                  tc::pack_bf16(hs[c + 4], hs[c + 5]), tc::pack_bf16(hs[c + 6], hs[c + 7]));
-      }
-    }
-    if (ok && valid) {
-      // partial over this half's columns: V parts [chunk][half]
-      float* vp = p.Vpart + (((size_t)chunk * 2 + half) * p.R + i) * KE * kRank;
-#pragma unroll
-      for (int s = 0; s < KE; ++s)
-#pragma unroll
-        for (int k = 0; k < kRank; k += 4)
-          *reinterpret_cast<float4*>(vp + s * kRank + k) =
-              make_float4(gt[s] * vacc[s][k / 2].x, gt[s] * vacc[s][k / 2].y, gt[s] * vacc[s][k / 2 + 1].x,
-                          gt[s] * vacc[s][k / 2 + 1].y);
-    }
-  }
-  tc::fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc::fence_after();
-    tc::tmem_dealloc(tmem, 512);
-  }
-}
-
-// ------------------------------------------------------------------------------------------
-// 4d. 4c on CTA pairs.  The two CTAs of a cluster take two 128-row tiles of one group (pair
-//     tiles as in the pair GEMM) and the same chunk of d_ff tiles; rank 0 issues every MMA with
-//     M = 256 (cta_group::2).  For the base product rank 0 holds the W_gate tile and rank 1 the
-//     W_up tile of B (N = 256 = gate | up), so a K step lands 16 KB of X and 16 KB of W per SM
-//     instead of 16 + 32 KB: the shared-memory fill rate, not the tensor pipe, bounds the
-//     single-CTA form.  The residual MMAs (N = 128 each) split B_gate / B_up by rows (64 per CTA);
-//     each CTA keeps its own U~ tiles, A_down^T tile (CUDA-core V) and epilogue.  Both CTAs'
-//     loads of a stage complete on rank 0's barrier; rank 0's commits arrive on the barriers of
-//     the CTAs that wait on them; the epilogues of both CTAs arrive on rank 0's barriers.
-// ------------------------------------------------------------------------------------------
 constexpr int kStages4p = 5;
 
 template <int KE>
@@ -2337,20 +2010,6 @@ static cudaError_t launch_up_ke(const CUtensorMap* maps, const UpArgs& p, int nc
 }
 
 template <int KE>
-static cudaError_t launch_up4(const CUtensorMap* maps, const UpArgs& p, int nchunks, int tiles, cudaStream_t stream) {
-  const size_t smem = 1024 + (size_t)kStages3 * (kTile * 128 + 2 * kNf3 * 128) + 2 * (size_t)(kNf3 * 64 * 2) +
-                      (size_t)kNf3 * 64 * 2 + 2 * (size_t)(kTile * 64 * 2);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = set_smem(ffn_up4_kernel<KE>, smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  return launch_pdl(ffn_up4_kernel<KE>, dim3(nchunks, tiles), dim3(kUpWarps * 32), smem, stream, maps[0], maps[1],
-                    maps[2], maps[3], maps[4], maps[5], p);
-}
-
-template <int KE>
 static cudaError_t launch_up4p(const CUtensorMap* maps, const UpArgs& p, int nchunks, int pairs, cudaStream_t stream) {
   const size_t smem = 1024 + (size_t)kStages4p * (kTile * 128 + kNf3 * 128) + 2 * (size_t)((kNf3 / 2) * 64 * 2) +
                       (size_t)kNf3 * 64 * 2 + 2 * (size_t)(kTile * 64 * 2);
@@ -2388,7 +2047,7 @@ static cudaError_t launch_up(const CUtensorMap* maps, const UpArgs& p, int nchun
   }
 }
 
-// The double-buffered form (4c) hides its heavier epilogue (V on the CUDA cores) only behind
+// The double-buffered pair form (4c) hides its heavier epilogue (V on the CUDA cores) only behind
 // long K loops over many rows; shorter ones run the single-buffered form (4b).
 static bool up4_ok(const LayerArgs& a) { return up3_ok(a) && a.d >= 4096 && a.R >= 2048; }
 
@@ -2429,7 +2088,6 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   const PrepArgs pa = prep_args(a, rp, b);
   const bool u_simt = R <= kUSimtMaxRows;
   const bool up3 = up3_ok(a), up4 = up4_ok(a);
-  const bool up4p = up4;                    // 4c runs in its CTA-pair form (4d)
   if (!prep_done && (e = launch_resid_prep(a, rp, b, st)) != cudaSuccess) return e;
 
   // 2. rows of x in (group, token) order (the CUDA-core U kernel writes them itself)
@@ -2486,17 +2144,15 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   p.R = R; p.n_ftiles = f / nf_up;
   const int nchunks = tc_up_chunks(a);
   p.ftiles_per_chunk = (p.n_ftiles + nchunks - 1) / nchunks;
-  if (up4p) {
+  if (up4) {
     CUtensorMap mBgP, mBuP;     // halves of the B_gate / B_up tiles (64 rows per CTA of a pair)
     if (!make_map(&mBgP, b.Bgs, (uint64_t)G * f, KRP, kNf3 / 2) || !make_map(&mBuP, b.Bus, (uint64_t)G * f, KRP, kNf3 / 2))
       return cudaErrorInvalidValue;
     const CUtensorMap mp[6] = {mX, mWg, mWu, mBgP, mBuP, mAdt};
     e = a.ke == 1 ? launch_up4p<1>(mp, p, nchunks, pairs, st) : launch_up4p<2>(mp, p, nchunks, pairs, st);
   } else {
-    const CUtensorMap maps[6] = {mX, mWg, mWu, mBg, mBu, up4 ? mAdt : mAd};
-    if (up4)
-      e = a.ke == 1 ? launch_up4<1>(maps, p, nchunks, tiles, st) : launch_up4<2>(maps, p, nchunks, tiles, st);
-    else if (up3)
+    const CUtensorMap maps[6] = {mX, mWg, mWu, mBg, mBu, mAd};
+    if (up3)
       e = a.ke == 1 ? launch_up3<1>(maps, p, nchunks, tiles, st) : launch_up3<2>(maps, p, nchunks, tiles, st);
     else
       e = KRP == 128 ? launch_up<128>(maps, p, nchunks, tiles, st) : launch_up<64>(maps, p, nchunks, tiles, st);
