@@ -100,6 +100,23 @@ __global__ void __launch_bounds__(WT * WR * 32, MINB) router_logits_bf16_kernel(
 // exact for BF16 x BF16 -- and per add), then the xor butterfly 16, 8, 4, 2, 1.
 constexpr int kRtTok = 32, kRtRows = 16, kRtDC = 256, kRtStages = 3;
 
+// The xor butterfly 16, 8, 4, 2, 1 of 32 per-lane values v[0..31] at once: at the step of
+// distance k a lane keeps the half of its values whose index bit matches its own lane bit, adds
+// the partner's copy of each (own + partner, the butterfly's add for that lane), and hands the
+// other half over.  Lane l returns the butterfly total of value l, bit for bit.
+__device__ __forceinline__ float butterfly_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int k = 16; k >= 1; k >>= 1) {
+    const bool hi = (lane & k) != 0;
+#pragma unroll
+    for (int j = 0; j < k; ++j) {
+      const float keep = hi ? v[j + k] : v[j], send = hi ? v[j] : v[j + k];
+      v[j] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, k));
+    }
+  }
+  return v[0];
+}
+
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem)), "l"(gmem)
                : "memory");
@@ -175,23 +192,22 @@ __global__ void __launch_bounds__(256, 2) router_logits_smem_kernel(
     if (cn < nchunk) load_chunk(cn, cn % kRtStages);
     cp_async_commit();
   }
+  // the butterfly of each of the 64 sums, as two reduce-scatters of 32 sums each: lane l ends with
+  // sum l of each half (tokens 0..3 / 4..7) and every add is the butterfly's own add
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+  for (int hf = 0; hf < 2; ++hf) {
+    float v[32];
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) acc[i][q] = __fadd_rn(acc[i][q], __shfl_xor_sync(0xffffffffu, acc[i][q], o));
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int t = t_base + tg * 8 + i, rr = r_base + rg * 8 + q;
-      if (((i * 8 + q) & 31) == lane && t < Tn && rr < R) {
-        float v = acc[i][q];
-        if (rr < G && bg != nullptr) v = __fadd_rn(v, bg[rr]);
-        logits[(size_t)t * R + rr] = v;
-      }
+    for (int o = 0; o < 32; ++o) v[o] = acc[4 * hf + (o >> 3)][o & 7];
+    const float s = butterfly_scatter32(v, lane);
+    const int i = 4 * hf + (lane >> 3), q = lane & 7;
+    const int t = t_base + tg * 8 + i, rr = r_base + rg * 8 + q;
+    if (t < Tn && rr < R) {
+      float out = s;
+      if (rr < G && bg != nullptr) out = __fadd_rn(out, bg[rr]);
+      logits[(size_t)t * R + rr] = out;
     }
+  }
 }
 
 // FP32 router logits (same canonical order; products rounded before the add, no contraction).
