@@ -1115,7 +1115,7 @@ __global__ void __launch_bounds__(kUp3Warps * 32, 1) ffn_up3_kernel(
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full[STAGES], empty[STAGES];
-  __shared__ uint64_t base_full, acc_empty, rb_full, rb_empty, ad_full, ad_empty;
+  __shared__ uint64_t acc_empty, rb_full, rb_empty, ad_full, ad_empty;
   __shared__ uint64_t acc_full, acc_read, u_ready, h_ready[2], v_done[2], fin1, fin2;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
@@ -1143,7 +1143,7 @@ __global__ void __launch_bounds__(kUp3Warps * 32, 1) ffn_up3_kernel(
   constexpr int kEpiArrive = kUp3EpiWarps;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { tc::bar_init(&full[s], 1); tc::bar_init(&empty[s], 1); }
-    tc::bar_init(&base_full, 1); tc::bar_init(&acc_empty, kEpiArrive);
+    tc::bar_init(&acc_empty, kEpiArrive);
     tc::bar_init(&rb_full, 1); tc::bar_init(&rb_empty, 1); tc::bar_init(&ad_full, 1); tc::bar_init(&ad_empty, 1);
     tc::bar_init(&acc_full, 1);
     tc::bar_init(&acc_read, kEpiArrive);
@@ -1203,8 +1203,12 @@ __global__ void __launch_bounds__(kUp3Warps * 32, 1) ffn_up3_kernel(
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---------------- base MMA issuer: acc = X [Wg | Wu]^T, N = 256
+      // ---------------- base MMA issuer: acc = X [Wg | Wu]^T, N = 256, then slot 0's residual
+      //                  acc += D_0 [Bg | Bu]^T right behind the K loop
       constexpr uint32_t id_base = tc::idesc_bf16(kTile, 2 * NF);
+      constexpr uint32_t id_res = tc::idesc_f16(kTile, NF);
+      const uint32_t ug = tc::smem_u32(sUg), uu = tc::smem_u32(sUu);
+      const uint32_t bg = tc::smem_u32(sBg), bu = tc::smem_u32(sBu);
       int kc = 0;
       bool ok = true;
       for (int lt = 0; lt < nft && ok; ++lt) {
@@ -1222,7 +1226,17 @@ __global__ void __launch_bounds__(kUp3Warps * 32, 1) ffn_up3_kernel(
           tc::mma_commit(&empty[s]);
         }
         if (!ok) break;
-        tc::mma_commit(&base_full);
+        if (!tc::bar_wait(&rb_full, lt & 1, ab, 58)) break;
+        if (!tc::bar_wait(&u_ready, (lt * KE) & 1, ab, 60)) break;
+        tc::fence_after();
+#pragma unroll
+        for (int kk = 0; kk < KRP / 16; ++kk) {
+          const uint32_t off = (kk & 3) * 32;
+          tc::mma_bf16(tmem, tc::sdesc(ug + off), tc::sdesc(bg + off), id_res, 1u);
+          tc::mma_bf16(tmem + NF, tc::sdesc(uu + off), tc::sdesc(bu + off), id_res, 1u);
+        }
+        tc::mma_commit(&acc_full);
+        if (KE == 1) tc::mma_commit(&rb_empty);
       }
       tc::mma_commit(&fin1);
       const uint64_t t0 = tc::now_ns();
@@ -1230,7 +1244,8 @@ __global__ void __launch_bounds__(kUp3Warps * 32, 1) ffn_up3_kernel(
     }
   } else if (warp == 2) {
     if (lane == 0) {
-      // ---------------- residual issuer: acc += D_s [Bg | Bu]^T; V_s += h_s Adn^T (one slot behind)
+      // ---------------- residual issuer: acc += D_s [Bg | Bu]^T for slots s >= 1; V_s += h_s Adn^T
+      //                  (one slot behind)
       constexpr uint32_t id_res = tc::idesc_f16(kTile, NF);
       constexpr uint32_t id_v = tc::idesc_f16(kTile, KRP);
       const uint32_t ug = tc::smem_u32(sUg), uu = tc::smem_u32(sUu);
@@ -1253,15 +1268,16 @@ __global__ void __launch_bounds__(kUp3Warps * 32, 1) ffn_up3_kernel(
       bool ok = true;
       for (int sig = 0; sig < n_slots && ok; ++sig) {
         const int lt = sig / KE, s = sig % KE;
-        // V of the previous tile's last slot goes first (the new tile's base K loop is long);
-        // inside a tile, V of slot s - 1 follows R_s so that R_s does not wait for h_{s-1}
-        if (s == 0 && sig >= 1 && !issue_v(sig - 1)) { ok = false; break; }
+        // slot 0's residual is the base issuer's; the V of the previous tile's last slot goes
+        // here (the new tile's base K loop is long); inside a tile, V of slot s - 1 follows R_s
+        // so that R_s does not wait for h_{s-1}
+        (void)lt;
         if (s == 0) {
-          if (!tc::bar_wait(&base_full, lt & 1, ab, 58)) { ok = false; break; }
-          if (!tc::bar_wait(&rb_full, lt & 1, ab, 59)) { ok = false; break; }
+          if (sig >= 1 && !issue_v(sig - 1)) { ok = false; break; }
+          continue;
         }
         if (!tc::bar_wait(&u_ready, sig & 1, ab, 60)) { ok = false; break; }
-        if (s > 0 && !tc::bar_wait(&acc_read, (sig - 1) & 1, ab, 61)) { ok = false; break; }
+        if (!tc::bar_wait(&acc_read, (sig - 1) & 1, ab, 61)) { ok = false; break; }
         tc::fence_after();
 #pragma unroll
         for (int kk = 0; kk < KRP / 16; ++kk) {
@@ -1271,7 +1287,7 @@ __global__ void __launch_bounds__(kUp3Warps * 32, 1) ffn_up3_kernel(
         }
         tc::mma_commit(&acc_full);
         if (s == KE - 1) tc::mma_commit(&rb_empty);
-        if (s > 0 && !issue_v(sig - 1)) { ok = false; break; }
+        if (!issue_v(sig - 1)) { ok = false; break; }
       }
       if (ok && n_slots > 0) issue_v(n_slots - 1);
       tc::mma_commit(&fin2);
