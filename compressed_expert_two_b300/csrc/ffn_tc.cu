@@ -230,9 +230,9 @@ __global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ x, const in
 // 3'. U on the CUDA cores, for batches of few rows (decode): block (row i, matrix m) computes
 //     (blocks m = 0 also write the gathered row X[i] of step 2)
 //     U[i][m*KRP + o] = sum_c x[t(i)][c] A_m,e_j^T[k][c] (o = j*r + k) for the K experts of the
-//     row's group straight from the INT4 codes; warp w takes 8 outputs at a time, lanes stride
-//     over c in 32-element chunks (one 16-byte load of codes per output and chunk), FP32
-//     accumulation, FP16 out, padding columns zero.
+//     row's group straight from the INT4 codes; block z of the row takes 32 of them, warp w four,
+//     lanes stride over c in 32-element chunks (one 16-byte load of codes per output and chunk,
+//     four chunks' loads in flight together), FP32 accumulation, FP16 out, padding columns zero.
 //     Codes become BF16 values without a per-element conversion: a nibble q or'ed into the
 //     mantissa of the BF16 number 128 (bits 0x4300) is the BF16 number 128 + q, and subtracting
 //     136 leaves q - 8 exactly (the exponent-bias conversion used by weight-only quantised GEMM
@@ -287,9 +287,10 @@ __device__ __forceinline__ float dot8_int4(uint32_t w, uint32_t X0, uint32_t X1,
   return acc;
 }
 
-constexpr int kUSimtOut = 8;    // outputs per warp pass
+constexpr int kUSimtOut = 4;    // outputs per warp
+constexpr int kUSimtChunks = 4; // 32-element chunks per lane whose loads are in flight together
 
-__global__ void __launch_bounds__(256) u_simt_kernel(const __nv_bfloat16* __restrict__ x,
+__global__ void __launch_bounds__(256, 2) u_simt_kernel(const __nv_bfloat16* __restrict__ x,
                                                      const int32_t* __restrict__ row_asg,
                                                      const int32_t* __restrict__ eidx, PrepArgs p, GroupTable tab,
                                                      int kg, int ke, __half* __restrict__ U,
@@ -304,57 +305,69 @@ __global__ void __launch_bounds__(256) u_simt_kernel(const __nv_bfloat16* __rest
   for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
     const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)t * d + c);
     *reinterpret_cast<uint4*>(xs + c) = v;
-    if (m == 0) *reinterpret_cast<uint4*>(X + (size_t)i * d + c) = v;   // the row in (group, token) order
+    if (m == 0 && blockIdx.z == 0) *reinterpret_cast<uint4*>(X + (size_t)i * d + c) = v;   // the row in (group, token) order
   }
   __syncthreads();
   const ResidView& v = p.A[m];
   const uint8_t* codes = (const uint8_t*)v.vals;
   const int nchunk = d / 32;                                  // 32-element chunks of a rank row
-  for (int ob = warp * kUSimtOut; ob < KRP; ob += nwarps * kUSimtOut) {
-    const uint8_t* crow[kUSimtOut];
-    const __half* srow[kUSimtOut];
-    bool live[kUSimtOut];
+  // block z takes outputs [z * nwarps * 4, ...) of the row's 2 x KRP; warp w four of them
+  const int ob = (blockIdx.z * nwarps + warp) * kUSimtOut;
+  if (ob >= KRP) return;
+  const uint8_t* crow[kUSimtOut];
+  const __half* srow[kUSimtOut];
+  bool live[kUSimtOut];
 #pragma unroll
-    for (int q = 0; q < kUSimtOut; ++q) {
-      const int o = ob + q, j = o / r, k = o % r;
-      live[q] = o < KRP && j < K;
-      const size_t row = live[q] ? (size_t)tab.member[g * K + j] * r + k : 0;
-      crow[q] = codes + row * (d / 2);
-      srow[q] = v.scales + row * (d / kQGroup);
-    }
-    float acc[kUSimtOut];
+  for (int q = 0; q < kUSimtOut; ++q) {
+    const int o = ob + q, j = o / r, k = o % r;
+    live[q] = o < KRP && j < K;
+    const size_t row = live[q] ? (size_t)tab.member[g * K + j] * r + k : 0;
+    crow[q] = codes + row * (d / 2);
+    srow[q] = v.scales + row * (d / kQGroup);
+  }
+  float acc[kUSimtOut];
 #pragma unroll
-    for (int q = 0; q < kUSimtOut; ++q) acc[q] = 0.f;
-    for (int c = lane; c < nchunk; c += 32) {
-      uint4 cw[kUSimtOut];
-      float sc[kUSimtOut];
+  for (int q = 0; q < kUSimtOut; ++q) acc[q] = 0.f;
+  for (int c0 = lane; c0 < nchunk; c0 += 32 * kUSimtChunks) {
+    // every load of this group of chunks first, then the arithmetic
+    uint4 cw[kUSimtChunks][kUSimtOut];
+    float sc[kUSimtChunks][kUSimtOut];
+#pragma unroll
+    for (int u = 0; u < kUSimtChunks; ++u) {
+      const int c = c0 + 32 * u;
 #pragma unroll
       for (int q = 0; q < kUSimtOut; ++q) {
-        cw[q] = live[q] ? __ldg(reinterpret_cast<const uint4*>(crow[q] + (size_t)c * 16)) : make_uint4(0, 0, 0, 0);
-        sc[q] = live[q] ? __half2float(srow[q][c >> 1]) : 0.f;
+        const bool on = live[q] && c < nchunk;
+        cw[u][q] = on ? __ldg(reinterpret_cast<const uint4*>(crow[q] + (size_t)c * 16)) : make_uint4(0, 0, 0, 0);
+        sc[u][q] = on ? __half2float(srow[q][c >> 1]) : 0.f;
       }
+    }
+#pragma unroll
+    for (int u = 0; u < kUSimtChunks; ++u) {
+      const int c = c0 + 32 * u;
+      if (c >= nchunk) break;
       const uint4* xp = reinterpret_cast<const uint4*>(xs + c * 32);
       const uint4 x0 = xp[0], x1 = xp[1], x2 = xp[2], x3 = xp[3];
 #pragma unroll
       for (int q = 0; q < kUSimtOut; ++q) {
         float s = 0.f;
-        s = dot8_int4(cw[q].x, x0.x, x0.y, x0.z, x0.w, s);
-        s = dot8_int4(cw[q].y, x1.x, x1.y, x1.z, x1.w, s);
-        s = dot8_int4(cw[q].z, x2.x, x2.y, x2.z, x2.w, s);
-        s = dot8_int4(cw[q].w, x3.x, x3.y, x3.z, x3.w, s);
-        acc[q] = fmaf(s, sc[q], acc[q]);
+        s = dot8_int4(cw[u][q].x, x0.x, x0.y, x0.z, x0.w, s);
+        s = dot8_int4(cw[u][q].y, x1.x, x1.y, x1.z, x1.w, s);
+        s = dot8_int4(cw[u][q].z, x2.x, x2.y, x2.z, x2.w, s);
+        s = dot8_int4(cw[u][q].w, x3.x, x3.y, x3.z, x3.w, s);
+        acc[q] = fmaf(s, sc[u][q], acc[q]);
       }
     }
+  }
 #pragma unroll
-    for (int q = 0; q < kUSimtOut; ++q)
+  for (int q = 0; q < kUSimtOut; ++q)
 #pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], off);
-    if (lane < kUSimtOut && ob + lane < KRP) {
-      float val = acc[0];
+    for (int off = 16; off >= 1; off >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], off);
+  if (lane < kUSimtOut && ob + lane < KRP) {
+    float val = acc[0];
 #pragma unroll
-      for (int q = 1; q < kUSimtOut; ++q) val = lane == q ? acc[q] : val;
-      U[(size_t)i * 2 * KRP + m * KRP + ob + lane] = __float2half_rn(val);
-    }
+    for (int q = 1; q < kUSimtOut; ++q) val = lane == q ? acc[q] : val;
+    U[(size_t)i * 2 * KRP + m * KRP + ob + lane] = __float2half_rn(val);
   }
 }
 
@@ -2138,7 +2151,7 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   // 3. U = X (Ain_hi + Ain_lo)^T (FP32 accumulation, FP16 out): the hi stack is at rows g*4*KRP, the lo stack 2*KRP later
   if (prep_done && !u_simt && (e = cudaStreamWaitEvent(st, prep_done, 0)) != cudaSuccess) return e;
   if (u_simt) {
-    e = launch_pdl(u_simt_kernel, dim3(R, 2), dim3(256), (size_t)d * 2, st, (const __nv_bfloat16*)x,
+    e = launch_pdl(u_simt_kernel, dim3(R, 2, (KRP + 31) / 32), dim3(256), (size_t)d * 2, st, (const __nv_bfloat16*)x,
                    row_asg, eidx, pa, a.tab, a.kg, a.ke, b.U, b.X);
     prof_mark("u_simt", st);
   } else {
