@@ -93,12 +93,90 @@ __global__ void __launch_bounds__(WT * WR * 32, MINB) router_logits_bf16_kernel(
     }
 }
 
-// BF16 router logits with the operands staged in shared memory.  A CTA of 8 warps computes 32
-// tokens x 16 router rows (warp (tg, rg): tokens 8 tg.., rows 8 rg..); d streams through a
+// L lanes per token (L = the power of two >= max(G, K), at most 32): top-k_g groups, softmax p;
+// inside each chosen group top-k_e experts, softmax q; gate = p * q.  Higher logit first, equal
+// logits -> lower index first.  Lane l of a token holds groups l, l + L, ... and, per chosen
+// group, its member l; each pick is an argmax over the token's lanes; lane j keeps the j-th pick.
+// The softmax sums run over the picks in order.
+constexpr int kSelGroupsPerLane = kMaxE / 32;
+
+template <int L>
+__device__ __forceinline__ void seg_argmax(float& v, int& idx) {
+  // idx < 0: nothing to offer; ties go to the lower index
+#pragma unroll
+  for (int o = L / 2; o >= 1; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o, L);
+    const int oi = __shfl_xor_sync(0xffffffffu, idx, o, L);
+    if (oi >= 0 && (idx < 0 || ov > v || (ov == v && oi < idx))) { v = ov; idx = oi; }
+  }
+}
+
+template <int L>
+__device__ __forceinline__ void select_token(const float* sg, const GroupTable& tab, int t, bool valid, int kg,
+                                             int ke, int li, int32_t* __restrict__ gidx, int32_t* __restrict__ eidx,
+                                             float* __restrict__ gate) {
+  const int G = tab.G, K = tab.K, k = kg * ke;
+  const float* se = sg + G;
+  float gv[kSelGroupsPerLane];
+  uint32_t avail = 0u;
+#pragma unroll
+  for (int u = 0; u < kSelGroupsPerLane; ++u) {
+    const int g = li + L * u;
+    gv[u] = g < G ? sg[g] : 0.f;
+    if (g < G) avail |= 1u << u;
+  }
+  // group picks: lane j keeps pick j
+  int my_g = -1;
+  float my_gv = 0.f;
+  for (int j = 0; j < kg; ++j) {
+    float bv = 0.f;
+    int bi = -1;
+#pragma unroll
+    for (int u = 0; u < kSelGroupsPerLane; ++u)
+      if (((avail >> u) & 1u) && (bi < 0 || gv[u] > bv)) { bv = gv[u]; bi = li + L * u; }
+    seg_argmax<L>(bv, bi);
+    if (bi % L == li) avail &= ~(1u << (bi / L));
+    if (li == j) { my_g = bi; my_gv = bv; }
+  }
+  const float g0 = __shfl_sync(0xffffffffu, my_gv, 0, L);
+  const float my_pe = expf(my_gv - g0);
+  float pden = 0.f;
+  for (int j = 0; j < kg; ++j) pden += __shfl_sync(0xffffffffu, my_pe, j, L);
+  const float my_p = my_pe / pden;
+  for (int j = 0; j < kg; ++j) {
+    const int g = __shfl_sync(0xffffffffu, my_g, j, L);
+    const float p = __shfl_sync(0xffffffffu, my_p, j, L);
+    if (valid && li == 0) gidx[(size_t)t * kg + j] = g;
+    const float v_l = li < K ? se[tab.member[g * K + li]] : 0.f;
+    bool open = li < K;
+    int my_e = -1;
+    float my_ev = 0.f;
+    for (int s2 = 0; s2 < ke; ++s2) {
+      float bv = open ? v_l : 0.f;
+      int bi = open ? li : -1;
+      seg_argmax<L>(bv, bi);
+      if (bi == li) open = false;
+      if (li == s2) { my_e = (int)tab.member[g * K + bi]; my_ev = bv; }
+    }
+    const float e0 = __shfl_sync(0xffffffffu, my_ev, 0, L);
+    const float my_qe = expf(my_ev - e0);
+    float qden = 0.f;
+    for (int s2 = 0; s2 < ke; ++s2) qden += __shfl_sync(0xffffffffu, my_qe, s2, L);
+    if (valid && li < ke) {
+      eidx[(size_t)t * k + j * ke + li] = my_e;
+      gate[(size_t)t * k + j * ke + li] = p * (my_qe / qden);
+    }
+  }
+}
+
+// BF16 router logits with the operands staged in shared memory.  A CTA of 4 x RG warps computes
+// 32 tokens x 8 RG router rows (warp (tg, rg): tokens 8 tg.., rows 8 rg..); d streams through a
 // three-stage cp.async pipeline in chunks of 256 elements.  Canonical order as above: lane l adds
 // the products of its elements 128*j + 4*l + u in ascending index (one rounding per product --
-// exact for BF16 x BF16 -- and per add), then the xor butterfly 16, 8, 4, 2, 1.
-constexpr int kRtTok = 32, kRtRows = 16, kRtDC = 256, kRtStages = 3;
+// exact for BF16 x BF16 -- and per add), then the xor butterfly 16, 8, 4, 2, 1.  With L > 0 the
+// CTA holds every router row of its tokens (G + E <= 8 RG): the logits stay in shared memory and
+// the CTA's warps make the selection itself (L lanes per token, as router_select_kernel<L>).
+constexpr int kRtTok = 32, kRtDC = 256, kRtStages = 3;
 
 // The xor butterfly 16, 8, 4, 2, 1 of 32 per-lane values v[0..31] at once: at the step of
 // distance k a lane keeps the half of its values whose index bit matches its own lane bit, adds
@@ -124,12 +202,16 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N> __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-__global__ void __launch_bounds__(256, 2) router_logits_smem_kernel(
+template <int RG, int L>
+__global__ void __launch_bounds__(128 * RG, RG <= 2 ? 2 : 1) router_logits_smem_kernel(
     const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ wg, const float* __restrict__ bg,
-    const __nv_bfloat16* __restrict__ we, float* __restrict__ logits, int Tn, int d, int G, int E) {
+    const __nv_bfloat16* __restrict__ we, float* __restrict__ logits, int Tn, int d, int G, int E, GroupTable tab,
+    int kg, int ke, int32_t* __restrict__ gidx, int32_t* __restrict__ eidx, float* __restrict__ gate) {
   pdl_wait();
   pdl_trigger();
-  extern __shared__ __align__(16) uint8_t rt_smem[];   // [stages][32][256] x, then [stages][16][256] w
+  constexpr int kRtRows = 8 * RG;
+  extern __shared__ __align__(16) uint8_t rt_smem[];   // [stages][32][256] x, then [stages][8 RG][256] w
+  __shared__ float s_logit[L > 0 ? kRtTok * kRtRows : 1];
   auto xs = reinterpret_cast<__nv_bfloat16 (*)[kRtTok][kRtDC]>(rt_smem);
   auto ws = reinterpret_cast<__nv_bfloat16 (*)[kRtRows][kRtDC]>(rt_smem + sizeof(__nv_bfloat16) * kRtStages * kRtTok * kRtDC);
   const int R = G + E;
@@ -202,10 +284,23 @@ __global__ void __launch_bounds__(256, 2) router_logits_smem_kernel(
     const float s = butterfly_scatter32(v, lane);
     const int i = 4 * hf + (lane >> 3), q = lane & 7;
     const int t = t_base + tg * 8 + i, rr = r_base + rg * 8 + q;
-    if (t < Tn && rr < R) {
-      float out = s;
-      if (rr < G && bg != nullptr) out = __fadd_rn(out, bg[rr]);
+    float out = s;
+    if (rr < G && bg != nullptr) out = __fadd_rn(out, bg[rr]);
+    if constexpr (L > 0) {
+      s_logit[(tg * 8 + i) * kRtRows + rg * 8 + q] = out;
+    } else if (t < Tn && rr < R) {
       logits[(size_t)t * R + rr] = out;
+    }
+  }
+  if constexpr (L > 0) {
+    // selection of the CTA's 32 tokens: L lanes per token, 32 / L tokens per warp
+    __syncthreads();
+    constexpr int kPerWarp = 32 / L;
+    const int li = lane & (L - 1);
+    for (int tt0 = warp * kPerWarp; tt0 < kRtTok; tt0 += 4 * RG * kPerWarp) {
+      const int tt = tt0 + lane / L, t = t_base + tt;
+      const bool valid = t < Tn;
+      select_token<L>(s_logit + tt * kRtRows, tab, valid ? t : Tn - 1, valid, kg, ke, li, gidx, eidx, gate);
     }
   }
 }
@@ -272,24 +367,6 @@ __global__ void __launch_bounds__(256) router_logits_f32_kernel(
     }
 }
 
-// L lanes per token (L = the power of two >= max(G, K), at most 32): top-k_g groups, softmax p;
-// inside each chosen group top-k_e experts, softmax q; gate = p * q.  Higher logit first, equal
-// logits -> lower index first.  Lane l of a token holds groups l, l + L, ... and, per chosen
-// group, its member l; each pick is an argmax over the token's lanes; lane j keeps the j-th pick.
-// The softmax sums run over the picks in order.
-constexpr int kSelGroupsPerLane = kMaxE / 32;
-
-template <int L>
-__device__ __forceinline__ void seg_argmax(float& v, int& idx) {
-  // idx < 0: nothing to offer; ties go to the lower index
-#pragma unroll
-  for (int o = L / 2; o >= 1; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, o, L);
-    const int oi = __shfl_xor_sync(0xffffffffu, idx, o, L);
-    if (oi >= 0 && (idx < 0 || ov > v || (ov == v && oi < idx))) { v = ov; idx = oi; }
-  }
-}
-
 template <int L>
 __global__ void __launch_bounds__(256) router_select_kernel(const float* __restrict__ logits, GroupTable tab,
                                                             int Tn, int kg, int ke, int32_t* __restrict__ gidx,
@@ -301,59 +378,7 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
   if ((int)((blockIdx.x * blockDim.x + (threadIdx.x & ~31u)) / L) >= Tn) return;   // the whole warp is past the batch
   const bool valid = t_raw < Tn;
   const int t = valid ? t_raw : Tn - 1;
-  const int G = tab.G, E = tab.E, K = tab.K, k = kg * ke;
-  const float* sg = logits + (size_t)t * (G + E);
-  const float* se = sg + G;
-  float gv[kSelGroupsPerLane];
-  uint32_t avail = 0u;
-#pragma unroll
-  for (int u = 0; u < kSelGroupsPerLane; ++u) {
-    const int g = li + L * u;
-    gv[u] = g < G ? sg[g] : 0.f;
-    if (g < G) avail |= 1u << u;
-  }
-  // group picks: lane j keeps pick j
-  int my_g = -1;
-  float my_gv = 0.f;
-  for (int j = 0; j < kg; ++j) {
-    float bv = 0.f;
-    int bi = -1;
-#pragma unroll
-    for (int u = 0; u < kSelGroupsPerLane; ++u)
-      if (((avail >> u) & 1u) && (bi < 0 || gv[u] > bv)) { bv = gv[u]; bi = li + L * u; }
-    seg_argmax<L>(bv, bi);
-    if (bi % L == li) avail &= ~(1u << (bi / L));
-    if (li == j) { my_g = bi; my_gv = bv; }
-  }
-  const float g0 = __shfl_sync(0xffffffffu, my_gv, 0, L);
-  const float my_pe = expf(my_gv - g0);
-  float pden = 0.f;
-  for (int j = 0; j < kg; ++j) pden += __shfl_sync(0xffffffffu, my_pe, j, L);
-  const float my_p = my_pe / pden;
-  for (int j = 0; j < kg; ++j) {
-    const int g = __shfl_sync(0xffffffffu, my_g, j, L);
-    const float p = __shfl_sync(0xffffffffu, my_p, j, L);
-    if (valid && li == 0) gidx[(size_t)t * kg + j] = g;
-    const float v_l = li < K ? se[tab.member[g * K + li]] : 0.f;
-    bool open = li < K;
-    int my_e = -1;
-    float my_ev = 0.f;
-    for (int s2 = 0; s2 < ke; ++s2) {
-      float bv = open ? v_l : 0.f;
-      int bi = open ? li : -1;
-      seg_argmax<L>(bv, bi);
-      if (bi == li) open = false;
-      if (li == s2) { my_e = (int)tab.member[g * K + bi]; my_ev = bv; }
-    }
-    const float e0 = __shfl_sync(0xffffffffu, my_ev, 0, L);
-    const float my_qe = expf(my_ev - e0);
-    float qden = 0.f;
-    for (int s2 = 0; s2 < ke; ++s2) qden += __shfl_sync(0xffffffffu, my_qe, s2, L);
-    if (valid && li < ke) {
-      eidx[(size_t)t * k + j * ke + li] = my_e;
-      gate[(size_t)t * k + j * ke + li] = p * (my_qe / qden);
-    }
-  }
+  select_token<L>(logits + (size_t)t * (tab.G + tab.E), tab, t, valid, kg, ke, li, gidx, eidx, gate);
 }
 
 template <int L>
@@ -373,20 +398,47 @@ static void launch_bf16_logits(const void* x, const void* wg, const float* bg, c
              (const __nv_bfloat16*)x, (const __nv_bfloat16*)wg, bg, (const __nv_bfloat16*)we, logits, Tn, d, G, E);
 }
 
-static cudaError_t launch_logits(bool bf16, const void* x, const void* wg, const float* bg, const void* we,
-                                 float* logits, int Tn, int d, int G, int E, cudaStream_t st) {
+template <int RG, int L>
+static cudaError_t launch_smem_logits(const LayerArgs& a, const void* x, const void* wg, const float* bg,
+                                      const void* we, float* logits, int32_t* gidx, int32_t* eidx, float* gate,
+                                      cudaStream_t st) {
+  constexpr int rows = 8 * RG;
+  const int Tn = a.T, d = a.d, G = a.G, E = a.E;
+  dim3 grid((Tn + kRtTok - 1) / kRtTok, (G + E + rows - 1) / rows);
+  constexpr size_t smem = sizeof(__nv_bfloat16) * kRtStages * (kRtTok + rows) * kRtDC;
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t e = cudaFuncSetAttribute(router_logits_smem_kernel<RG, L>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  return launch_pdl(router_logits_smem_kernel<RG, L>, grid, dim3(128 * RG), smem, st, (const __nv_bfloat16*)x,
+                    (const __nv_bfloat16*)wg, bg, (const __nv_bfloat16*)we, logits, Tn, d, G, E, a.tab, a.kg, a.ke,
+                    gidx, eidx, gate);
+}
+
+// Router logits and selection in one launch when a CTA can hold every router row of its tokens
+// (G + E <= 24, at least 1024 tokens); returns false (nothing launched) otherwise.
+static bool launch_fused_route(const LayerArgs& a, const void* x, const void* wg, const float* bg, const void* we,
+                               int32_t* gidx, int32_t* eidx, float* gate, cudaStream_t st, cudaError_t* err) {
+  const int R = a.G + a.E, need = a.G > a.K ? a.G : a.K;
+  if (!a.bf16 || a.T < 1024 || R > 24 || need > 8) return false;
+  if (R <= 16)
+    *err = need <= 4 ? launch_smem_logits<2, 4>(a, x, wg, bg, we, nullptr, gidx, eidx, gate, st)
+                     : launch_smem_logits<2, 8>(a, x, wg, bg, we, nullptr, gidx, eidx, gate, st);
+  else
+    *err = need <= 4 ? launch_smem_logits<3, 4>(a, x, wg, bg, we, nullptr, gidx, eidx, gate, st)
+                     : launch_smem_logits<3, 8>(a, x, wg, bg, we, nullptr, gidx, eidx, gate, st);
+  prof_mark("router", st);
+  return true;
+}
+
+static cudaError_t launch_logits(const LayerArgs& a, bool bf16, const void* x, const void* wg, const float* bg,
+                                 const void* we, float* logits, int Tn, int d, int G, int E, cudaStream_t st) {
   if (bf16 && Tn >= 1024) {
-    dim3 grid((Tn + kRtTok - 1) / kRtTok, (G + E + kRtRows - 1) / kRtRows);
-    constexpr size_t smem = sizeof(__nv_bfloat16) * kRtStages * (kRtTok + kRtRows) * kRtDC;   // 72 KB
-    static bool attr = false;
-    if (!attr) {
-      const cudaError_t e = cudaFuncSetAttribute(router_logits_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)smem);
-      if (e != cudaSuccess) return e;
-      attr = true;
-    }
-    launch_pdl(router_logits_smem_kernel, grid, dim3(256), smem, st, (const __nv_bfloat16*)x, (const __nv_bfloat16*)wg,
-               bg, (const __nv_bfloat16*)we, logits, Tn, d, G, E);
+    const cudaError_t e = launch_smem_logits<2, 0>(a, x, wg, bg, we, logits, nullptr, nullptr, nullptr, st);
+    if (e != cudaSuccess) return e;
   } else if (bf16) {
     // few tokens: small warp blocks and a deep unroll so that the loads of many j blocks are in
     // flight at once
@@ -405,7 +457,9 @@ cudaError_t launch_route(const LayerArgs& a, const void* x, const void* wg, cons
                          const void* we, float* logits, int32_t* gidx, int32_t* eidx, float* gate,
                          cudaStream_t st) {
   if (a.T == 0) return cudaSuccess;
-  cudaError_t err = launch_logits(a.bf16, x, wg, bg, we, logits, a.T, a.d, a.G, a.E, st);
+  cudaError_t err = cudaSuccess;
+  if (launch_fused_route(a, x, wg, bg, we, gidx, eidx, gate, st, &err)) return err != cudaSuccess ? err : cudaGetLastError();
+  err = launch_logits(a, a.bf16, x, wg, bg, we, logits, a.T, a.d, a.G, a.E, st);
   if (err != cudaSuccess) return err;
   const int need = a.G > a.K ? a.G : a.K;
   if (need <= 4) launch_select<4>(a, logits, gidx, eidx, gate, st);

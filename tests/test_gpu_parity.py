@@ -70,6 +70,7 @@ CASES = {
                                       group_map="contiguous"),
     "bf16_rows2100_ke3": small(T=2100, d=256, f=192, E=16, G=4, kg=1, ke=3, seed=44, resid_std=0.2),
     "bf16_rows2100_ke4": small(T=2100, d=256, f=320, E=16, G=4, kg=1, ke=4, seed=45, resid_std=0.2),
+    "bf16_fused_route_L8": small(T=1500, d=256, f=192, E=16, G=8, kg=2, ke=2, seed=46, resid_std=0.2),
     "bf16_K32": small(T=300, E=128, G=4, kg=2, ke=3, group_map="perm", seed=36, resid_std=0.2),
     "bf16_G64": small(T=200, E=128, G=64, kg=3, ke=2, group_map="perm", seed=37, resid_std=0.2),
     "bf16_K1": small(T=200, E=4, G=4, kg=2, ke=1, seed=28),
