@@ -494,6 +494,165 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_kernel(
 }
 
 // ------------------------------------------------------------------------------------------
+// 3/6 (persistent).  The same grouped GEMM for grids of many waves: one CTA per SM walks the work
+// items w = blockIdx.x + k * gridDim.x (item = row tile * n_tiles + N tile; unused row tiles are
+// skipped by every role alike), the stage ring runs on across items, and TMEM holds two
+// accumulators (2 x BN columns) so that the epilogue of one item overlaps the K loop of the next.
+// ------------------------------------------------------------------------------------------
+template <int BN, int STAGES, int OUT>
+__global__ void __launch_bounds__(192, 1) tc_gemm_persist_kernel(
+    const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
+    const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1, int nk0, int nk1,
+    const int32_t* __restrict__ row_begin, int G, int b_stride, int b1_off, int tiles, int n_tiles,
+    void* __restrict__ out, int out_ld, const int32_t* __restrict__ scatter, DevStatus* status) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr uint32_t A_BYTES = kTile * 128, B_BYTES = BN * 128;
+  static_assert(2 * BN <= 512, "two accumulators in TMEM");
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], fin;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const tc::Abort ab{&abort_flag, status};
+  const int items = tiles * n_tiles;
+  const int nk = nk0 + nk1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) { tc::bar_init(&full[s], 1); tc::bar_init(&empty[s], 1); }
+    for (int b = 0; b < 2; ++b) { tc::bar_init(&acc_full[b], 1); tc::bar_init(&acc_empty[b], 4); }
+    tc::bar_init(&fin, 1);
+    abort_flag = 0;
+    tc::bar_fence_init();
+  }
+  if (warp == 1) tc::tmem_alloc(&tmem_base, 2 * BN);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = tmem_base;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer: the stage ring runs on across items
+    tc::prefetch_map(&mA0); tc::prefetch_map(&mB0);
+    if (nk1) { tc::prefetch_map(&mA1); tc::prefetch_map(&mB1); }
+    int kc = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < items && ok; w += gridDim.x) {
+      int g, r0, r1;
+      if (!tile_of(row_begin, G, w / n_tiles, g, r0, r1)) continue;
+      const int n0 = (w % n_tiles) * BN;
+      for (int kb = 0; kb < nk; ++kb, ++kc) {
+        const int s = kc % STAGES, it = kc / STAGES;
+        if (kc >= STAGES && !tc::bar_wait(&empty[s], (it - 1) & 1, ab, 151)) { ok = false; break; }
+        tc::bar_expect_tx(&full[s], A_BYTES + B_BYTES);
+        const bool first = kb < nk0;
+        const int kx = (first ? kb : kb - nk0) * 64;
+        tc::tma_load_2d(sA + s * A_BYTES, first ? &mA0 : &mA1, &full[s], kx, r0);
+        tc::tma_load_2d(sB + s * B_BYTES, first ? &mB0 : &mB1, &full[s], kx, g * b_stride + (first ? 0 : b1_off) + n0);
+      }
+    }
+    if (abort_flag) tc::drain_copies();
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer: item li into acc[li & 1]
+    constexpr uint32_t idesc = tc::idesc_bf16(kTile, BN);
+    int kc = 0, li = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < items && ok; w += gridDim.x) {
+      int g, r0, r1;
+      if (!tile_of(row_begin, G, w / n_tiles, g, r0, r1)) continue;
+      const int b = li & 1;
+      if (li >= 2 && !tc::bar_wait(&acc_empty[b], ((li >> 1) - 1) & 1, ab, 152)) break;
+      tc::fence_after();
+      const uint32_t dcol = tmem + b * BN;
+      for (int kb = 0; kb < nk; ++kb, ++kc) {
+        const int s = kc % STAGES, it = kc / STAGES;
+        if (!tc::bar_wait(&full[s], it & 1, ab, 153)) { ok = false; break; }
+        tc::fence_after();
+        const uint32_t a0 = tc::smem_u32(sA + s * A_BYTES), b0 = tc::smem_u32(sB + s * B_BYTES);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma_bf16(dcol, tc::sdesc(a0 + 32 * k), tc::sdesc(b0 + 32 * k), idesc, (kb | k) != 0);
+        tc::mma_commit(&empty[s]);
+      }
+      if (!ok) break;
+      tc::mma_commit(&acc_full[b]);
+      ++li;
+    }
+    tc::mma_commit(&fin);
+    const uint64_t t0 = tc::now_ns();
+    while (!tc::bar_test(&fin, 0) && tc::now_ns() - t0 < tc::kWaitNs) {}
+  } else if (warp >= 2) {
+    // ---------------- epilogue: TMEM -> rows, item li from acc[li & 1]
+    const int q = warp & 3, row = q * 32 + lane;
+    int li = 0;
+    for (int w = blockIdx.x; w < items; w += gridDim.x) {
+      int g, r0, r1;
+      if (!tile_of(row_begin, G, w / n_tiles, g, r0, r1)) continue;
+      const int b = li & 1, n0 = (w % n_tiles) * BN;
+      const bool got = tc::bar_wait(&acc_full[b], (li >> 1) & 1, ab, 154);
+      if (!__all_sync(0xffffffffu, got) || abort_flag) break;
+      tc::fence_after();
+      const int i = r0 + row;
+      const bool valid = i < r1;
+      const size_t orow = valid ? (size_t)(scatter ? scatter[i] : i) : 0;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t v[32];
+        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + b * BN + c, *reinterpret_cast<uint32_t(*)[16]>(v));
+        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + b * BN + c + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+        tc::tmem_ld_wait();
+        if (c + 32 >= BN) {
+          // this warp has read the whole accumulator: the MMA of item li + 2 may overwrite it
+          tc::fence_before();
+          __syncwarp();
+          if (lane == 0) tc::bar_arrive(&acc_empty[b]);
+        }
+        if (valid) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint32_t* vv = v + 16 * hh;
+            const int cc = c + 16 * hh;
+            if constexpr (OUT == kOutF32) {
+              uint4* d4 = reinterpret_cast<uint4*>((float*)out + orow * out_ld + n0 + cc);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) d4[e] = make_uint4(vv[4 * e], vv[4 * e + 1], vv[4 * e + 2], vv[4 * e + 3]);
+            } else if constexpr (OUT == kOutF16) {
+              uint32_t pk[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                __half2 h2 = __floats2half2_rn(__uint_as_float(vv[2 * e]), __uint_as_float(vv[2 * e + 1]));
+                pk[e] = *reinterpret_cast<uint32_t*>(&h2);
+              }
+              uint4* d4 = reinterpret_cast<uint4*>((__half*)out + orow * out_ld + n0 + cc);
+              d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            } else {
+              uint32_t pk[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) pk[e] = tc::pack_bf16(__uint_as_float(vv[2 * e]), __uint_as_float(vv[2 * e + 1]));
+              uint4* d4 = reinterpret_cast<uint4*>((__nv_bfloat16*)out + orow * out_ld + n0 + cc);
+              d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
+          }
+        }
+      }
+      ++li;
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after();
+    tc::tmem_dealloc(tmem, 2 * BN);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
 // 3/6 (pairs). The same grouped GEMM on CTA pairs: the two CTAs of a cluster take two 128-row
 //      tiles of one group (pair P covers the group's tiles 2P and 2P + 1; the second may lie past
 //      the group's end and then only feeds the pair) and one MMA of M = 256 x N = BN, issued by
@@ -2001,6 +2160,31 @@ static cudaError_t launch_gemm(const CUtensorMap& A0, const CUtensorMap& A1, con
                     row_begin, G, b_stride, b1_off, out, out_ld, scatter, st);
 }
 
+// Persistent version: one CTA per SM over all (row tile, N tile) items.
+template <int BN, int OUT>
+static cudaError_t launch_gemm_persist(const CUtensorMap& A0, const CUtensorMap& A1, const CUtensorMap& B0,
+                                       const CUtensorMap& B1, int nk0, int nk1, const int32_t* row_begin, int G,
+                                       int n_out, int b_stride, int b1_off, int tiles, void* out, int out_ld,
+                                       const int32_t* scatter, DevStatus* st, cudaStream_t stream) {
+  constexpr int STAGES = BN >= 256 ? 4 : 6;
+  const size_t smem = 1024 + (size_t)STAGES * (kTile * 128 + BN * 128);
+  static bool attr = false;
+  static int sms = 0;
+  if (!attr) {
+    cudaError_t e = set_smem(tc_gemm_persist_kernel<BN, STAGES, OUT>, smem);
+    if (e == cudaSuccess) {
+      int dev = 0;
+      e = cudaGetDevice(&dev);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    }
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int n_tiles = n_out / BN, items = tiles * n_tiles;
+  return launch_pdl(tc_gemm_persist_kernel<BN, STAGES, OUT>, dim3(items < sms ? items : sms), dim3(192), smem, stream,
+                    A0, A1, B0, B1, nk0, nk1, row_begin, G, b_stride, b1_off, tiles, n_tiles, out, out_ld, scatter, st);
+}
+
 // CTA-pair version: grid.x = 2 x (an upper bound of the row-tile pairs), clusters of two CTAs
 // along x (the pair of a cta_group::2 MMA is formed along x), grid.y = N tiles of BN.
 template <int BN, int OUT>
@@ -2196,8 +2380,13 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   // 6. Y = [hsum | V~] [Wd | Bdn]^T, rows to their token slot
+  // many waves of single-CTA tiles: the persistent form overlaps each tile's epilogue with the
+  // next tile's K loop
+  const bool down_persist = !down_pair && BN2 == 256 && tiles * (d / 256) > 2 * 148;
   e = down_pair ? launch_gemm_pair<256, kOutBf16>(mH, mVt, mWd, mBd, f / 64, 2 * KRP / 64, row_begin, G, d, d, 0,
                                                   pairs, y_rows, d, row_asg, status, st)
+      : down_persist ? launch_gemm_persist<256, kOutBf16>(mH, mVt, mWd, mBd, f / 64, 2 * KRP / 64, row_begin, G, d,
+                                                          d, 0, tiles, y_rows, d, row_asg, status, st)
                 : (BN2 == 256 ? launch_gemm<256, kOutBf16>(mH, mVt, mWd, mBd, f / 64, 2 * KRP / 64, row_begin, G, d,
                                                            d, 0, tiles, y_rows, d, row_asg, status, st)
                               : launch_gemm<128, kOutBf16>(mH, mVt, mWd, mBd, f / 64, 2 * KRP / 64, row_begin, G, d,

@@ -218,3 +218,10 @@ def test_long_k_gate_up_sampled(T, ke, seed):
     a ragged last pair (T not a multiple of 256 rows per group); sampled tokens against the oracle."""
     cfg = small(T=T, d=4096, f=1024, E=8, G=2, kg=1, ke=ke, seed=seed, resid_std=0.2)
     full_size_check("long_k", 40, cfg)
+
+
+def test_persistent_down_gemm_sampled():
+    """Many waves of down-projection tiles with a short K loop (d_ff = 256): the persistent grouped
+    GEMM with double-buffered accumulators; sampled tokens against the oracle, ragged groups."""
+    cfg = small(T=16384, d=1024, f=256, E=8, G=2, kg=1, ke=2, seed=47, resid_std=0.2)
+    full_size_check("persist", 48, cfg)
