@@ -63,6 +63,7 @@ Plan make_plan(const LayerArgs& a) {
     p.Adn = take(G * KRP * f * 2);
     p.Bdn = take(G * d * 2 * KRP * 2);
     p.Ubf = take(Rp * 2 * KRP * 2);
+    p.Ud = take(tc_u_dense(a) ? T * G * 2 * KRP * 2 : 0);
     p.hsum_bf = take(Rp * f * 2);
     p.Vpart = take((size_t)p.nchunks * 2 * R * a.ke * a.r * 4);   // up to two partials per chunk
     p.Vt = take(Rp * 2 * KRP * 2);
@@ -150,7 +151,7 @@ static TcBufs tc_bufs(const Plan& p, void* ws) {
                 at<__half>(ws, p.Bus),        at<__half>(ws, p.Adt),           at<__nv_bfloat16>(ws, p.Adn),
                 at<__nv_bfloat16>(ws, p.Bdn),
                 at<__half>(ws, p.Ubf), at<__nv_bfloat16>(ws, p.hsum_bf), at<__nv_bfloat16>(ws, p.Vt),
-                at<float>(ws, p.Vpart)};
+                at<float>(ws, p.Vpart), at<__half>(ws, p.Ud)};
 }
 
 static cudaError_t run_ffn(const LayerArgs& a, const Plan& p, void* ws, const void* x, const void* wg,
@@ -312,7 +313,8 @@ int moe_hier_forward(const moe_hier_desc* desc, const void* x, const void* w_gro
   if (e == cudaSuccess && side) {
     e = cudaEventRecord(side->fork, s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(side->st, side->fork, 0);
-    if (e == cudaSuccess) e = launch_resid_prep(a, resid_ptrs(a, resid), tc_bufs(p, ws), side->st);
+    if (e == cudaSuccess)
+      e = launch_resid_prep(a, resid_ptrs(a, resid), tc_bufs(p, ws), x, at<DevStatus>(ws, p.status), side->st);
     if (e == cudaSuccess) e = cudaEventRecord(side->join, side->st);
     prep_done = side->join;
   }

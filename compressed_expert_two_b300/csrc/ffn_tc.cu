@@ -680,7 +680,7 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_pair_kernel(
     const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
     const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1, int nk0, int nk1,
     const int32_t* __restrict__ row_begin, int G, int b_stride, int b1_off, void* __restrict__ out, int out_ld,
-    const int32_t* __restrict__ scatter, DevStatus* status) {
+    const int32_t* __restrict__ scatter, DevStatus* status, int dense_rows) {
   constexpr int BH = BN / 2;                                  // B rows held by each CTA
   constexpr uint32_t A_BYTES = kTile * 128, B_BYTES = BH * 128, STAGE_BYTES = A_BYTES + B_BYTES;
   extern __shared__ uint8_t smem_raw[];
@@ -692,8 +692,19 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_pair_kernel(
 
   const uint32_t rank = tc::cluster_rank();
   int g, r0, r1;
-  if (!pair_tile_of(row_begin, G, blockIdx.x >> 1, (int)rank, g, r0, r1)) return;   // same for both CTAs
-  const int n0 = blockIdx.y * BN;
+  // dense_rows > 0: rows [0, dense_rows) of A against every group's B (N tile y = group y, its
+  // BN rows), output columns y * BN ..; else rows of each group against that group's B
+  if (dense_rows > 0) {
+    const int P = blockIdx.x >> 1;
+    if (P * 2 * kTile >= dense_rows) return;                                      // same for both CTAs
+    g = blockIdx.y;
+    r0 = (2 * P + (int)rank) * kTile;
+    r1 = dense_rows;
+  } else if (!pair_tile_of(row_begin, G, blockIdx.x >> 1, (int)rank, g, r0, r1)) {
+    return;                                                                        // same for both CTAs
+  }
+  const int n0 = dense_rows > 0 ? 0 : blockIdx.y * BN;         // B rows of the N tile inside group g
+  const int oc0 = blockIdx.y * BN;                             // output columns
   uint8_t* smem = align1024(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const tc::Abort ab{&abort_flag, status};
@@ -763,7 +774,7 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_pair_kernel(
         tc::tmem_ld_wait();
         if (valid) {
           if constexpr (OUT == kOutF32) {
-            uint4* d4 = reinterpret_cast<uint4*>((float*)out + orow * out_ld + n0 + c);
+            uint4* d4 = reinterpret_cast<uint4*>((float*)out + orow * out_ld + oc0 + c);
 #pragma unroll
             for (int e = 0; e < 4; ++e) d4[e] = make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
           } else if constexpr (OUT == kOutF16) {
@@ -773,14 +784,14 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_pair_kernel(
               __half2 h2 = __floats2half2_rn(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
               pk[e] = *reinterpret_cast<uint32_t*>(&h2);
             }
-            uint4* d4 = reinterpret_cast<uint4*>((__half*)out + orow * out_ld + n0 + c);
+            uint4* d4 = reinterpret_cast<uint4*>((__half*)out + orow * out_ld + oc0 + c);
             d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           } else {
             uint32_t pk[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) pk[e] = tc::pack_bf16(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
-            uint4* d4 = reinterpret_cast<uint4*>((__nv_bfloat16*)out + orow * out_ld + n0 + c);
+            uint4* d4 = reinterpret_cast<uint4*>((__nv_bfloat16*)out + orow * out_ld + oc0 + c);
             d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           }
@@ -827,6 +838,8 @@ struct UpArgs {
   const int32_t* eidx;
   const float* gate;
   const __half* U;          // [R][2*KRP] FP16: A_gate^T x | A_up^T x of the group's experts
+                            // (u_by_token: [T][G*2*KRP], token t's block of every group)
+  int u_by_token;
   const __half* sAd;        // FP16 scales [E][16][f/64] of A_down^T
   __nv_bfloat16* hsum;      // [R][f]
   float* Vpart;             // [nchunks][R][ke][16]
@@ -1493,7 +1506,8 @@ __global__ void __launch_bounds__(kUp3Warps * 32, 1) ffn_up3_kernel(
         eid[s] = e;
         gt[s] = p.gate[(size_t)t * k + j * KE + s];
       }
-      urow = p.U + (size_t)i * 2 * KRP + (part & 1) * KRP;
+      urow = p.U + (p.u_by_token ? (size_t)t * p.G * 2 * KRP + (size_t)g * 2 * KRP : (size_t)i * 2 * KRP) +
+             (part & 1) * KRP;
     }
     if (builds) {
       uint4* z = reinterpret_cast<uint4*>(sU + (row >> 3) * 1024 + (row & 7) * 128);
@@ -1878,7 +1892,8 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up4p_kernel(
         le[s] = p.tab.local_of[e];
         gt[s] = p.gate[(size_t)t * k + j * KE + s];
       }
-      urow = p.U + (size_t)i * 2 * KRP + half * KRP;
+      urow = p.U + (p.u_by_token ? (size_t)t * p.G * 2 * KRP + (size_t)g * 2 * KRP : (size_t)i * 2 * KRP) +
+             half * KRP;
     }
     {
       uint4* z = reinterpret_cast<uint4*>(sU + (row >> 3) * 1024 + (row & 7) * 128);
@@ -2191,7 +2206,7 @@ template <int BN, int OUT>
 static cudaError_t launch_gemm_pair(const CUtensorMap& A0, const CUtensorMap& A1, const CUtensorMap& B0,
                                     const CUtensorMap& B1, int nk0, int nk1, const int32_t* row_begin, int G,
                                     int n_out, int b_stride, int b1_off, int pairs, void* out, int out_ld,
-                                    const int32_t* scatter, DevStatus* st, cudaStream_t stream) {
+                                    const int32_t* scatter, DevStatus* st, cudaStream_t stream, int dense_rows = 0) {
   constexpr int STAGES = BN >= 256 ? 6 : 8;
   const size_t smem = 1024 + (size_t)STAGES * (kTile * 128 + (BN / 2) * 128);
   static bool attr = false;
@@ -2202,7 +2217,7 @@ static cudaError_t launch_gemm_pair(const CUtensorMap& A0, const CUtensorMap& A1
   }
   return launch_pdl_cluster(tc_gemm_pair_kernel<BN, STAGES, OUT>, dim3(2 * pairs, n_out / BN), dim3(192),
                             dim3(2, 1, 1), smem, stream, A0, A1, B0, B1, nk0, nk1, row_begin, G, b_stride, b1_off,
-                            out, out_ld, scatter, st);
+                            out, out_ld, scatter, st, dense_rows);
 }
 
 template <int KRP, int KE>
@@ -2276,16 +2291,33 @@ static PrepArgs prep_args(const LayerArgs& a, const ResidPtrs& rp, const TcBufs&
   return pa;
 }
 
-// 1. residual stacks (weights only: may run on another stream, concurrently with the routing)
-cudaError_t launch_resid_prep(const LayerArgs& a, const ResidPtrs& rp, const TcBufs& b, cudaStream_t st) {
+bool tc_u_dense(const LayerArgs& a) {
+  return tc_path_ok(a) && a.R > kUSimtMaxRows && up3_ok(a) && a.G * 2 * tc_krp(a) <= 512;
+}
+
+// 1. residual stacks (weights only: may run on another stream, concurrently with the routing),
+//    and, when tc_u_dense, U = A^T x of every token for every group (token order: it needs no
+//    routing either) -- a dense GEMM of x against all groups' stacked A^T, which the gate/up
+//    kernel then reads at (token, group)
+cudaError_t launch_resid_prep(const LayerArgs& a, const ResidPtrs& rp, const TcBufs& b, const void* x,
+                              DevStatus* status, cudaStream_t st) {
   if (a.R == 0) return cudaSuccess;
   const PrepArgs pa = prep_args(a, rp, b);
-  const int G = a.G, d = a.d, f = a.f;
+  const int G = a.G, d = a.d, f = a.f, KRP = tc_krp(a);
   launch_pdl(resid_prep_rows_kernel, dim3(148 * 4), dim3(256), 0, st, pa, a.tab);
   launch_pdl(resid_prep_t_kernel, dim3(G * (2 * (f / 64) + d / 64 + (pa.Adt ? f / 64 : 0))), dim3(256), 0, st, pa,
              a.tab);
   prof_mark("resid_prep", st);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !tc_u_dense(a)) return e;
+  CUtensorMap mXt, mA;
+  if (!make_map(&mXt, x, (uint64_t)a.T, d, kTile) || !make_map(&mA, b.Ain, (uint64_t)G * 4 * KRP, d, KRP))
+    return cudaErrorInvalidValue;
+  e = launch_gemm_pair<128, kOutF16>(mXt, mXt, mA, mA, d / 64, d / 64, nullptr, G, G * 2 * KRP, 4 * KRP, 2 * KRP,
+                                     (a.T + 2 * kTile - 1) / (2 * kTile), b.Ud, G * 2 * KRP, nullptr, status, st,
+                                     a.T);
+  prof_mark("u_gemm", st);
+  return e;
 }
 
 cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, const void* wu, const void* wd,
@@ -2301,7 +2333,8 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   const PrepArgs pa = prep_args(a, rp, b);
   const bool u_simt = R <= kUSimtMaxRows;
   const bool up3 = up3_ok(a), up4 = up4_ok(a);
-  if (!prep_done && (e = launch_resid_prep(a, rp, b, st)) != cudaSuccess) return e;
+  const bool u_dense = tc_u_dense(a);
+  if (!prep_done && (e = launch_resid_prep(a, rp, b, x, status, st)) != cudaSuccess) return e;
 
   // 2. rows of x in (group, token) order (the CUDA-core U kernel writes them itself)
   if (!u_simt) {
@@ -2333,8 +2366,10 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   if (!ok) return cudaErrorInvalidValue;
 
   // 3. U = X (Ain_hi + Ain_lo)^T (FP32 accumulation, FP16 out): the hi stack is at rows g*4*KRP, the lo stack 2*KRP later
-  if (prep_done && !u_simt && (e = cudaStreamWaitEvent(st, prep_done, 0)) != cudaSuccess) return e;
-  if (u_simt) {
+  if (prep_done && !u_simt && !u_dense && (e = cudaStreamWaitEvent(st, prep_done, 0)) != cudaSuccess) return e;
+  if (u_dense) {
+    // U came with the residual stacks
+  } else if (u_simt) {
     e = launch_pdl(u_simt_kernel, dim3(R, 2, (KRP + 31) / 32), dim3(256), (size_t)d * 2, st, (const __nv_bfloat16*)x,
                    row_asg, eidx, pa, a.tab, a.kg, a.ke, b.U, b.X);
     prof_mark("u_simt", st);
@@ -2349,9 +2384,11 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   if (e != cudaSuccess) return e;
 
   // 4. fused gate/up
-  if (prep_done && u_simt && (e = cudaStreamWaitEvent(st, prep_done, 0)) != cudaSuccess) return e;
+  if (prep_done && (u_simt || u_dense) && (e = cudaStreamWaitEvent(st, prep_done, 0)) != cudaSuccess) return e;
   UpArgs p;
-  p.row_begin = row_begin; p.row_asg = row_asg; p.eidx = eidx; p.gate = gate; p.U = b.U; p.hsum = b.hsum;
+  p.row_begin = row_begin; p.row_asg = row_asg; p.eidx = eidx; p.gate = gate; p.hsum = b.hsum;
+  p.U = u_dense ? b.Ud : b.U;
+  p.u_by_token = u_dense ? 1 : 0;
   p.sAd = rp.A[2].scales;
   p.Vpart = b.Vpart; p.status = status; p.tab = a.tab; p.G = G; p.d = d; p.f = f; p.kg = a.kg; p.ke = a.ke;
   p.R = R; p.n_ftiles = f / nf_up;

@@ -26,7 +26,7 @@ struct Plan {
   // tensor-core path
   bool tc;
   int krp, nchunks;
-  size_t X, Ain, Bgs, Bus, Adt, Adn, Bdn, Ubf, hsum_bf, Vpart, Vt;
+  size_t X, Ain, Bgs, Bus, Adt, Adn, Bdn, Ubf, Ud, hsum_bf, Vpart, Vt;
   size_t total;
 };
 
@@ -67,6 +67,7 @@ struct TcBufs {
   __half* U;
   __nv_bfloat16 *hsum, *Vt;
   float* Vpart;
+  __half* Ud;               // [T][G*2*KRP] U in token order (tc_u_dense)
 };
 bool tc_path_ok(const LayerArgs& a);
 int tc_krp(const LayerArgs& a);
@@ -77,7 +78,10 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
                           cudaEvent_t prep_done, cudaStream_t st);
 // The weight-only first step of launch_ffn_tc (residual stacks); launch_ffn_tc skips it when
 // given prep_done, an event recorded after this call's work (it then waits for the event).
-cudaError_t launch_resid_prep(const LayerArgs& a, const ResidPtrs& rp, const TcBufs& b, cudaStream_t st);
+cudaError_t launch_resid_prep(const LayerArgs& a, const ResidPtrs& rp, const TcBufs& b, const void* x,
+                              DevStatus* status, cudaStream_t st);
+// Whether U is computed densely, in token order for every group, with the residual stacks.
+bool tc_u_dense(const LayerArgs& a);
 
 cudaError_t launch_combine(const LayerArgs& a, const void* y_rows, void* y, cudaStream_t st);
 
