@@ -36,6 +36,7 @@ Plan make_plan(const LayerArgs& a) {
   const size_t T = a.T, R = a.R, k = a.k, E = a.E, G = a.G;
   p.status = take(sizeof(DevStatus));
   p.logits = take(T * (G + E) * 4);
+  p.redo = take(T * 4);
   p.gidx = take(T * a.kg * 4);
   p.eidx = take(T * k * 4);
   p.gate = take(T * k * 4);
@@ -231,8 +232,9 @@ int moe_hier_route(const moe_hier_desc* desc, const void* x, const void* w_group
   const Plan p = make_plan(a);
   if ((st = check_ws(p, ws, ws_bytes)) != MOE_OK) return st;
   prof_start((cudaStream_t)stream);
-  return cuda_status(launch_route(a, x, w_group, b_group, w_expert, at<float>(ws, p.logits), gidx,
-                                  eidx, gate, (cudaStream_t)stream));
+  return cuda_status(launch_route(a, x, w_group, b_group, w_expert, at<float>(ws, p.logits),
+                                  at<int32_t>(ws, p.redo), gidx, eidx, gate, at<DevStatus>(ws, p.status),
+                                  false, (cudaStream_t)stream));
 }
 
 int moe_hier_permute(const moe_hier_desc* desc, const int32_t* group_map_host, const int32_t* eidx,
@@ -319,7 +321,8 @@ int moe_hier_forward(const moe_hier_desc* desc, const void* x, const void* w_gro
     prep_done = side->join;
   }
   if (e == cudaSuccess)
-    e = launch_route(a, x, w_group, b_group, w_expert, at<float>(ws, p.logits), gidx, eidx, gate, s);
+    e = launch_route(a, x, w_group, b_group, w_expert, at<float>(ws, p.logits), at<int32_t>(ws, p.redo), gidx,
+                     eidx, gate, at<DevStatus>(ws, p.status), true, s);
   PermOut o{perm, at<int32_t>(ws, p.inv_pos), at<int32_t>(ws, p.ebeg), at<int32_t>(ws, p.ecnt),
             at<int32_t>(ws, p.gbeg), at<int32_t>(ws, p.row_asg), at<int32_t>(ws, p.row_of),
             at<int32_t>(ws, p.rbeg)};

@@ -67,7 +67,7 @@ struct DevStatus {
   int code;
   int where;
   unsigned int grid_bar;   // arrivals at the permutation's grid-wide barrier (zeroed before it)
-  int pad;
+  int route_redo;          // tokens the tensor-core router leaves to the canonical-order kernels
 };
 
 __device__ __forceinline__ float to_f32(float v) { return v; }

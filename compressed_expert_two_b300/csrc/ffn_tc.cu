@@ -2104,6 +2104,10 @@ static bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t c
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  return make_map(m, base, rows, cols, box_rows);
+}
+
 // 16-bit matrix [rows][cols], box {cols, box_rows}, no swizzle (rows land contiguously in shared
 // memory, for CUDA-core reads); cols * 2 bytes must be a multiple of 16.
 static bool make_map_plain(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {

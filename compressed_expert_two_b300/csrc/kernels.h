@@ -1,5 +1,6 @@
 // Host-side launchers of libmoehier (internal to the library).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -18,7 +19,7 @@ struct LayerArgs {
 
 // Workspace carving (offsets in bytes from ws; every region 256-byte aligned).
 struct Plan {
-  size_t status, logits, gidx, eidx, gate;
+  size_t status, logits, redo, gidx, eidx, gate;
   size_t perm, inv_pos, ebeg, ecnt, gbeg, row_asg, row_of, rbeg;
   size_t cnt, off;   // per-block histograms and their exclusive offsets
   int nblk;          // permutation blocks
@@ -36,9 +37,20 @@ Plan make_plan(const LayerArgs& a);
 void prof_start(cudaStream_t st);
 void prof_mark(const char* kernel_name, cudaStream_t st);
 
+// Routing.  logits: [T][G+E] FP32 scratch; redo: [T] int32 scratch; status->route_redo must be
+// zero on entry when status_zeroed (else it is cleared here).
 cudaError_t launch_route(const LayerArgs& a, const void* x, const void* wg, const float* bg,
-                         const void* we, float* logits, int32_t* gidx, int32_t* eidx, float* gate,
-                         cudaStream_t st);
+                         const void* we, float* logits, int32_t* redo, int32_t* gidx, int32_t* eidx,
+                         float* gate, DevStatus* status, bool status_zeroed, cudaStream_t st);
+// The tensor-core router with exact verification (route_tc.cu): writes the verified tokens and
+// lists the others in redo[0 .. status->route_redo).
+bool route_tc_ok(const LayerArgs& a);
+int route_tc_columns(const LayerArgs& a);
+cudaError_t launch_route_tc(const LayerArgs& a, const void* x, const void* wg, const float* bg, const void* we,
+                            int32_t* gidx, int32_t* eidx, float* gate, int32_t* redo, DevStatus* status,
+                            cudaStream_t st);
+// BF16 [rows][cols] tensor map, box {64, box_rows}, 128-byte swizzle (ffn_tc.cu).
+bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 
 struct PermOut {
   int32_t *perm, *inv_pos, *ebeg, *ecnt, *gbeg, *row_asg, *row_of, *rbeg;

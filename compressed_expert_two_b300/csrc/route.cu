@@ -367,26 +367,147 @@ __global__ void __launch_bounds__(256) router_logits_f32_kernel(
     }
 }
 
+// Selection over logits rows 0 .. n-1 (n = Tn, or *list_n with list: row p belongs to token
+// list[p]); L lanes per row, grid-stride.
 template <int L>
 __global__ void __launch_bounds__(256) router_select_kernel(const float* __restrict__ logits, GroupTable tab,
-                                                            int Tn, int kg, int ke, int32_t* __restrict__ gidx,
-                                                            int32_t* __restrict__ eidx, float* __restrict__ gate) {
+                                                            int Tn, const int32_t* __restrict__ list,
+                                                            const int* list_n, int kg, int ke,
+                                                            int32_t* __restrict__ gidx, int32_t* __restrict__ eidx,
+                                                            float* __restrict__ gate) {
   pdl_wait();
   pdl_trigger();
+  const int n = list ? *(volatile const int*)list_n : Tn;
   const int li = threadIdx.x & (L - 1);
-  const int t_raw = (blockIdx.x * blockDim.x + threadIdx.x) / L;
-  if ((int)((blockIdx.x * blockDim.x + (threadIdx.x & ~31u)) / L) >= Tn) return;   // the whole warp is past the batch
-  const bool valid = t_raw < Tn;
-  const int t = valid ? t_raw : Tn - 1;
-  select_token<L>(logits + (size_t)t * (tab.G + tab.E), tab, t, valid, kg, ke, li, gidx, eidx, gate);
+  for (int base = blockIdx.x * blockDim.x;; base += gridDim.x * blockDim.x) {
+    if ((base + (int)(threadIdx.x & ~31u)) / L >= n) break;   // the whole warp is past the rows
+    const int p_raw = (base + (int)threadIdx.x) / L;
+    const bool valid = p_raw < n;
+    const int p = valid ? p_raw : n - 1;
+    const int t = list ? list[p] : p;
+    select_token<L>(logits + (size_t)p * (tab.G + tab.E), tab, t, valid, kg, ke, li, gidx, eidx, gate);
+  }
 }
 
 template <int L>
-static void launch_select(const LayerArgs& a, const float* logits, int32_t* gidx, int32_t* eidx, float* gate,
-                          cudaStream_t st) {
+static void launch_select(const LayerArgs& a, const float* logits, const int32_t* list, const int* list_n,
+                          int32_t* gidx, int32_t* eidx, float* gate, cudaStream_t st) {
   const int per_block = 256 / L;
-  launch_pdl(router_select_kernel<L>, dim3((a.T + per_block - 1) / per_block), dim3(256), 0, st, logits, a.tab, a.T,
-             a.kg, a.ke, gidx, eidx, gate);
+  int blocks = (a.T + per_block - 1) / per_block;
+  if (list && blocks > 148) blocks = 148;      // rows known on the device only: grid-stride
+  launch_pdl(router_select_kernel<L>, dim3(blocks), dim3(256), 0, st, logits, a.tab, a.T, list, list_n, a.kg, a.ke,
+             gidx, eidx, gate);
+}
+
+static void launch_select_any(const LayerArgs& a, const float* logits, const int32_t* list, const int* list_n,
+                              int32_t* gidx, int32_t* eidx, float* gate, cudaStream_t st) {
+  const int need = a.G > a.K ? a.G : a.K;
+  if (need <= 4) launch_select<4>(a, logits, list, list_n, gidx, eidx, gate, st);
+  else if (need <= 8) launch_select<8>(a, logits, list, list_n, gidx, eidx, gate, st);
+  else if (need <= 16) launch_select<16>(a, logits, list, list_n, gidx, eidx, gate, st);
+  else launch_select<32>(a, logits, list, list_n, gidx, eidx, gate, st);
+}
+
+// Canonical-order BF16 logits of the listed tokens (the ones the tensor-core router could not
+// verify), grid-stride; logits row p belongs to token list[p].  Lane l adds the products of its
+// elements 128 j + 4 l + u in ascending index, then the xor butterfly 16, 8, 4, 2, 1 (as a
+// reduce-scatter for the 8 x 8 tiles), as the other canonical kernels.  Few tokens: one warp per
+// (token, 8 router rows), so that they spread over every SM; many: one warp per (8 tokens,
+// 8 router rows), which reads each row once for 8 tokens.
+__global__ void __launch_bounds__(256, 1) router_exact_list_kernel(
+    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ wg, const float* __restrict__ bg,
+    const __nv_bfloat16* __restrict__ we, const int32_t* __restrict__ list, const int* list_n, int d, int G, int E,
+    float* __restrict__ logits) {
+  pdl_wait();
+  pdl_trigger();
+  const int n = *(volatile const int*)list_n;
+  const int R = G + E, nrb = (R + 7) / 8, ntb = (n + 7) / 8;
+  const int lane = threadIdx.x & 31;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  if (n * nrb <= 2 * nw) {
+    for (int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < n * nrb; item += nw) {
+      const int p = item / nrb, r0 = (item % nrb) * 8;
+      const __nv_bfloat16* xr = x + (size_t)list[p] * d + 4 * lane;
+      const __nv_bfloat16* wr[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int rr = min(r0 + q, R - 1);
+        wr[q] = (rr < G ? wg + (size_t)rr * d : we + (size_t)(rr - G) * d) + 4 * lane;
+      }
+      float acc[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+#pragma unroll 4
+      for (int j = 0; j < d; j += 128) {
+        const uint2 xv = *reinterpret_cast<const uint2*>(xr + j);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint2 wv = *reinterpret_cast<const uint2*>(wr[q] + j);
+          acc[q] = fma_bf16_lo(xv.x, wv.x, acc[q]);
+          acc[q] = fma_bf16_hi(xv.x, wv.x, acc[q]);
+          acc[q] = fma_bf16_lo(xv.y, wv.y, acc[q]);
+          acc[q] = fma_bf16_hi(xv.y, wv.y, acc[q]);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) acc[q] = __fadd_rn(acc[q], __shfl_xor_sync(0xffffffffu, acc[q], o));
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int rr = r0 + q;
+        if (lane == q && rr < R) {
+          float v = acc[q];
+          if (rr < G && bg != nullptr) v = __fadd_rn(v, bg[rr]);
+          logits[(size_t)p * R + rr] = v;
+        }
+      }
+    }
+    return;
+  }
+  for (int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < ntb * nrb; item += nw) {
+    const int p0 = (item / nrb) * 8, r0 = (item % nrb) * 8;
+    const __nv_bfloat16* xr[8];
+    const __nv_bfloat16* wr[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      xr[i] = x + (size_t)list[min(p0 + i, n - 1)] * d + 4 * lane;
+      const int rr = min(r0 + i, R - 1);
+      wr[i] = (rr < G ? wg + (size_t)rr * d : we + (size_t)(rr - G) * d) + 4 * lane;
+    }
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[i][q] = 0.f;
+#pragma unroll 2
+    for (int j = 0; j < d; j += 128) {
+      uint2 xv[8], wv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) { xv[i] = *reinterpret_cast<const uint2*>(xr[i] + j); wv[i] = *reinterpret_cast<const uint2*>(wr[i] + j); }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t a = u < 2 ? xv[i].x : xv[i].y;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t w = u < 2 ? wv[q].x : wv[q].y;
+            acc[i][q] = (u & 1) ? fma_bf16_hi(a, w, acc[i][q]) : fma_bf16_lo(a, w, acc[i][q]);
+          }
+        }
+    }
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      float v[32];
+#pragma unroll
+      for (int o = 0; o < 32; ++o) v[o] = acc[4 * hf + (o >> 3)][o & 7];
+      float out = butterfly_scatter32(v, lane);
+      const int p = p0 + 4 * hf + (lane >> 3), rr = r0 + (lane & 7);
+      if (rr < G && bg != nullptr) out = __fadd_rn(out, bg[rr]);
+      if (p < n && rr < R) logits[(size_t)p * R + rr] = out;
+    }
+  }
 }
 
 template <int TPW, int RPW, int WT, int WR, int MINB, int UNR>
@@ -420,10 +541,15 @@ static cudaError_t launch_smem_logits(const LayerArgs& a, const void* x, const v
 
 // Router logits and selection in one launch when a CTA can hold every router row of its tokens
 // (G + E <= 24, at least 1024 tokens); returns false (nothing launched) otherwise.
+static bool fused_route_ok(const LayerArgs& a) {
+  const int R = a.G + a.E, need = a.G > a.K ? a.G : a.K;
+  return a.bf16 && a.T >= 1024 && R <= 24 && need <= 8;
+}
+
 static bool launch_fused_route(const LayerArgs& a, const void* x, const void* wg, const float* bg, const void* we,
                                int32_t* gidx, int32_t* eidx, float* gate, cudaStream_t st, cudaError_t* err) {
   const int R = a.G + a.E, need = a.G > a.K ? a.G : a.K;
-  if (!a.bf16 || a.T < 1024 || R > 24 || need > 8) return false;
+  if (!fused_route_ok(a)) return false;
   if (R <= 16)
     *err = need <= 4 ? launch_smem_logits<2, 4>(a, x, wg, bg, we, nullptr, gidx, eidx, gate, st)
                      : launch_smem_logits<2, 8>(a, x, wg, bg, we, nullptr, gidx, eidx, gate, st);
@@ -454,18 +580,27 @@ static cudaError_t launch_logits(const LayerArgs& a, bool bf16, const void* x, c
 }
 
 cudaError_t launch_route(const LayerArgs& a, const void* x, const void* wg, const float* bg,
-                         const void* we, float* logits, int32_t* gidx, int32_t* eidx, float* gate,
-                         cudaStream_t st) {
+                         const void* we, float* logits, int32_t* redo, int32_t* gidx, int32_t* eidx,
+                         float* gate, DevStatus* status, bool status_zeroed, cudaStream_t st) {
   if (a.T == 0) return cudaSuccess;
   cudaError_t err = cudaSuccess;
+  if (!fused_route_ok(a) && route_tc_ok(a)) {
+    // tensor-core logits with verification, then the canonical order for the unverified tokens
+    if (!status_zeroed && (err = cudaMemsetAsync(&status->route_redo, 0, sizeof(int), st)) != cudaSuccess)
+      return err;
+    if ((err = launch_route_tc(a, x, wg, bg, we, gidx, eidx, gate, redo, status, st)) != cudaSuccess) return err;
+    const int* n = &status->route_redo;
+    launch_pdl(router_exact_list_kernel, dim3(148), dim3(256), 0, st, (const __nv_bfloat16*)x,
+               (const __nv_bfloat16*)wg, bg, (const __nv_bfloat16*)we, (const int32_t*)redo, n, a.d, a.G, a.E, logits);
+    prof_mark("router_exact_list", st);
+    launch_select_any(a, logits, redo, n, gidx, eidx, gate, st);
+    prof_mark("router_select_list", st);
+    return cudaGetLastError();
+  }
   if (launch_fused_route(a, x, wg, bg, we, gidx, eidx, gate, st, &err)) return err != cudaSuccess ? err : cudaGetLastError();
   err = launch_logits(a, a.bf16, x, wg, bg, we, logits, a.T, a.d, a.G, a.E, st);
   if (err != cudaSuccess) return err;
-  const int need = a.G > a.K ? a.G : a.K;
-  if (need <= 4) launch_select<4>(a, logits, gidx, eidx, gate, st);
-  else if (need <= 8) launch_select<8>(a, logits, gidx, eidx, gate, st);
-  else if (need <= 16) launch_select<16>(a, logits, gidx, eidx, gate, st);
-  else launch_select<32>(a, logits, gidx, eidx, gate, st);
+  launch_select_any(a, logits, nullptr, nullptr, gidx, eidx, gate, st);
   prof_mark("router_select", st);
   return cudaGetLastError();
 }

@@ -17,6 +17,10 @@ namespace tc {
 
 constexpr uint64_t kWaitNs = 2000000000ull;   // a bounded wait gives up after 2 s
 
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
@@ -59,7 +63,7 @@ struct Abort {
   DevStatus* status;      // global (may be null)
 };
 
-__device__ __noinline__ void report_timeout(const Abort& ab, int where) {
+static __device__ __noinline__ void report_timeout(const Abort& ab, int where) {
   *ab.flag = 1;
   if (ab.status) {
     atomicExch(&ab.status->code, (int)MOE_ERR_TIMEOUT);

@@ -1,8 +1,15 @@
 """Parity of the CUDA path (through the C ABI) with the CPU oracle.
 
-Bar: routing indices, gidx and every permutation output bit-exact; gates within 1e-6; layer
+Bar: routing indices, gidx and every permutation output bit-exact; gates within 2e-5; layer
 output y within max|y - y_ref| <= 2e-2 max|y_ref| and sum|y - y_ref| <= 5e-3 sum|y_ref|
 (BF16 inputs, FP32 accumulation).
+
+Gates: with at least 1024 BF16 tokens the router computes the logits on the tensor cores (an FP32
+sum in another order than the canonical one), settles every decision the error bound allows and
+recomputes the rest in the canonical order, so indices stay exact while the gates of verified
+tokens come from logits that differ from the canonical ones by a few units of 2^-24 sum|x_i w_i|
+(measured up to 3e-6 at d_model = 4096); a softmax moves by at most the largest change of its
+inputs, and 2e-5 leaves a margin above that.
 """
 import numpy as np
 import pytest
@@ -13,7 +20,7 @@ from synth import CONFIGS, MoEConfig, make_inputs, variant
 
 pytestmark = pytest.mark.gpu
 
-MAX_TOL, MEAN_TOL, GATE_TOL = 2e-2, 5e-3, 1e-6
+MAX_TOL, MEAN_TOL, GATE_TOL = 2e-2, 5e-3, 2e-5
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -124,6 +131,52 @@ def test_all_tokens_one_group_and_empty_experts():
     for key in ("expert_begin", "expert_count", "group_begin", "row_begin"):
         assert np.array_equal(p[key].cpu().numpy(), ref[key]), key
     check_y(out["y"], ref["y"])
+
+
+def route_redo(layer):
+    """Tokens the tensor-core router left to the canonical-order kernels in the last call (a
+    counter of the status word at the start of the workspace)."""
+    return int(layer.ws[12:16].view(torch.int32).item())
+
+
+@pytest.mark.parametrize("kind", ["group_rows", "expert_rows", "zero_tokens"])
+def test_tc_router_ties(kind):
+    """Exact ties (duplicated router rows, all-zero tokens) cannot be settled from the tensor-core
+    logits: those tokens go through the canonical order and the indices still equal the oracle's
+    (ties -> lower index)."""
+    cfg = small(T=2048, d=512, f=192, E=32, G=4, kg=2, ke=2, group_map="contiguous", seed=52, resid_std=0.2)
+    inp = make_inputs(cfg)
+    if kind == "group_rows":
+        inp["w_group"][1] = inp["w_group"][0]
+    elif kind == "expert_rows":
+        inp["w_expert"][3] = inp["w_expert"][5]
+    else:
+        inp["x"][::5] = 0
+    layer = device_layer(inp)
+    out = layer.forward()
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    redo = route_redo(layer)
+    ref = oracle.forward(inp)
+    check_routing(out, ref)
+    assert np.array_equal(out["perm"].cpu().numpy(), ref["perm"])
+    check_y(out["y"], ref["y"], kind)
+    assert 0 < redo < cfg.T
+    if kind == "zero_tokens":
+        assert redo >= (cfg.T + 4) // 5
+
+
+def test_tc_router_standalone_route_call():
+    """moe_hier_route on its own (no forward before it) clears the recompute counter itself."""
+    cfg = small(T=1536, d=256, E=32, G=4, kg=1, ke=2, seed=53)
+    inp = make_inputs(cfg)
+    layer = device_layer(inp)
+    ref = oracle.forward(inp)
+    for _ in range(3):
+        r = layer.route()
+        torch.cuda.synchronize()
+        check_routing(r, ref)
+        assert route_redo(layer) < cfg.T // 4
 
 
 def synthetic_eidx(T, group_map, G, kg, ke, seed, skew=0.0):
