@@ -202,6 +202,32 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N> __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// BF16 -> FP32 (exact: the 16 bits move to the top) of element u (0..3) of a 4-element piece.
+__device__ __forceinline__ float bf16_elem(const uint2& v, int u) {
+  const uint32_t w = u < 2 ? v.x : v.y;
+  return __uint_as_float((u & 1) ? (w & 0xffff0000u) : (w << 16));
+}
+
+// acc[i][q] += x_i[u] * w_q[u] for u = 0..3 in order (8 x 8 sums, each element rounded once per
+// FMA), with the operands converted once and the FMAs paired over (q, q+1): the same rounding
+// sequence as 256 scalar FMAs.
+__device__ __forceinline__ void fma_tile8x8(const uint2 (&xr)[8], const uint2 (&wr)[8], float2 (&acc)[8][4]) {
+  float2 wp[4][4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int qp = 0; qp < 4; ++qp) wp[u][qp] = make_float2(bf16_elem(wr[2 * qp], u), bf16_elem(wr[2 * qp + 1], u));
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float xv = bf16_elem(xr[i], u);
+      const float2 a = make_float2(xv, xv);
+#pragma unroll
+      for (int qp = 0; qp < 4; ++qp) acc[i][qp] = fma2(a, wp[u][qp], acc[i][qp]);
+    }
+}
+
 template <int RG, int L>
 __global__ void __launch_bounds__(128 * RG, RG <= 2 ? 2 : 1) router_logits_smem_kernel(
     const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ wg, const float* __restrict__ bg,
@@ -475,33 +501,23 @@ __global__ void __launch_bounds__(256, 1) router_exact_list_kernel(
       const int rr = min(r0 + i, R - 1);
       wr[i] = (rr < G ? wg + (size_t)rr * d : we + (size_t)(rr - G) * d) + 4 * lane;
     }
-    float acc[8][8];
+    float2 acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[i][q] = 0.f;
+      for (int q = 0; q < 4; ++q) acc[i][q] = make_float2(0.f, 0.f);
 #pragma unroll 2
     for (int j = 0; j < d; j += 128) {
       uint2 xv[8], wv[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) { xv[i] = *reinterpret_cast<const uint2*>(xr[i] + j); wv[i] = *reinterpret_cast<const uint2*>(wr[i] + j); }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t a = u < 2 ? xv[i].x : xv[i].y;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint32_t w = u < 2 ? wv[q].x : wv[q].y;
-            acc[i][q] = (u & 1) ? fma_bf16_hi(a, w, acc[i][q]) : fma_bf16_lo(a, w, acc[i][q]);
-          }
-        }
+      fma_tile8x8(xv, wv, acc);
     }
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
       float v[32];
 #pragma unroll
-      for (int o = 0; o < 32; ++o) v[o] = acc[4 * hf + (o >> 3)][o & 7];
+      for (int o = 0; o < 32; ++o) v[o] = (o & 1) ? acc[4 * hf + (o >> 3)][(o & 7) >> 1].y : acc[4 * hf + (o >> 3)][(o & 7) >> 1].x;
       float out = butterfly_scatter32(v, lane);
       const int p = p0 + 4 * hf + (lane >> 3), rr = r0 + (lane & 7);
       if (rr < G && bg != nullptr) out = __fadd_rn(out, bg[rr]);

@@ -166,6 +166,30 @@ def test_tc_router_ties(kind):
         assert redo >= (cfg.T + 4) // 5
 
 
+def test_recomputed_logits_are_canonical_bits():
+    """The canonical-order kernel's logits of the tokens the tensor-core router left over equal the
+    oracle's FP32 canonical logits bit for bit (read from the workspace: status word, then the
+    [T][G+E] logits scratch, then the [T] token list, each region 256-byte aligned)."""
+    cfg = small(T=2048, d=512, f=192, E=32, G=4, kg=2, ke=2, group_map="contiguous", seed=54, resid_std=0.2)
+    inp = make_inputs(cfg)
+    inp["w_group"][2] = inp["w_group"][1]                   # many exact ties -> many recomputed tokens
+    layer = device_layer(inp)
+    layer.route()
+    torch.cuda.synchronize()
+    n = route_redo(layer)
+    assert n > 100
+    R = cfg.G + cfg.E
+    off_logits = 256
+    off_redo = off_logits + (cfg.T * R * 4 + 255) // 256 * 256
+    toks = layer.ws[off_redo:off_redo + 4 * n].view(torch.int32).cpu().numpy()
+    got = layer.ws[off_logits:off_logits + 4 * n * R].view(torch.float32).cpu().numpy().reshape(n, R)
+    assert len(set(toks.tolist())) == n and toks.min() >= 0 and toks.max() < cfg.T
+    x = oracle.moe._np(inp["x"])[toks]
+    want = np.concatenate([oracle.canonical_logits(x, oracle.moe._np(inp["w_group"])),
+                           oracle.canonical_logits(x, oracle.moe._np(inp["w_expert"]))], axis=1)
+    assert np.array_equal(got.view(np.uint32), want.astype(np.float32).view(np.uint32))
+
+
 def test_tc_router_standalone_route_call():
     """moe_hier_route on its own (no forward before it) clears the recompute counter itself."""
     cfg = small(T=1536, d=256, E=32, G=4, kg=1, ke=2, seed=53)
