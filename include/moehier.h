@@ -102,7 +102,12 @@ typedef struct {
 size_t moe_hier_workspace_size(const moe_hier_desc* desc, int* status_out);
 
 /* Level-1 and level-2 routing ("Breaking the MoE LLM Trilemma", key design 3).
- * Writes gidx, eidx and gate (shapes above).  Uses the workspace for the logits. */
+ * Writes gidx, eidx and gate (shapes above).  Uses the workspace for the logits and, on the
+ * tensor-core path (BF16, T >= 1024, router rows beyond what the fused kernel holds), for the
+ * list of tokens whose decision the tensor-core logits do not settle provably: those are
+ * recomputed in the canonical FP32 order, so the indices are the canonical ones in every case;
+ * the gates of the other tokens come from the tensor-core logits (another FP32 summation order,
+ * "router in FP32", routing-mechanisms page §3.1). */
 int moe_hier_route(const moe_hier_desc* desc, const void* x, const void* w_group,
                    const float* b_group, const void* w_expert, const int32_t* group_map_host,
                    int32_t* gidx, int32_t* eidx, float* gate,
