@@ -78,6 +78,9 @@ CASES = {
     "bf16_rows2100_ke3": small(T=2100, d=256, f=192, E=16, G=4, kg=1, ke=3, seed=44, resid_std=0.2),
     "bf16_rows2100_ke4": small(T=2100, d=256, f=320, E=16, G=4, kg=1, ke=4, seed=45, resid_std=0.2),
     "bf16_fused_route_L8": small(T=1500, d=256, f=192, E=16, G=8, kg=2, ke=2, seed=46, resid_std=0.2),
+    # tensor-core router, general selection path (more than 8 members, more than 8 groups)
+    "bf16_tc_route_K16": small(T=1200, d=256, f=192, E=64, G=4, kg=2, ke=3, seed=48, resid_std=0.2),
+    "bf16_tc_route_G16": small(T=1300, d=256, f=192, E=64, G=16, kg=3, ke=2, seed=49, resid_std=0.2),
     "bf16_K32": small(T=300, E=128, G=4, kg=2, ke=3, group_map="perm", seed=36, resid_std=0.2),
     "bf16_G64": small(T=200, E=128, G=64, kg=3, ke=2, group_map="perm", seed=37, resid_std=0.2),
     "bf16_K1": small(T=200, E=4, G=4, kg=2, ke=1, seed=28),
@@ -166,19 +169,28 @@ def test_tc_router_ties(kind):
         assert redo >= (cfg.T + 4) // 5
 
 
-def test_recomputed_logits_are_canonical_bits():
+@pytest.mark.parametrize("many", [True, False])
+def test_recomputed_logits_are_canonical_bits(many):
     """The canonical-order kernel's logits of the tokens the tensor-core router left over equal the
     oracle's FP32 canonical logits bit for bit (read from the workspace: status word, then the
-    [T][G+E] logits scratch, then the [T] token list, each region 256-byte aligned)."""
+    [T][G+E] logits scratch, then the [T] token list, each region 256-byte aligned).  Many listed
+    tokens take the 8-token tiles, few the one-token-per-warp form."""
     cfg = small(T=2048, d=512, f=192, E=32, G=4, kg=2, ke=2, group_map="contiguous", seed=54, resid_std=0.2)
     inp = make_inputs(cfg)
-    inp["w_group"][2] = inp["w_group"][1]                   # many exact ties -> many recomputed tokens
+    if many:
+        inp["w_group"][2] = inp["w_group"][1]               # exact ties for most tokens
+    else:
+        inp["w_expert"][9] = inp["w_expert"][10]            # ties for the tokens that reach them
     layer = device_layer(inp)
     layer.route()
     torch.cuda.synchronize()
     n = route_redo(layer)
-    assert n > 100
     R = cfg.G + cfg.E
+    nw = 148 * 8                                            # warps of the recompute launch
+    if many:
+        assert n * ((R + 7) // 8) > 2 * nw
+    else:
+        assert 0 < n and n * ((R + 7) // 8) <= 2 * nw
     off_logits = 256
     off_redo = off_logits + (cfg.T * R * 4 + 255) // 256 * 256
     toks = layer.ws[off_redo:off_redo + 4 * n].view(torch.int32).cpu().numpy()
