@@ -273,6 +273,24 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
+# ------------------------------------------------------------------ multi-rank aggregation
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time, on every rank: the job is done when its last rank is.  Ranks are
+    independent replicas, so this reduction of one number is the only cross-rank exchange."""
+    if world == 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_rank: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank * steps / (ms / 1e3)
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -368,12 +386,8 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError("device status after timed steps: %d" % layer.status())
 
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * cfg.T * K / (total_ms / 1e3)
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    value = job_tokens_per_s(world, cfg.T, K, total_ms)
 
     # ---- end to end through the C ABI with host buffers (copies inside the timed region).  Every
     # step copies its x from pinned host memory, runs moe_hier_forward and copies its y back; the
@@ -425,11 +439,8 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = e_start.elapsed_time(e_end)
     if not torch.equal(y_h[(K - 1) & 1], outs[(K - 1) & 1]["y"].cpu()):
         raise RuntimeError("end-to-end output differs from the device result")
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * cfg.T * K / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    e2e_value = job_tokens_per_s(world, cfg.T, K, e2e_ms)
     act_b = 2 if cfg.dtype == "bf16" else 4
 
     # ---- roofline of the dominant kernel (its own algorithmic work / its mean event time)
