@@ -328,6 +328,7 @@ def run_ours(args, rank, world, local_rank):
     eidx = out["eidx"].cpu()
     experts_hit = int(torch.unique(eidx).numel())
     groups_hit = int(torch.unique(out["gidx"].cpu()).numel())
+    load = workload.load_stats(out["gidx"].cpu().numpy(), eidx.numpy(), cfg.G, cfg.E)
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
@@ -474,7 +475,9 @@ def run_ours(args, rank, world, local_rank):
                    "E": cfg.E, "G": cfg.G, "top_k_group": cfg.kg, "top_k_expert": cfg.ke,
                    "rank": cfg.r, "parallelism": "replicas" if world > 1 else "single",
                    "l2": "flushed between timed steps (256 MiB write)",
-                   "groups_hit": groups_hit, "experts_hit": experts_hit},
+                   "groups_hit": groups_hit, "experts_hit": experts_hit,
+                   "load_max_over_mean": {"group": round(load["group"]["max_over_mean"], 3),
+                                          "expert": round(load["expert"]["max_over_mean"], 3)}},
         "roofline": roof,
         "achieved_tflops_step": round(workload.flops(cfg) / (step_mean / 1e3) / 1e12, 2),
         "kernels_ms": {n: round(statistics.mean(v), 5) for n, v in kern_ms.items()},

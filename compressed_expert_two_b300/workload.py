@@ -65,3 +65,21 @@ def kernel_work(cfg, kernel: str, groups_hit: int, experts_hit: int, T=None):
     if kernel.startswith("router"):
         return 2.0 * d * (cfg.G + cfg.E) * T, (T + cfg.G + cfg.E) * d * s_act
     return flops(cfg, T), bytes_moved(cfg, groups_hit, experts_hit, T)
+
+
+def load_stats(gidx, eidx, G: int, E: int) -> dict:
+    """Load balance of one batch's routing (the imbalance the clustering is meant to bound; the
+    pages report load variance and the max/mean ratio): rows per group (one per token and chosen
+    group) and assignments per expert, from the router's gidx [T][k_g] and eidx [T][k] (integer
+    arrays or tensors).  max/mean is 1 for a perfectly even batch; cv = std/mean of the loads."""
+    import numpy as np
+    g = np.bincount(np.asarray(gidx).reshape(-1), minlength=G).astype(np.float64)
+    e = np.bincount(np.asarray(eidx).reshape(-1), minlength=E).astype(np.float64)
+
+    def summary(c):
+        m = c.mean()
+        return {"max_over_mean": float(c.max() / m) if m > 0 else 0.0,
+                "cv": float(c.std() / m) if m > 0 else 0.0,
+                "min": int(c.min()), "max": int(c.max())}
+
+    return {"group": summary(g), "expert": summary(e)}

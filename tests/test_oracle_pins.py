@@ -285,3 +285,4 @@ def test_compression_ratio_closed_form():
     pc = oracle.param_counts(d=4096, f=4096, E=8, G=1, r=16)
     # one matrix type of one group reproduces CR exactly
     assert pc["standard"] / pc["clustered"] == pytest.approx(cr, rel=1e-12)
+
