@@ -213,16 +213,28 @@ __global__ void __launch_bounds__(256) resid_prep_t_kernel(PrepArgs p, GroupTabl
 // ------------------------------------------------------------------------------------------
 // 2. X rows in (group, token) order
 // ------------------------------------------------------------------------------------------
+// One warp per row (grid-stride over rows): the row's token is looked up once, then each lane
+// moves four 16-byte pieces per round with all four loads in flight before the stores.
 __global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ row_asg,
                                    int R, int d, int kg, __nv_bfloat16* __restrict__ X) {
   pdl_wait();
   pdl_trigger();
-  const int per_row = d / 8;
-  const size_t n = (size_t)R * per_row;
-  for (size_t w = blockIdx.x * (size_t)blockDim.x + threadIdx.x; w < n; w += (size_t)gridDim.x * blockDim.x) {
-    const int i = (int)(w / per_row), c = (int)(w % per_row) * 8;
+  const int per_row = d / 8;                       // 16-byte pieces per row (d % 128 == 0)
+  const int lane = threadIdx.x & 31;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  for (int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < R; i += nw) {
     const int t = row_asg[i] / kg;
-    *reinterpret_cast<uint4*>(X + (size_t)i * d + c) = *reinterpret_cast<const uint4*>(x + (size_t)t * d + c);
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    uint4* dst = reinterpret_cast<uint4*>(X + (size_t)i * d);
+    for (int c = lane; c < per_row; c += 128) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c + 32 * u < per_row) v[u] = src[c + 32 * u];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c + 32 * u < per_row) dst[c + 32 * u] = v[u];
+    }
   }
 }
 
