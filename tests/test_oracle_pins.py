@@ -77,6 +77,45 @@ def test_canonical_logits_fp64_error_bound():
     assert np.all(np.abs(got - exact) <= n * 2.0 ** -24 * mag * 1.01)
 
 
+def test_canonical_routing_differs_from_fp64_only_at_near_ties():
+    """The canonical FP32 logits decide like exact (FP64) logits except where two candidates lie
+    within the canonical order's rounding bound of each other: every token whose FP64 routing
+    differs has such a near tie, and forcing exact ties (duplicated router rows) makes the lower
+    index win in both."""
+    rng = np.random.default_rng(3)
+    T, d, G, K, kg, ke = 400, 256, 4, 4, 2, 2
+    E = G * K
+    gm = np.arange(E) // K
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    wg = (rng.standard_normal((G, d)) / math.sqrt(d)).astype(np.float32)
+    we = (rng.standard_normal((E, d)) / math.sqrt(d)).astype(np.float32)
+    we[5] = we[6]                                             # exact ties inside group 1
+    r = oracle.route(x, wg, None, we, gm, kg, ke)
+    ex_g = x.astype(np.float64) @ wg.astype(np.float64).T
+    ex_e = x.astype(np.float64) @ we.astype(np.float64).T
+    bound_g = (d // 32 + 6) * 2.0 ** -24 * (np.abs(x) @ np.abs(wg).T)
+    bound_e = (d // 32 + 6) * 2.0 ** -24 * (np.abs(x) @ np.abs(we).T)
+    def has_near_tie(vals, bnd, cands):
+        return any(abs(vals[a] - vals[b]) <= bnd[a] + bnd[b] for a in cands for b in cands if a < b)
+
+    for t in range(T):
+        gs = sorted(range(G), key=lambda g: (-ex_g[t, g], g))[:kg]
+        if gs != list(r["gidx"][t]):
+            assert has_near_tie(ex_g[t], bound_g[t], range(G)), t
+            continue
+        for j, g in enumerate(gs):
+            mem = list(np.nonzero(gm == g)[0])
+            es = sorted(mem, key=lambda e: (-ex_e[t, e], e))[:ke]
+            if es != list(r["eidx"][t, j * ke:(j + 1) * ke]):
+                assert has_near_tie(ex_e[t], bound_e[t], mem), t
+    # the duplicated rows: wherever both are picked, the lower id comes first
+    for t in range(T):
+        for j in range(kg):
+            picks = list(r["eidx"][t, j * ke:(j + 1) * ke])
+            if 5 in picks and 6 in picks:
+                assert picks.index(5) < picks.index(6)
+
+
 # ------------------------------------------------------------------ INT4 format
 def test_int4_golden_convention():
     spec = json.load(open(os.path.join(GOLDEN, "int4_convention.json")))
