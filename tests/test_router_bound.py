@@ -1,0 +1,71 @@
+"""The error bound the tensor-core router verifies its decisions with (CPU, no GPU).
+
+The tensor-core router accepts a token's decision only when every pick's interval
+[s - delta, s + delta] clears the next candidate's, with
+    delta = c(d) * ||x|| * ||w|| + 2^-22 |s|,  c(d) = 1.01 ((d/8 + 8) 2^-22 + (d/32 + 6) 2^-24)
+(the constant of the router kernel).  This checks the bound against the canonical FP32 order of
+the oracle and against FP32 sums in other orders a tensor core may use: 16-product blocks summed
+exactly and added into an FP32 accumulator rounded to nearest or truncated, in one accumulator or
+in four interleaved ones.  Every such sum must lie within delta of the canonical logit.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+
+
+def c_err(d: int) -> float:
+    return 1.01 * ((d / 8 + 8) * 2.0 ** -22 + (d / 32 + 6) * 2.0 ** -24)
+
+
+def to_f32(v: np.ndarray, mode: str) -> np.ndarray:
+    """FP64 -> FP32, round to nearest or toward zero."""
+    f = v.astype(np.float32)
+    if mode == "rz":
+        over = np.abs(f.astype(np.float64)) > np.abs(v)
+        f = np.where(over, np.nextafter(f, np.float32(0)), f)
+    return f
+
+
+def blocked_sum(x: np.ndarray, w: np.ndarray, mode: str, n_acc: int) -> np.ndarray:
+    """sum_i x_i w_i: exact 16-product blocks, added into n_acc FP32 accumulators in turn
+    (block b into accumulator b mod n_acc), each add rounded by `mode`; the accumulators are
+    summed in FP32 at the end."""
+    d = x.shape[1]
+    prod = x.astype(np.float64)[:, None, :] * w.astype(np.float64)[None, :, :]   # exact
+    blocks = prod.reshape(prod.shape[0], prod.shape[1], d // 16, 16).sum(-1)     # exact enough
+    acc = np.zeros((n_acc,) + blocks.shape[:2], dtype=np.float32)
+    for b in range(blocks.shape[2]):
+        a = b % n_acc
+        acc[a] = to_f32(acc[a].astype(np.float64) + blocks[:, :, b], mode)
+    out = acc[0]
+    for a in range(1, n_acc):
+        out = (out + acc[a]).astype(np.float32)
+    return out
+
+
+def bf16(a: np.ndarray) -> np.ndarray:
+    """Round FP32 values to BF16 (nearest even), kept as FP32."""
+    u = a.astype(np.float32).view(np.uint32)
+    u = ((u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000).astype(np.uint32)
+    return u.view(np.float32)
+
+
+@pytest.mark.parametrize("d", [256, 1024, 4096])
+@pytest.mark.parametrize("mode,n_acc", [("rn", 1), ("rz", 1), ("rz", 4)])
+def test_tensor_core_orders_stay_inside_the_bound(d, mode, n_acc):
+    rng = np.random.default_rng(d + n_acc)
+    x = bf16(rng.standard_normal((24, d)).astype(np.float32))
+    w = bf16((rng.standard_normal((12, d)) / math.sqrt(d)).astype(np.float32))
+    x[0] *= 1e3                                          # a large token
+    w[1] = np.abs(w[1])                                  # a row with a large sum|x w| / |s| ratio
+    canon = oracle.canonical_logits(x, w).astype(np.float64)
+    other = blocked_sum(x, w, mode, n_acc).astype(np.float64)
+    delta = c_err(d) * np.linalg.norm(x.astype(np.float64), axis=1)[:, None] * \
+        np.linalg.norm(w.astype(np.float64), axis=1)[None, :] + 2.0 ** -22 * np.abs(other)
+    diff = np.abs(other - canon)
+    assert np.all(diff <= delta)
+    # and the bound is not vacuous: the realised differences use a small part of it
+    assert diff.max() <= 0.05 * delta.max()
