@@ -31,7 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer fwd tokens/s on 1 B300; % of BF16 tensor or HBM roofline"
-DEFAULT_CONFIG = "small_bf16_int4"
+DEFAULT_CONFIG = "mixtral_prefill"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 

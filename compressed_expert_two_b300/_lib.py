@@ -33,7 +33,8 @@ class MoeHierResid(ctypes.Structure):
 
 EXPORTS = ["moe_hier_workspace_size", "moe_hier_route", "moe_hier_permute", "moe_hier_ffn",
            "moe_hier_combine", "moe_hier_forward", "moe_hier_get_status", "moe_hier_status_string",
-           "moe_hier_last_cuda_error", "moe_hier_profile_begin", "moe_hier_profile_end"]
+           "moe_hier_last_cuda_error", "moe_hier_profile_begin", "moe_hier_profile_end",
+           "moe_hier_debug_set_wait", "moe_hier_debug_route_tc", "moe_hier_permute_noalloc"]
 
 
 class MoeError(RuntimeError):
@@ -64,6 +65,9 @@ def _load() -> ctypes.CDLL:
     lib.moe_hier_profile_end.argtypes = [ctypes.POINTER(ctypes.c_char_p), I]
     lib.moe_hier_status_string.argtypes = [I]
     lib.moe_hier_status_string.restype = ctypes.c_char_p
+    lib.moe_hier_debug_set_wait.argtypes = [ctypes.c_uint64, I]
+    lib.moe_hier_debug_route_tc.argtypes = [D, P, P, P, P, P, P, P, S, P]
+    lib.moe_hier_permute_noalloc.argtypes = [D] + [P] * 11
     lib.moe_hier_last_cuda_error.argtypes = []
     lib.moe_hier_last_cuda_error.restype = ctypes.c_char_p
     for name in EXPORTS:
@@ -146,6 +150,23 @@ def moe_hier_profile_end(max_names: int = 256) -> list:
     names = (ctypes.c_char_p * max_names)()
     n = lib.moe_hier_profile_end(names, max_names)
     return [names[i].decode() for i in range(min(n, max_names))]
+
+
+def moe_hier_permute_noalloc(desc, group_map_host, eidx, perm, inv_pos, expert_begin, expert_count,
+                             group_begin, row_asg, row_of, row_begin, stream):
+    _check("moe_hier_permute_noalloc", lib.moe_hier_permute_noalloc(
+        ctypes.byref(desc), _p(group_map_host), _p(eidx), _p(perm), _p(inv_pos), _p(expert_begin),
+        _p(expert_count), _p(group_begin), _p(row_asg), _p(row_of), _p(row_begin), stream))
+
+
+def moe_hier_debug_set_wait(wait_ns: int, phantom_arrivals: int) -> None:
+    _check("moe_hier_debug_set_wait", lib.moe_hier_debug_set_wait(wait_ns, phantom_arrivals))
+
+
+def moe_hier_debug_route_tc(desc, x, w_group, b_group, w_expert, group_map_host, out, ws, ws_bytes, stream):
+    _check("moe_hier_debug_route_tc", lib.moe_hier_debug_route_tc(
+        ctypes.byref(desc), _p(x), _p(w_group), _p(b_group), _p(w_expert), _p(group_map_host), _p(out),
+        _p(ws), ws_bytes, stream))
 
 
 def moe_hier_get_status(ws, stream) -> int:

@@ -196,6 +196,19 @@ static SideStream* side_stream() {
   return &g_side;
 }
 
+// Test setting of the permutation's grid-wide wait (moe_hier_debug_set_wait); read by
+// moe_hier_permute only.
+static std::atomic<uint64_t> g_wait_ns{0};
+static std::atomic<unsigned int> g_wait_phantom{0};
+
+static PermWait perm_wait_setting() {
+  PermWait w = kPermWaitDefault;
+  const uint64_t ns = g_wait_ns.load(std::memory_order_relaxed);
+  if (ns) w.limit_ns = ns;
+  w.phantom = g_wait_phantom.load(std::memory_order_relaxed);
+  return w;
+}
+
 // The last CUDA error a call of this host thread returned as MOE_ERR_CUDA.
 static thread_local cudaError_t g_last_cuda_error = cudaSuccess;
 
@@ -251,7 +264,8 @@ int moe_hier_permute(const moe_hier_desc* desc, const int32_t* group_map_host, c
   PermOut o{perm, inv_pos, expert_begin, expert_count, group_begin, row_asg, row_of, row_begin};
   prof_start((cudaStream_t)stream);
   return cuda_status(launch_permute(a, eidx, o, at<int32_t>(ws, p.cnt), at<int32_t>(ws, p.off),
-                                    p.nblk, at<DevStatus>(ws, p.status), false, (cudaStream_t)stream));
+                                    p.nblk, at<DevStatus>(ws, p.status), false, (cudaStream_t)stream,
+                                    perm_wait_setting()));
 }
 
 int moe_hier_ffn(const moe_hier_desc* desc, const void* x, const int32_t* group_map_host,
@@ -338,6 +352,34 @@ int moe_hier_forward(const moe_hier_desc* desc, const void* x, const void* w_gro
     const cudaError_t j = cudaStreamWaitEvent(s, prep_done, 0);
     if (e == cudaSuccess) e = j;
   }
+  return cuda_status(e);
+}
+
+int moe_hier_debug_set_wait(uint64_t wait_ns, int phantom_arrivals) {
+  if (phantom_arrivals < 0) return MOE_ERR_INVALID;
+  g_wait_ns.store(wait_ns, std::memory_order_relaxed);
+  g_wait_phantom.store((unsigned int)phantom_arrivals, std::memory_order_relaxed);
+  return MOE_OK;
+}
+
+int moe_hier_debug_route_tc(const moe_hier_desc* desc, const void* x, const void* w_group, const float* b_group,
+                            const void* w_expert, const int32_t* group_map_host, float* out, void* ws,
+                            size_t ws_bytes, void* stream) {
+  LayerArgs a;
+  if (!group_map_host) return MOE_ERR_INVALID;
+  int st = validate(desc, group_map_host, &a);
+  if (st != MOE_OK) return st;
+  if (!route_tc_ok(a)) return MOE_ERR_UNSUPPORTED;
+  if (!x || !w_group || !w_expert || !out) return MOE_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(w_group) || !aligned16(w_expert)) return MOE_ERR_INVALID;
+  const Plan p = make_plan(a);
+  if ((st = check_ws(p, ws, ws_bytes)) != MOE_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  DevStatus* status = at<DevStatus>(ws, p.status);
+  cudaError_t e = cudaMemsetAsync(&status->route_redo, 0, sizeof(int), s);
+  if (e == cudaSuccess)
+    e = launch_route_tc(a, x, w_group, b_group, w_expert, at<int32_t>(ws, p.gidx), at<int32_t>(ws, p.eidx),
+                        at<float>(ws, p.gate), at<int32_t>(ws, p.redo), status, s, out);
   return cuda_status(e);
 }
 

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "../../include/moehier.h"
@@ -47,6 +48,22 @@ template <typename... KArgs, typename... Args>
 static inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                                      Args&&... args) {
   return launch_pdl_cluster(kernel, grid, block, dim3(1, 1, 1), smem, st, std::forward<Args>(args)...);
+}
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current device, once per device
+// (`done` holds one bit per device index; the attribute belongs to the device, so a process that
+// drives several GPUs sets it on each).  Setting it twice is harmless, so two host threads that
+// race on a device's first launch only repeat the call.
+template <typename K>
+static inline cudaError_t smem_attr_once(K kernel, size_t bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
 }
 
 constexpr int kMaxE = 256;

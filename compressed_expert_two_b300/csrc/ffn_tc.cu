@@ -2134,11 +2134,6 @@ static bool make_map_plain(CUtensorMap* m, const void* base, uint64_t rows, uint
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename K>
-static cudaError_t set_smem(K kernel, size_t bytes) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-}
-
 bool tc_path_ok(const LayerArgs& a) {
   const int KRP = ((a.K * a.r + 63) / 64) * 64;
   return a.bf16 && a.int4 && a.r == kRank && a.K * a.r <= 128 && KRP <= 128 && a.ke <= kMaxKe &&
@@ -2180,12 +2175,8 @@ static cudaError_t launch_gemm(const CUtensorMap& A0, const CUtensorMap& A1, con
                                const int32_t* scatter, DevStatus* st, cudaStream_t stream) {
   constexpr int STAGES = BN >= 256 ? 4 : 6;
   const size_t smem = 1024 + (size_t)STAGES * (kTile * 128 + BN * 128);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = set_smem(tc_gemm_kernel<BN, STAGES, OUT>, smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  if (const cudaError_t e = smem_attr_once(tc_gemm_kernel<BN, STAGES, OUT>, smem, attr); e != cudaSuccess) return e;
   dim3 grid(n_out / BN, tiles);
   return launch_pdl(tc_gemm_kernel<BN, STAGES, OUT>, grid, dim3(192), smem, stream, A0, A1, B0, B1, nk0, nk1,
                     row_begin, G, b_stride, b1_off, out, out_ld, scatter, st);
@@ -2199,18 +2190,12 @@ static cudaError_t launch_gemm_persist(const CUtensorMap& A0, const CUtensorMap&
                                        const int32_t* scatter, DevStatus* st, cudaStream_t stream) {
   constexpr int STAGES = BN >= 256 ? 4 : 6;
   const size_t smem = 1024 + (size_t)STAGES * (kTile * 128 + BN * 128);
-  static bool attr = false;
-  static int sms = 0;
-  if (!attr) {
-    cudaError_t e = set_smem(tc_gemm_persist_kernel<BN, STAGES, OUT>, smem);
-    if (e == cudaSuccess) {
-      int dev = 0;
-      e = cudaGetDevice(&dev);
-      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    }
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  if (const cudaError_t e = smem_attr_once(tc_gemm_persist_kernel<BN, STAGES, OUT>, smem, attr); e != cudaSuccess)
+    return e;
+  int dev = 0, sms = 0;
+  if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return e;
+  if (cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev); e != cudaSuccess) return e;
   const int n_tiles = n_out / BN, items = tiles * n_tiles;
   return launch_pdl(tc_gemm_persist_kernel<BN, STAGES, OUT>, dim3(items < sms ? items : sms), dim3(192), smem, stream,
                     A0, A1, B0, B1, nk0, nk1, row_begin, G, b_stride, b1_off, tiles, n_tiles, out, out_ld, scatter, st);
@@ -2225,12 +2210,8 @@ static cudaError_t launch_gemm_pair(const CUtensorMap& A0, const CUtensorMap& A1
                                     const int32_t* scatter, DevStatus* st, cudaStream_t stream, int dense_rows = 0) {
   constexpr int STAGES = BN >= 256 ? 6 : 8;
   const size_t smem = 1024 + (size_t)STAGES * (kTile * 128 + (BN / 2) * 128);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = set_smem(tc_gemm_pair_kernel<BN, STAGES, OUT>, smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  if (const cudaError_t e = smem_attr_once(tc_gemm_pair_kernel<BN, STAGES, OUT>, smem, attr); e != cudaSuccess) return e;
   return launch_pdl_cluster(tc_gemm_pair_kernel<BN, STAGES, OUT>, dim3(2 * pairs, n_out / BN), dim3(192),
                             dim3(2, 1, 1), smem, stream, A0, A1, B0, B1, nk0, nk1, row_begin, G, b_stride, b1_off,
                             out, out_ld, scatter, st, dense_rows);
@@ -2242,12 +2223,8 @@ static cudaError_t launch_up_ke(const CUtensorMap* maps, const UpArgs& p, int nc
   constexpr int RBUF = KRP >= 128 ? 1 : 2;
   const size_t smem = 1024 + (size_t)STAGES * (kTile * 128 + 2 * kNf * 128) +
                       (size_t)RBUF * (2 * (KRP * kNf * 2) + KRP * 128) + 2 * (kTile * KRP * 2) + kTile * 128;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = set_smem(ffn_up_tc_kernel<KRP, STAGES, KE, RBUF>, smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  if (const cudaError_t e = smem_attr_once(ffn_up_tc_kernel<KRP, STAGES, KE, RBUF>, smem, attr); e != cudaSuccess) return e;
   dim3 grid(nchunks, tiles);
   return launch_pdl(ffn_up_tc_kernel<KRP, STAGES, KE, RBUF>, grid, dim3(kUpWarps * 32), smem, stream, maps[0],
                     maps[1], maps[2], maps[3], maps[4], maps[5], p);
@@ -2257,12 +2234,8 @@ template <int KE>
 static cudaError_t launch_up4p(const CUtensorMap* maps, const UpArgs& p, int nchunks, int pairs, cudaStream_t stream) {
   const size_t smem = 1024 + (size_t)kStages4p * (kTile * 128 + kNf3 * 128) + 2 * (size_t)((kNf3 / 2) * 64 * 2) +
                       (size_t)kNf3 * 64 * 2 + 2 * (size_t)(kTile * 64 * 2);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = set_smem(ffn_up4p_kernel<KE>, smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  if (const cudaError_t e = smem_attr_once(ffn_up4p_kernel<KE>, smem, attr); e != cudaSuccess) return e;
   return launch_pdl_cluster(ffn_up4p_kernel<KE>, dim3(2 * pairs, nchunks), dim3(kUpWarps * 32), dim3(2, 1, 1), smem,
                             stream, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
 }
@@ -2271,12 +2244,8 @@ template <int KE>
 static cudaError_t launch_up3(const CUtensorMap* maps, const UpArgs& p, int nchunks, int tiles, cudaStream_t stream) {
   const size_t smem = 1024 + (size_t)kStages3 * (kTile * 128 + 2 * kNf3 * 128) + 2 * (size_t)(kNf3 * 64 * 2) +
                       (size_t)64 * kNf3 * 2 + 2 * (size_t)(kTile * 64 * 2);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = set_smem(ffn_up3_kernel<KE>, smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  if (const cudaError_t e = smem_attr_once(ffn_up3_kernel<KE>, smem, attr); e != cudaSuccess) return e;
   return launch_pdl(ffn_up3_kernel<KE>, dim3(nchunks, tiles), dim3(kUp3Warps * 32), smem, stream, maps[0], maps[1],
                     maps[2], maps[3], maps[4], maps[5], p);
 }

@@ -46,17 +46,28 @@ cudaError_t launch_route(const LayerArgs& a, const void* x, const void* wg, cons
 // lists the others in redo[0 .. status->route_redo).
 bool route_tc_ok(const LayerArgs& a);
 int route_tc_columns(const LayerArgs& a);
+// dbg (test aid): null, or [T][2 (G + E)] FP32 receiving each token's tensor-core logits (groups,
+// then experts, bias included) and the verification half-widths delta of the same candidates.
 cudaError_t launch_route_tc(const LayerArgs& a, const void* x, const void* wg, const float* bg, const void* we,
                             int32_t* gidx, int32_t* eidx, float* gate, int32_t* redo, DevStatus* status,
-                            cudaStream_t st);
+                            cudaStream_t st, float* dbg = nullptr);
 // BF16 [rows][cols] tensor map, box {64, box_rows}, 128-byte swizzle (ffn_tc.cu).
 bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 
 struct PermOut {
   int32_t *perm, *inv_pos, *ebeg, *ecnt, *gbeg, *row_asg, *row_of, *rbeg;
 };
+// Limit of the cooperative permutation's grid-wide wait and the arrivals it expects beyond the
+// permutation's own blocks (0 in normal use; a positive count makes the wait run out, which is how
+// the failure path is tested without faulting or hanging the GPU).
+struct PermWait {
+  uint64_t limit_ns;
+  unsigned int phantom;
+};
+constexpr PermWait kPermWaitDefault{2000000000ull, 0u};
 cudaError_t launch_permute(const LayerArgs& a, const int32_t* eidx, const PermOut& o, int32_t* cnt,
-                           int32_t* off, int nblk, DevStatus* status, bool bar_zeroed, cudaStream_t st);
+                           int32_t* off, int nblk, DevStatus* status, bool bar_zeroed, cudaStream_t st,
+                           PermWait wait = kPermWaitDefault);
 
 struct ResidPtrs {
   ResidView A[3], B[3];

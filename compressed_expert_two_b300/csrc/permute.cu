@@ -275,11 +275,11 @@ __device__ __forceinline__ uint64_t perm_now_ns() {
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
   return t;
 }
-constexpr uint64_t kPermWaitNs = 2000000000ull;     // the grid barrier gives up after 2 s
-
+// The grid barrier waits for gridDim.x + wait.phantom arrivals and gives up after wait.limit_ns
+// (2 s in normal use, with no phantom arrivals).
 __global__ void __launch_bounds__(kCoopBlock) perm_coop_kernel(
     const int32_t* __restrict__ eidx, GroupTable tab, int Tn, int kg, int ke, int32_t* __restrict__ cnt,
-    DevStatus* status, int32_t* __restrict__ perm, int32_t* __restrict__ inv_pos, int32_t* __restrict__ ebeg,
+    DevStatus* status, PermWait wait, int32_t* __restrict__ perm, int32_t* __restrict__ inv_pos, int32_t* __restrict__ ebeg,
     int32_t* __restrict__ ecnt, int32_t* __restrict__ gbeg, int32_t* __restrict__ row_asg,
     int32_t* __restrict__ row_of, int32_t* __restrict__ rbeg) {
   pdl_wait();
@@ -328,8 +328,8 @@ __global__ void __launch_bounds__(kCoopBlock) perm_coop_kernel(
     for (uint32_t it = 1;; ++it) {
       unsigned int v;
       asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(bar) : "memory");
-      if (v >= (unsigned int)nblk) break;
-      if ((it & 63) == 0 && perm_now_ns() - t0 > kPermWaitNs) {
+      if (v >= (unsigned int)nblk + wait.phantom) break;
+      if ((it & 63) == 0 && perm_now_ns() - t0 > wait.limit_ns) {
         atomicExch(&status->code, (int)MOE_ERR_TIMEOUT);
         atomicExch(&status->where, 90);
         ab = 1;
@@ -416,7 +416,8 @@ static bool coop_fits(int nblk, size_t smem) {
 }
 
 cudaError_t launch_permute(const LayerArgs& a, const int32_t* eidx, const PermOut& o, int32_t* cnt,
-                           int32_t* off, int nblk, DevStatus* status, bool bar_zeroed, cudaStream_t st) {
+                           int32_t* off, int nblk, DevStatus* status, bool bar_zeroed, cudaStream_t st,
+                           PermWait wait) {
   if (a.T == 0) {
     // empty batch: offsets are all zero
     cudaError_t e = cudaSuccess;
@@ -429,13 +430,11 @@ cudaError_t launch_permute(const LayerArgs& a, const int32_t* eidx, const PermOu
   if (a.T <= kFusedMaxT && a.E + a.G <= kFusedMaxKeys) {
     const int threads = (a.T + 31) / 32 * 32;
     const size_t smem = (size_t)(2 + 2 * (threads / 32)) * (a.E + a.G) * sizeof(int);
-    static bool attr = false;
-    if (!attr) {
-      const cudaError_t e = cudaFuncSetAttribute(perm_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)((2 + 2 * (kFusedThreads / 32)) * kFusedMaxKeys * sizeof(int)));
-      if (e != cudaSuccess) return e;
-      attr = true;
-    }
+    static std::atomic<uint64_t> attr{0};
+    if (const cudaError_t e = smem_attr_once(perm_fused_kernel,
+                                             (2 + 2 * (kFusedThreads / 32)) * kFusedMaxKeys * sizeof(int), attr);
+        e != cudaSuccess)
+      return e;
     launch_pdl(perm_fused_kernel, dim3(1), dim3(threads), smem, st, eidx, a.tab, a.T, a.kg, a.ke, o.perm,
                o.inv_pos, o.ebeg,
                                                    o.ecnt, o.gbeg, o.row_asg, o.row_of, o.rbeg);
@@ -458,7 +457,7 @@ cudaError_t launch_permute(const LayerArgs& a, const int32_t* eidx, const PermOu
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, perm_coop_kernel, eidx, a.tab, a.T, a.kg, a.ke, cnt, status, o.perm,
+    cudaError_t e = cudaLaunchKernelEx(&cfg, perm_coop_kernel, eidx, a.tab, a.T, a.kg, a.ke, cnt, status, wait, o.perm,
                                        o.inv_pos, o.ebeg, o.ecnt, o.gbeg, o.row_asg, o.row_of, o.rbeg);
     prof_mark("perm_coop", st);
     return e;

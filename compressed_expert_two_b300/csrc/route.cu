@@ -543,13 +543,8 @@ static cudaError_t launch_smem_logits(const LayerArgs& a, const void* x, const v
   const int Tn = a.T, d = a.d, G = a.G, E = a.E;
   dim3 grid((Tn + kRtTok - 1) / kRtTok, (G + E + rows - 1) / rows);
   constexpr size_t smem = sizeof(__nv_bfloat16) * kRtStages * (kRtTok + rows) * kRtDC;
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t e = cudaFuncSetAttribute(router_logits_smem_kernel<RG, L>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  if (const cudaError_t e = smem_attr_once(router_logits_smem_kernel<RG, L>, smem, attr); e != cudaSuccess) return e;
   return launch_pdl(router_logits_smem_kernel<RG, L>, grid, dim3(128 * RG), smem, st, (const __nv_bfloat16*)x,
                     (const __nv_bfloat16*)wg, bg, (const __nv_bfloat16*)we, logits, Tn, d, G, E, a.tab, a.kg, a.ke,
                     gidx, eidx, gate);

@@ -40,6 +40,7 @@ struct RtcArgs {
   float* gate;
   int32_t* redo;        // tokens left to the canonical kernels
   DevStatus* status;    // status->route_redo counts them
+  float* dbg;           // null, or [T][2 (G + E)]: each token's logits (groups, then experts) and deltas
 };
 
 // Sum of squares of one 64-element row of a 128-byte-swizzled tile, into two pairs of partial
@@ -255,6 +256,11 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(
           if (p.bg) lv[g] = __fadd_rn(lv[g], p.bg[g]);
         const float xs = p.c_err * sqrtf(xn);
         auto delta = [&](int col) { return xs * s_wn[col] + 0x1p-22f * fabsf(lv[col]); };
+        if (p.dbg) {
+          float* o = p.dbg + (size_t)t * 2 * (G + E);
+          for (int g = 0; g < G; ++g) { o[g] = lv[g]; o[G + E + g] = delta(g); }
+          for (int e = 0; e < E; ++e) { o[G + e] = lv[Gp + e]; o[2 * G + E + e] = delta(Gp + e); }
+        }
         const int K = tab.K, kg = p.kg, ke = p.ke, k = kg * ke;
         if (G <= 8 && K <= 8) {
           // register path
@@ -379,7 +385,7 @@ bool route_tc_ok(const LayerArgs& a) {
 
 cudaError_t launch_route_tc(const LayerArgs& a, const void* x, const void* wg, const float* bg, const void* we,
                             int32_t* gidx, int32_t* eidx, float* gate, int32_t* redo, DevStatus* status,
-                            cudaStream_t st) {
+                            cudaStream_t st, float* dbg) {
   CUtensorMap mX, mWg, mWe;
   if (!make_map_bf16(&mX, x, (uint64_t)a.T, a.d, kRtcTile) || !make_map_bf16(&mWg, wg, a.G, a.d, a.G) ||
       !make_map_bf16(&mWe, we, a.E, a.d, a.E))
@@ -387,19 +393,15 @@ cudaError_t launch_route_tc(const LayerArgs& a, const void* x, const void* wg, c
   RtcArgs p;
   p.bg = bg; p.T = a.T; p.nk = a.d / 64; p.N = route_tc_columns(a); p.Gp = (a.G + 7) / 8 * 8;
   p.c_err = route_tc_c_err(a.d); p.kg = a.kg; p.ke = a.ke;
-  p.gidx = gidx; p.eidx = eidx; p.gate = gate; p.redo = redo; p.status = status;
+  p.gidx = gidx; p.eidx = eidx; p.gate = gate; p.redo = redo; p.status = status; p.dbg = dbg;
   const size_t stage = (size_t)(kRtcTile + p.N) * 128;
   p.stages = (int)((kRtcSmem - 1024) / stage);
   if (p.stages > kRtcMaxStages) p.stages = kRtcMaxStages;
   const size_t smem = 1024 + (size_t)p.stages * stage;
   // the logits of the epilogue (128 rows of N + 1 floats) reuse the stages
   if ((size_t)kRtcTile * (kRtcMaxN + 1) * 4 > (size_t)p.stages * stage) return cudaErrorInvalidValue;
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t e = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtcSmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  if (const cudaError_t e = smem_attr_once(router_tc_kernel, kRtcSmem, attr); e != cudaSuccess) return e;
   const cudaError_t e = launch_pdl(router_tc_kernel, dim3((a.T + kRtcTile - 1) / kRtcTile), dim3(192), smem, st,
                                    mX, mWg, mWe, a.tab, p);
   prof_mark("router_tc", st);

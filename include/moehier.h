@@ -172,6 +172,32 @@ const char* moe_hier_last_cuda_error(void);
 int moe_hier_profile_begin(void* const* events, int n_events);
 int moe_hier_profile_end(const char** names, int max_names);
 
+/* Test aids.  The pages have no counterpart; neither changes a result of the calls above.
+ *
+ * moe_hier_debug_set_wait sets, for the calling process, the limit of the grid-wide wait inside
+ * the single-launch form of moe_hier_permute (batches of more than 1024 tokens; default 2 s;
+ * wait_ns = 0 keeps the default) and a number of arrivals that the wait expects beyond the
+ * launch's own blocks (default 0).  With phantom_arrivals > 0 the wait cannot complete: every
+ * block gives up after the limit, writes MOE_ERR_TIMEOUT to the workspace status word (read it
+ * with moe_hier_get_status) and returns without placing its items, so that call's outputs are
+ * unspecified and the stream stays usable.  This drives the failure path of a bounded device
+ * wait without faulting or hanging the GPU.  Only moe_hier_permute reads the setting
+ * (moe_hier_forward always runs with the defaults); moe_hier_debug_set_wait(0, 0) restores them.
+ * MOE_ERR_INVALID if phantom_arrivals < 0. */
+int moe_hier_debug_set_wait(uint64_t wait_ns, int phantom_arrivals);
+
+/* Runs the tensor-core router alone (BF16 layers with T >= 1024, at most 128 router columns
+ * after padding the group rows to 8, k_g and k_e <= 8; MOE_ERR_UNSUPPORTED otherwise) and writes,
+ * for every token t, out[t][0 .. G+E) = its FP32 tensor-core logits (group logits with the bias,
+ * then expert logits) and out[t][G+E .. 2(G+E)) = the half-widths delta of the intervals the
+ * router verified its decision with, for the same candidates.  out: device, [T][2(G+E)] FP32.
+ * The routing results go to the workspace.  With it a test checks the router's bound
+ * |s_tc - s_canonical| <= delta element by element ("router in FP32", routing-mechanisms page
+ * section 3.1, is what makes the canonical logits the reference). */
+int moe_hier_debug_route_tc(const moe_hier_desc* desc, const void* x, const void* w_group,
+                            const float* b_group, const void* w_expert, const int32_t* group_map_host,
+                            float* out, void* ws, size_t ws_bytes, void* stream);
+
 /* moe_hier_permute for callers that cannot supply a workspace: a host that owns all device
  * memory through its own pool and allows no other allocation, or a latency-critical loop that
  * may not pay an allocation's implicit device synchronisation.  The paper has no counterpart;
@@ -181,8 +207,9 @@ int moe_hier_profile_end(const char** names, int max_names);
  * process exits; a layer needs 2 * ceil(T/256) * (E + G) of them, and larger layers are rejected
  * with MOE_ERR_WORKSPACE before anything is enqueued (batches of at most 1024 tokens are
  * permuted by a single-CTA kernel that uses no scratch).  The call allocates nothing.  The first
- * call on a device looks up the array's device address (with that device current); make that
- * first call before any stream capture.  All calls share the one array and each kernel
+ * call on a device looks up the array's device address (with that device current) and keeps it
+ * for the life of the process; make that first call before any stream capture, and do not call
+ * cudaDeviceReset on a device between calls (a reset would leave the kept address stale).  All calls share the one array and each kernel
  * overwrites every entry it later reads, so nothing needs clearing between calls, but calls
  * whose work overlaps on the GPU (other streams, other host threads) race on it. */
 int moe_hier_permute_noalloc(const moe_hier_desc* desc, const int32_t* group_map_host,

@@ -89,3 +89,14 @@ def test_product_path_does_not_import_oracle():
             "sorted(m for m in sys.modules if m.startswith('oracle'))" % ROOT)
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_test_aids_validate_on_the_host(L):
+    assert L.lib.moe_hier_debug_set_wait(0, -1) == L.MOE_ERR_INVALID
+    import numpy as np
+    d = desc_for(L)                                  # an FP32 layer: no tensor-core router
+    gm = np.array([0, 0, 0, 0, 1, 1, 1, 1], dtype=np.int32)
+    fake = 1 << 20
+    rc = L.lib.moe_hier_debug_route_tc(ctypes.byref(d), fake, fake, None, fake, gm.ctypes.data, fake, fake,
+                                       1 << 30, None)
+    assert rc == L.MOE_ERR_UNSUPPORTED

@@ -165,6 +165,31 @@ def test_gates_sum_to_one_and_group_gate_one():
             assert np.all(gm[es] == r["gidx"][t, j]) and len(set(es)) == cfg.ke
 
 
+def test_two_groups_two_experts_hand_computed_gates():
+    """k_g = 2, k_e = 2 on one token whose logits are small integers (x is one-hot, so every
+    canonical logit is a router row's first entry, exactly).  Groups (G = 3, K = 3, contiguous):
+    logits 2, 0, 1 -> groups 0 then 2, p = (e/(e+1), 1/(e+1)).  Group 0's experts 0, 1, 2 have
+    logits 0, 3, 1 -> experts 1 then 2, q = (e^2/(e^2+1), 1/(e^2+1)).  Group 2's experts 6, 7, 8
+    have logits -1, -1, 2 -> expert 8, then the tie between 6 and 7 goes to 6,
+    q = (e^3/(e^3+1), 1/(e^3+1)).  gate = p_g q_e in slot order (group rank, then expert rank)."""
+    d = 128
+    x = np.zeros((1, d), dtype=np.float32)
+    x[0, 0] = 1.0
+    wg = np.zeros((3, d), dtype=np.float32)
+    wg[:, 0] = [2, 0, 1]
+    we = np.zeros((9, d), dtype=np.float32)
+    we[:, 0] = [0, 3, 1, 5, 5, 5, -1, -1, 2]
+    gm = np.repeat(np.arange(3), 3)
+    r = oracle.route(x, wg, None, we, gm, 2, 2)
+    e = math.e
+    p0, p1 = e / (e + 1), 1 / (e + 1)
+    assert r["gidx"].tolist() == [[0, 2]]
+    assert r["eidx"].tolist() == [[1, 2, 8, 6]]
+    want = [p0 * e ** 2 / (e ** 2 + 1), p0 / (e ** 2 + 1), p1 * e ** 3 / (e ** 3 + 1), p1 / (e ** 3 + 1)]
+    assert np.allclose(r["gate"][0], want, rtol=0, atol=1e-15)
+    assert abs(r["gate"][0].sum() - 1.0) < 1e-15
+
+
 def test_route_matches_torch_topk_when_one_group():
     """G = 1: level 1 is trivial and level 2 is a plain top-k over all experts, softmax over the
     selected logits (library topk/softmax)."""

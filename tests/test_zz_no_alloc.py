@@ -4,9 +4,11 @@ Some hosts own all device memory through their own pool and forbid any other all
 some latency-critical loops may not pay an allocation's implicit synchronisation; neither can
 hand the library a workspace.  moe_hier_permute_noalloc serves them from a fixed scratch array
 inside the library.  These tests call it through the C ABI and check that it returns exactly
-what moe_hier_permute returns, on two calls in a row with different layers (the second call
-reuses the array the first one left behind).  Both layers have more than 4096 tokens: smaller
-batches are permuted by a single-CTA kernel that needs no histogram scratch at all.
+what moe_hier_permute returns and what the oracle's permutation returns, on calls in a row with
+different layers (each call reuses the array the one before left behind).  Batches of at most
+1024 tokens are permuted by a single-CTA kernel that needs no histogram scratch; larger ones use
+the array.  The cases cover both sides of that limit (1024 and 1025 tokens) and the largest layer
+the array accepts, 2 * ceil(T/256) * (E + G) = 65,536 entries exactly.
 """
 import ctypes
 
@@ -14,6 +16,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from synth import MoEConfig, make_inputs
 
 KEYS = ("perm", "inv_pos", "expert_begin", "expert_count", "group_begin", "row_asg", "row_of", "row_begin")
@@ -54,15 +57,22 @@ def noalloc_permute(L, layer, eidx):
 def test_noalloc_permute_matches_workspace_permute_twice(L, cuda_ok):
     from compressed_expert_two_b300.layer import DeviceLayer
     cases = [layer_case(), layer_case(T=8000, d=384, E=64, G=8, kg=2, ke=3, group_map="contiguous", seed=42,
-                                      zipf_s=1.2)]
+                                      zipf_s=1.2),
+             layer_case(T=1024, seed=43),                 # single-CTA kernel, no scratch
+             layer_case(T=1025, seed=44),                 # smallest batch that uses the array
+             # the largest layer the array holds: 2 * 256 blocks * (120 + 8) keys = 65,536 entries
+             layer_case(T=65536, d=128, f=64, E=120, G=8, kg=1, ke=2, group_map="contiguous", seed=45)]
     for cfg in cases:
-        layer = DeviceLayer(make_inputs(cfg), device="cuda")
+        inp = make_inputs(cfg)
+        layer = DeviceLayer(inp, device="cuda")
         eidx = layer.route()["eidx"]
         want = layer.permute(eidx)
         got = noalloc_permute(L, layer, eidx)
         torch.cuda.synchronize()
+        ref = oracle.permute(eidx.cpu().numpy(), inp["group_map"].numpy(), cfg.G, cfg.ke)
         for k in KEYS:
             assert torch.equal(got[k], want[k]), (cfg.name, cfg.T, k)
+            assert np.array_equal(got[k].cpu().numpy(), ref[k]), (cfg.name, cfg.T, k)
 
 
 def test_noalloc_rejects_layers_beyond_its_scratch(L):
