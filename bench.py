@@ -250,7 +250,7 @@ def oracle_tokens_per_s(inp, seconds: float, chunk: int):
     start = 0
     while True:
         toks = np.arange(start, min(start + chunk, cfg.T))
-        routing = oracle.route(x[toks], wgp, bgp, wep, gm, cfg.kg, cfg.ke)
+        routing = oracle.route(x[toks], wgp, bgp, wep, gm, cfg.kg, cfg.ke, cfg.route)
         sub = dict(inp)
         sub["x"] = inp["x"][toks[0]:toks[-1] + 1]
         sub["cfg"] = cfg.replace(T=len(toks))

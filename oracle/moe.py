@@ -84,13 +84,21 @@ def _topk_desc(vals: np.ndarray, ids: np.ndarray, k: int) -> np.ndarray:
     return np.array([ids[i] for i in order[:k]], dtype=np.int64)
 
 
-def route(x, w_group, b_group, w_expert, group_map, kg: int, ke: int) -> Dict[str, np.ndarray]:
+def route(x, w_group, b_group, w_expert, group_map, kg: int, ke: int, mode: str = "within") -> Dict[str, np.ndarray]:
     """Two-level routing [T key design 3] with top-k-then-softmax gates [W ch. 1].
 
     Level 1: group logits s_g (+ b_g); the kg best groups.  Level 2: inside each chosen group g,
     the ke best experts among {e : group_map[e] == g} by expert logit.
     Slots: group rank major, then expert rank; gate[t, slot] = p_g * q_e.
     Returns gidx [T,kg] int32, eidx [T,kg*ke] int32, gate [T,kg*ke] float64, and the FP32 logits.
+
+    mode "across" is the other reading of the fine-grained workload's "top-3 experts across the
+    chosen groups": the ke best experts over the union of the chosen groups' members (by expert
+    logit, ties to the lower id), gates = softmax over those ke logits ([W ch. 1]: top-k, then
+    softmax), the group gates p unused.  The slot layout stays the within-group one -- each chosen
+    group's ke best members, which contain every member of the union's top ke -- and the slots
+    that the union's top ke does not pick get gate 0 (so they add nothing to y).  ``active``
+    [T, kg*ke] marks the picked slots.
     """
     group_map = np.asarray(group_map, dtype=np.int64)
     sg = canonical_logits(x, w_group, b_group)
@@ -111,7 +119,21 @@ def route(x, w_group, b_group, w_expert, group_map, kg: int, ke: int) -> Dict[st
             q = _softmax64(se[t, es])
             eidx[t, j * ke:(j + 1) * ke] = es
             gate[t, j * ke:(j + 1) * ke] = p[j] * q
-    return {"gidx": gidx, "eidx": eidx, "gate": gate, "group_logits": sg, "expert_logits": se}
+    active = np.ones((T, kg * ke), dtype=bool)
+    if mode == "across":
+        for t in range(T):
+            union = np.concatenate([members[g] for g in gidx[t]])
+            top = _topk_desc(se[t, union], union, ke)
+            q = _softmax64(se[t, top])
+            gate[t] = 0.0
+            active[t] = False
+            for i, e in enumerate(top):
+                slot = int(np.nonzero(eidx[t] == e)[0][0])
+                gate[t, slot] = q[i]
+                active[t, slot] = True
+    elif mode != "within":
+        raise ValueError(mode)
+    return {"gidx": gidx, "eidx": eidx, "gate": gate, "active": active, "group_logits": sg, "expert_logits": se}
 
 
 # --------------------------------------------------------------------------------------------
@@ -225,7 +247,7 @@ def forward_tokens(inp: dict, tokens: Optional[Sequence[int]] = None, routing: O
     x = _np(inp["x"]).astype(np.float32)
     if routing is None:
         routing = route(x, _np(inp["w_group"]), _np(inp["b_group"]), _np(inp["w_expert"]),
-                         _np(inp["group_map"]), cfg.kg, cfg.ke)
+                         _np(inp["group_map"]), cfg.kg, cfg.ke, getattr(cfg, "route", "within"))
     toks = np.arange(cfg.T) if tokens is None else np.asarray(tokens, dtype=np.int64)
     eidx = routing["eidx"][toks]
     gate = routing["gate"][toks]

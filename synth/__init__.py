@@ -56,6 +56,7 @@ class MoEConfig:
     zipf_s: Optional[float] = None   # group-router bias so group load follows Zipf(s)
     resid_std: float = 0.02
     base_scale: float = 1.0          # 0.0 gives the base-zero (pure low-rank) variant
+    route: str = "within"            # "within": top-ke in each chosen group; "across": top-ke over their union
 
     @property
     def K(self) -> int:
@@ -84,6 +85,8 @@ CONFIGS: Dict[str, MoEConfig] = {
                         dtype="bf16", resid="int4", group_map="contiguous", seed=4),
 }
 CONFIG_ORDER = ["tiny_f32", "small_bf16_int4", "mixtral_prefill", "finegrained_skewed", "decode"]
+# The other reading of the fine-grained workload: top-3 experts over the union of the 2 chosen groups.
+CONFIGS["finegrained_across"] = CONFIGS["finegrained_skewed"].replace(name="finegrained_across", route="across")
 
 
 def _torch_dtype(cfg: MoEConfig) -> torch.dtype:

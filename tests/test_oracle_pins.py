@@ -190,6 +190,81 @@ def test_two_groups_two_experts_hand_computed_gates():
     assert abs(r["gate"][0].sum() - 1.0) < 1e-15
 
 
+def test_across_groups_hand_computed_gates():
+    """The token of the test above in the across-groups reading: groups 0 and 2 are chosen; the
+    union of their members {0, 1, 2, 6, 7, 8} has logits 0, 3, 1, -1, -1, 2.  Top-2: experts 1 and
+    8, gates softmax(3, 2) = (e/(e+1), 1/(e+1)); the within-group slots [1, 2, 8, 6] stay, with
+    expert 2's and 6's gates 0.  Top-3: experts 1, 8, 2 with softmax(3, 2, 1); the slots are each
+    group's top 3, [1, 2, 0, 8, 6, 7] (6 before 7: equal logits, lower id first)."""
+    d = 128
+    x = np.zeros((1, d), dtype=np.float32)
+    x[0, 0] = 1.0
+    wg = np.zeros((3, d), dtype=np.float32)
+    wg[:, 0] = [2, 0, 1]
+    we = np.zeros((9, d), dtype=np.float32)
+    we[:, 0] = [0, 3, 1, 5, 5, 5, -1, -1, 2]
+    gm = np.repeat(np.arange(3), 3)
+    e = math.e
+    r = oracle.route(x, wg, None, we, gm, 2, 2, "across")
+    assert r["gidx"].tolist() == [[0, 2]] and r["eidx"].tolist() == [[1, 2, 8, 6]]
+    assert np.allclose(r["gate"][0], [e / (e + 1), 0, 1 / (e + 1), 0], rtol=0, atol=1e-15)
+    assert r["active"].tolist() == [[True, False, True, False]]
+    r = oracle.route(x, wg, None, we, gm, 2, 3, "across")
+    assert r["eidx"].tolist() == [[1, 2, 0, 8, 6, 7]]
+    z = e * e + e + 1
+    assert np.allclose(r["gate"][0], [e * e / z, 1 / z, 0, e / z, 0, 0], rtol=0, atol=1e-15)
+
+
+def test_across_groups_brute_force_and_special_cases():
+    """Brute force over every ke-subset of the union of the chosen groups' members (T = 8):
+    the picked experts are the unique subset whose members all beat every other member of the
+    union in (logit desc, id asc) order, and their gates are the softmax of their logits.  With
+    k_g = 1 the union is one group and the reading equals the within-group one; with k_g = G it is
+    a plain top-k over all experts (torch.topk / softmax)."""
+    cfg = tiny_cfg(T=8, E=12, G=3, kg=2, ke=2)
+    inp = make_inputs(cfg)
+    x, wg, we = (oracle.moe._np(inp[k]) for k in ("x", "w_group", "w_expert"))
+    gm = inp["group_map"].numpy()
+    r = oracle.route(x, wg, None, we, gm, 2, 2, "across")
+    se = r["expert_logits"]
+    for t in range(cfg.T):
+        union = [int(e) for g in r["gidx"][t] for e in np.nonzero(gm == g)[0]]
+        before = lambda a, b: se[t, a] > se[t, b] or (se[t, a] == se[t, b] and a < b)
+        winners = [set(S) for S in itertools.combinations(union, 2)
+                   if all(before(a, b) for a in S for b in union if b not in S)]
+        assert len(winners) == 1
+        picked = {int(e) for e, on in zip(r["eidx"][t], r["active"][t]) if on}
+        assert picked == winners[0]
+        lg = np.array([se[t, e] for e in sorted(picked)], dtype=np.float64)
+        want = dict(zip(sorted(picked), np.exp(lg - lg.max()) / np.exp(lg - lg.max()).sum()))
+        for e, g, on in zip(r["eidx"][t], r["gate"][t], r["active"][t]):
+            assert (g == 0.0) != on and (not on or abs(g - want[int(e)]) < 1e-15)
+    within = oracle.route(x, wg, None, we, gm, 1, 3)
+    across = oracle.route(x, wg, None, we, gm, 1, 3, "across")
+    assert np.array_equal(within["eidx"], across["eidx"]) and np.allclose(within["gate"], across["gate"], atol=1e-15)
+    r = oracle.route(x, wg, None, we, gm, 3, 2, "across")
+    vals, idx = torch.topk(torch.from_numpy(se).double(), 2, dim=-1)
+    for t in range(cfg.T):
+        picked = [int(e) for e, on in zip(r["eidx"][t], r["active"][t]) if on]
+        assert sorted(picked) == sorted(idx[t].tolist())
+        gates = {int(e): g for e, g in zip(r["eidx"][t], r["gate"][t]) if g > 0}
+        sm = torch.softmax(vals[t], -1).numpy()
+        assert all(abs(gates[int(e)] - p) < 1e-15 for e, p in zip(idx[t].tolist(), sm))
+
+
+def test_across_groups_output_brute_force():
+    """y of the across reading equals the gated sum over the picked experts only, each computed
+    independently in factored form."""
+    cfg = tiny_cfg(T=6, E=12, G=3, kg=2, ke=2, route="across", resid_std=0.2)
+    inp = make_inputs(cfg)
+    y, r = oracle.forward_tokens(inp)
+    for t in range(cfg.T):
+        xt = inp["x"][t].double().numpy()
+        want = sum(g * _expert_ffn_factored(inp, int(e), xt)
+                   for e, g, on in zip(r["eidx"][t], r["gate"][t], r["active"][t]) if on)
+        assert np.allclose(y[t], want, rtol=1e-10, atol=1e-12)
+
+
 def test_route_matches_torch_topk_when_one_group():
     """G = 1: level 1 is trivial and level 2 is a plain top-k over all experts, softmax over the
     selected logits (library topk/softmax)."""
