@@ -80,7 +80,8 @@ def recorded_traffic(config: str, kernel: str):
 
 def workload_name(cfg) -> str:
     return (f"{cfg.name}: T={cfg.T} d_model={cfg.d} d_ff={cfg.f} E={cfg.E} G={cfg.G} "
-            f"top{cfg.kg} group(s) then top{cfg.ke} in group, r={cfg.r} {cfg.resid} residual, "
+            f"top{cfg.kg} group(s) then top{cfg.ke} "
+            f"{'over their union' if cfg.route == 'across' else 'in group'}, r={cfg.r} {cfg.resid} residual, "
             f"{cfg.dtype} base, SwiGLU")
 
 
@@ -263,7 +264,7 @@ def oracle_tokens_per_s(inp, seconds: float, chunk: int):
 
 
 CPU_CHUNK = {"tiny_f32": 256, "small_bf16_int4": 1024, "mixtral_prefill": 16,
-             "finegrained_skewed": 512, "decode": 4}
+             "finegrained_skewed": 512, "finegrained_across": 512, "decode": 4}
 
 
 def cpu_cores() -> int:
@@ -328,7 +329,8 @@ def run_ours(args, rank, world, local_rank):
     eidx = out["eidx"].cpu()
     experts_hit = int(torch.unique(eidx).numel())
     groups_hit = int(torch.unique(out["gidx"].cpu()).numel())
-    load = workload.load_stats(out["gidx"].cpu().numpy(), eidx.numpy(), cfg.G, cfg.E)
+    load = workload.load_stats(out["gidx"].cpu().numpy(), eidx.numpy(), cfg.G, cfg.E,
+                               active=(out["gate"] > 0).cpu().numpy())
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 

@@ -17,13 +17,15 @@ MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, M
     0, -1, -2, -3, -4, -5
 MOE_F32, MOE_BF16 = 0, 1
 MOE_RESID_F32, MOE_RESID_INT4_G64 = 0, 1
+MOE_ROUTE_WITHIN, MOE_ROUTE_ACROSS = 0, 1
 
 
 class MoeHierDesc(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("G", ctypes.c_int32), ("topk_group", ctypes.c_int32),
                 ("topk_expert", ctypes.c_int32), ("rank", ctypes.c_int32),
-                ("act_dtype", ctypes.c_int32), ("resid_fmt", ctypes.c_int32)]
+                ("act_dtype", ctypes.c_int32), ("resid_fmt", ctypes.c_int32),
+                ("route_mode", ctypes.c_int32)]
 
 
 class MoeHierResid(ctypes.Structure):

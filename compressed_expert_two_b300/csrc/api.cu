@@ -96,12 +96,14 @@ static int validate(const moe_hier_desc* desc, const int32_t* group_map, LayerAr
   if (D.act_dtype != MOE_F32 && D.act_dtype != MOE_BF16) return MOE_ERR_INVALID;
   if (D.resid_fmt != MOE_RESID_F32 && D.resid_fmt != MOE_RESID_INT4_G64) return MOE_ERR_INVALID;
   if ((D.act_dtype == MOE_BF16) != (D.resid_fmt == MOE_RESID_INT4_G64)) return MOE_ERR_UNSUPPORTED;
+  if (D.route_mode != MOE_ROUTE_WITHIN && D.route_mode != MOE_ROUTE_ACROSS) return MOE_ERR_INVALID;
   memset(a, 0, sizeof(*a));
   a->T = D.T; a->d = D.d_model; a->f = D.d_ff; a->E = D.E; a->G = D.G; a->K = K;
   a->kg = D.topk_group; a->ke = D.topk_expert; a->k = a->kg * a->ke; a->r = D.rank;
   a->bf16 = D.act_dtype == MOE_BF16;
   a->int4 = D.resid_fmt == MOE_RESID_INT4_G64;
   a->R = a->T * a->kg;
+  a->across = D.route_mode == MOE_ROUTE_ACROSS;
   a->tab.E = D.E; a->tab.G = D.G; a->tab.K = K;
   if (group_map) {
     int fill[kMaxE];
@@ -369,7 +371,7 @@ int moe_hier_debug_route_tc(const moe_hier_desc* desc, const void* x, const void
   if (!group_map_host) return MOE_ERR_INVALID;
   int st = validate(desc, group_map_host, &a);
   if (st != MOE_OK) return st;
-  if (!route_tc_ok(a)) return MOE_ERR_UNSUPPORTED;
+  if (!route_tc_ok(a) || a.across) return MOE_ERR_UNSUPPORTED;
   if (!x || !w_group || !w_expert || !out) return MOE_ERR_INVALID;
   if (!aligned16(x) || !aligned16(w_group) || !aligned16(w_expert)) return MOE_ERR_INVALID;
   const Plan p = make_plan(a);

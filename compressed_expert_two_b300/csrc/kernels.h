@@ -14,6 +14,7 @@ struct LayerArgs {
   bool bf16;        // act dtype BF16 (else FP32)
   bool int4;        // residual INT4 group-64 (else FP32)
   int R;            // rows = T * kg
+  bool across;      // MOE_ROUTE_ACROSS: top k_e over the union of the chosen groups
   GroupTable tab;
 };
 

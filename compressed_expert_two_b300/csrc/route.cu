@@ -434,6 +434,59 @@ static void launch_select_any(const LayerArgs& a, const float* logits, const int
   else launch_select<32>(a, logits, list, list_n, gidx, eidx, gate, st);
 }
 
+// The across-groups reading of level 2: among a token's k = k_g k_e candidate slots (each chosen
+// group's top-k_e members, which hold every member of the union's top k_e), the k_e best by
+// canonical expert logit (ties to the lower id) get gate = softmax over their logits (in pick
+// order, as the within-group gates), every other slot gate 0.  One thread per token.
+__global__ void __launch_bounds__(256) router_across_kernel(const float* __restrict__ logits, int Tn, int G, int E,
+                                                            int k, int ke, const int32_t* __restrict__ eidx,
+                                                            float* __restrict__ gate) {
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= Tn) return;
+  const float* se = logits + (size_t)t * (G + E) + G;
+  int id[kMaxK];
+  float v[kMaxK], q[kMaxK];
+  int slot[kMaxK];
+#pragma unroll
+  for (int s = 0; s < kMaxK; ++s) {
+    id[s] = s < k ? eidx[(size_t)t * k + s] : 0;
+    v[s] = s < k ? se[id[s]] : 0.f;
+    slot[s] = 0;
+  }
+  uint32_t picked = 0;
+  float den = 0.f, v0 = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    if (j >= ke) break;
+    int bi = -1;
+#pragma unroll
+    for (int s = 0; s < kMaxK; ++s) {
+      const bool cand = s < k && !((picked >> s) & 1u);
+      if (cand && (bi < 0 || v[s] > v[bi] || (v[s] == v[bi] && id[s] < id[bi]))) bi = s;
+    }
+    picked |= 1u << bi;
+    slot[j] = bi;
+    if (j == 0) v0 = v[bi];
+    q[j] = expf(v[bi] - v0);
+    den += q[j];
+  }
+  float g[kMaxK];
+#pragma unroll
+  for (int s = 0; s < kMaxK; ++s) g[s] = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j)
+    if (j < ke) {
+#pragma unroll
+      for (int s = 0; s < kMaxK; ++s)
+        if (s == slot[j]) g[s] = q[j] / den;
+    }
+#pragma unroll
+  for (int s = 0; s < kMaxK; ++s)
+    if (s < k) gate[(size_t)t * k + s] = g[s];
+}
+
 // Canonical-order BF16 logits of the listed tokens (the ones the tensor-core router could not
 // verify), grid-stride; logits row p belongs to token list[p].  Lane l adds the products of its
 // elements 128 j + 4 l + u in ascending index, then the xor butterfly 16, 8, 4, 2, 1 (as a
@@ -595,6 +648,17 @@ cudaError_t launch_route(const LayerArgs& a, const void* x, const void* wg, cons
                          float* gate, DevStatus* status, bool status_zeroed, cudaStream_t st) {
   if (a.T == 0) return cudaSuccess;
   cudaError_t err = cudaSuccess;
+  if (a.across) {
+    // canonical logits of every token stay in the workspace: the within-group selection gives the
+    // candidate slots, then the picks over their union set the gates
+    if ((err = launch_logits(a, a.bf16, x, wg, bg, we, logits, a.T, a.d, a.G, a.E, st)) != cudaSuccess) return err;
+    launch_select_any(a, logits, nullptr, nullptr, gidx, eidx, gate, st);
+    prof_mark("router_select", st);
+    launch_pdl(router_across_kernel, dim3((a.T + 255) / 256), dim3(256), 0, st, (const float*)logits, a.T, a.G, a.E,
+               a.k, a.ke, (const int32_t*)eidx, gate);
+    prof_mark("router_across", st);
+    return cudaGetLastError();
+  }
   if (!fused_route_ok(a) && route_tc_ok(a)) {
     // tensor-core logits with verification, then the canonical order for the unverified tokens
     if (!status_zeroed && (err = cudaMemsetAsync(&status->route_redo, 0, sizeof(int), st)) != cudaSuccess)

@@ -15,7 +15,9 @@ def make_desc(cfg, T: Optional[int] = None) -> L.MoeHierDesc:
     return L.MoeHierDesc(T=cfg.T if T is None else T, d_model=cfg.d, d_ff=cfg.f, E=cfg.E, G=cfg.G,
                          topk_group=cfg.kg, topk_expert=cfg.ke, rank=cfg.r,
                          act_dtype=L.MOE_BF16 if cfg.dtype == "bf16" else L.MOE_F32,
-                         resid_fmt=L.MOE_RESID_INT4_G64 if cfg.resid == "int4" else L.MOE_RESID_F32)
+                         resid_fmt=L.MOE_RESID_INT4_G64 if cfg.resid == "int4" else L.MOE_RESID_F32,
+                         route_mode=L.MOE_ROUTE_ACROSS if getattr(cfg, "route", "within") == "across"
+                         else L.MOE_ROUTE_WITHIN)
 
 
 class DeviceLayer:

@@ -67,14 +67,18 @@ def kernel_work(cfg, kernel: str, groups_hit: int, experts_hit: int, T=None):
     return flops(cfg, T), bytes_moved(cfg, groups_hit, experts_hit, T)
 
 
-def load_stats(gidx, eidx, G: int, E: int) -> dict:
+def load_stats(gidx, eidx, G: int, E: int, active=None) -> dict:
     """Load balance of one batch's routing (the imbalance the clustering is meant to bound; the
     pages report load variance and the max/mean ratio): rows per group (one per token and chosen
     group) and assignments per expert, from the router's gidx [T][k_g] and eidx [T][k] (integer
-    arrays or tensors).  max/mean is 1 for a perfectly even batch; cv = std/mean of the loads."""
+    arrays or tensors); with ``active`` [T][k] (the across-groups reading's picked slots) only
+    those assignments count.  max/mean is 1 for a perfectly even batch; cv = std/mean."""
     import numpy as np
     g = np.bincount(np.asarray(gidx).reshape(-1), minlength=G).astype(np.float64)
-    e = np.bincount(np.asarray(eidx).reshape(-1), minlength=E).astype(np.float64)
+    ev = np.asarray(eidx).reshape(-1)
+    if active is not None:
+        ev = ev[np.asarray(active).reshape(-1).astype(bool)]
+    e = np.bincount(ev, minlength=E).astype(np.float64)
 
     def summary(c):
         m = c.mean()

@@ -78,6 +78,15 @@ typedef enum {
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 typedef enum { MOE_RESID_F32 = 0, MOE_RESID_INT4_G64 = 1 } moe_resid_fmt;
+/* Level-2 routing ("Breaking the MoE LLM Trilemma", key design 3).
+ *   MOE_ROUTE_WITHIN: the top-k_e experts inside each chosen group (k_g k_e active experts),
+ *     gate = p_g q_e (softmax over the chosen group logits times the softmax over the group's
+ *     chosen expert logits).
+ *   MOE_ROUTE_ACROSS: the top-k_e experts over the union of the chosen groups' members (k_e active
+ *     experts), gate = softmax over their logits.  The slot layout stays the within-group one --
+ *     eidx holds each chosen group's top-k_e members, which contain every expert the union's
+ *     top-k_e picks -- and the slots it does not pick get gate 0, so they add nothing to y. */
+typedef enum { MOE_ROUTE_WITHIN = 0, MOE_ROUTE_ACROSS = 1 } moe_route_mode;
 
 typedef struct {
   int32_t T, d_model, d_ff, E, G;
@@ -86,6 +95,7 @@ typedef struct {
   int32_t rank;         /* r >= 0; r == 0 means no residual (residual pointers may be NULL)      */
   int32_t act_dtype;    /* moe_dtype of x, y, routers and base weights                           */
   int32_t resid_fmt;    /* moe_resid_fmt                                                         */
+  int32_t route_mode;   /* moe_route_mode (0, the within-group reading, when zero-initialised)    */
 } moe_hier_desc;
 /* Limits: T >= 0; d_model % 128 == 0; d_ff % 64 == 0; E % G == 0; E <= 256; k_e*k_g <= 16;
  * r <= 64.  INT4 residuals need a BF16 layer, F32 residuals an F32 layer.                    */

@@ -46,7 +46,10 @@ def check_y(y_gpu, y_ref, what=""):
 def check_routing(out, ref):
     assert np.array_equal(out["gidx"].cpu().numpy(), ref["gidx"])
     assert np.array_equal(out["eidx"].cpu().numpy(), ref["eidx"])
-    assert np.abs(out["gate"].cpu().numpy().astype(np.float64) - ref["gate"]).max() <= GATE_TOL
+    gate = out["gate"].cpu().numpy().astype(np.float64)
+    assert np.abs(gate - ref["gate"]).max() <= GATE_TOL
+    # the slots a reading does not pick carry exactly zero (picked ones are positive)
+    assert np.array_equal(gate > 0, ref["active"])
 
 
 def small(**kw):
@@ -85,6 +88,12 @@ CASES = {
     "bf16_G64": small(T=200, E=128, G=64, kg=3, ke=2, group_map="perm", seed=37, resid_std=0.2),
     "bf16_K1": small(T=200, E=4, G=4, kg=2, ke=1, seed=28),
     "f32_kg2": small(T=130, dtype="f32", resid="f32", r=4, kg=2, ke=1, E=8, G=4, seed=29, resid_std=0.2),
+    # the across-groups reading: top-k_e over the union of the chosen groups, zero gates elsewhere
+    "bf16_across_kg2_ke3": small(T=1200, d=512, f=320, E=64, G=8, kg=2, ke=3, group_map="contiguous", seed=55,
+                                 zipf_s=1.2, resid_std=0.2, route="across"),
+    "bf16_across_few_tokens": small(T=300, E=32, G=4, kg=2, ke=2, seed=56, resid_std=0.2, route="across"),
+    "f32_across": small(T=130, dtype="f32", resid="f32", r=4, kg=2, ke=2, E=12, G=3, seed=57, resid_std=0.2,
+                        route="across"),
 }
 
 
@@ -284,7 +293,7 @@ def full_size_check(name, n_sample, cfg=None):
     gm = inp["group_map"].numpy()
     routing = oracle.route(oracle.moe._np(inp["x"]), oracle.moe._np(inp["w_group"]),
                            oracle.moe._np(inp["b_group"]), oracle.moe._np(inp["w_expert"]), gm,
-                           cfg.kg, cfg.ke)
+                           cfg.kg, cfg.ke, cfg.route)
     check_routing(out, routing)
     pref = oracle.permute(routing["eidx"], gm, cfg.G, cfg.ke)
     assert np.array_equal(out["perm"].cpu().numpy(), pref["perm"])
@@ -296,7 +305,8 @@ def full_size_check(name, n_sample, cfg=None):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name,n", [("mixtral_prefill", 24), ("finegrained_skewed", 64), ("decode", 8)])
+@pytest.mark.parametrize("name,n", [("mixtral_prefill", 24), ("finegrained_skewed", 64), ("decode", 8),
+                                    ("finegrained_across", 64)])
 def test_full_size_sampled(name, n):
     full_size_check(name, n)
 

@@ -27,3 +27,13 @@ def test_load_stats_counts_and_special_cases():
     assert even["group"]["max_over_mean"] == 1.0 and even["expert"]["cv"] == 0.0
     one = workload.load_stats(np.zeros((T, 1), np.int32), np.zeros((T, 1), np.int32), G, E)
     assert one["expert"]["max_over_mean"] == E and one["group"]["max_over_mean"] == G
+
+
+def test_load_stats_counts_only_active_assignments():
+    """With the across-groups reading's picked-slot mask, unpicked (zero-gate) slots add no load."""
+    from compressed_expert_two_b300 import workload
+    eidx = np.array([[0, 1, 4, 5], [0, 2, 4, 6]], dtype=np.int32)
+    active = np.array([[True, False, True, False], [True, True, False, False]])
+    st = workload.load_stats(np.array([[0, 1], [0, 1]]), eidx, 2, 8, active=active)
+    assert st["expert"]["max"] == 2 and st["expert"]["min"] == 0      # expert 0 twice, 1/5/6 never
+    assert np.isclose(st["expert"]["max_over_mean"], 2 / (4 / 8))
