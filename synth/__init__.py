@@ -181,3 +181,66 @@ def variant(cfg: MoEConfig, kind: str) -> MoEConfig:
     if kind == "rank0":
         return cfg.replace(name=cfg.name + "+r0", r=0)
     raise ValueError(kind)
+
+
+# --------------------------------------------------------------------------------------------
+# Dense experts for the compression step (the step that produces the layer's weights)
+# --------------------------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class CompressConfig:
+    name: str
+    E: int
+    G: int
+    d: int          # d_model
+    f: int          # d_ff
+    r: int          # residual rank kept
+    seed: int
+    oversample: int = 16      # extra columns of the randomised range finder's test matrix
+    power_iters: int = 4      # subspace iterations of the randomised range finder
+    dev_scale: float = 0.05   # ||expert's own rank-r deviation||_F / ||shared part||_F
+    noise: float = 0.01       # ||full-rank noise||_F / ||shared part||_F
+    group_map: str = "contiguous"
+
+    @property
+    def K(self) -> int:
+        return self.E // self.G
+
+    @property
+    def l(self) -> int:
+        return self.r + self.oversample
+
+
+COMPRESS_CONFIGS: Dict[str, CompressConfig] = {
+    # the layer shapes of the small BF16 and Mixtral-shaped workloads, as dense experts
+    "compress_small": CompressConfig("compress_small", E=16, G=4, d=1024, f=2816, r=16, seed=11),
+    "compress_mixtral": CompressConfig("compress_mixtral", E=8, G=2, d=4096, f=14336, r=16, seed=12),
+}
+
+
+def make_dense_experts(cfg: CompressConfig, kinds=("gate", "up", "down")) -> dict:
+    """Seeded dense expert weights W_i = shared_g + dev_i + noise_i, stored as BF16 [E][d_out][d_in]
+    per matrix kind, with shared_g ~ N(0, 1/d_in) per group, dev_i = U_i V_i^T of rank r (Gaussian
+    factors, scaled to dev_scale of the shared part's Frobenius norm) and Gaussian noise (noise of
+    it): experts of a group that share most of their weights, each with a low-rank individuality.
+    Also draws, per kind, the randomised range finder's Gaussian test matrix omega [d_in][r + p]
+    (FP32): the random numbers the GPU's truncated SVD uses are inputs, not drawn on the device."""
+    gen = torch.Generator().manual_seed(cfg.seed)
+    dims = {"gate": (cfg.d, cfg.f), "up": (cfg.d, cfg.f), "down": (cfg.f, cfg.d)}   # (d_in, d_out)
+    if cfg.group_map == "contiguous":
+        gm = (torch.arange(cfg.E) // cfg.K).to(torch.int32)
+    else:
+        gm = (torch.randperm(cfg.E, generator=gen) // cfg.K).to(torch.int32)
+    out = {"cfg": cfg, "group_map": gm}
+    for m in kinds:
+        d_in, d_out = dims[m]
+        W = torch.empty(cfg.E, d_out, d_in, dtype=torch.bfloat16)
+        for g in range(cfg.G):
+            shared = torch.randn(d_out, d_in, generator=gen) / math.sqrt(d_in)
+            for e in torch.nonzero(gm == g).flatten().tolist():
+                U = torch.randn(d_out, cfg.r, generator=gen)
+                V = torch.randn(d_in, cfg.r, generator=gen)
+                dev = (U @ V.T) * (cfg.dev_scale / math.sqrt(d_in * cfg.r))
+                noise = torch.randn(d_out, d_in, generator=gen) * (cfg.noise / math.sqrt(d_in))
+                W[e] = (shared + dev + noise).to(torch.bfloat16)
+        out[m] = {"W": W, "omega": torch.randn(d_in, cfg.l, generator=gen)}
+    return out
