@@ -44,7 +44,15 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="profiling aid: run the workload's layer on this many tokens instead of its T")
     return ap.parse_args()
+
+
+def workload_config(args):
+    from synth import CONFIGS
+    cfg = CONFIGS[args.config]
+    return cfg.replace(T=args.tokens) if args.tokens > 0 else cfg
 
 
 def load_peaks():
@@ -300,9 +308,9 @@ def run_ours(args, rank, world, local_rank):
     from compressed_expert_two_b300 import _lib as L
     from compressed_expert_two_b300 import workload
     from compressed_expert_two_b300.layer import DeviceLayer
-    from synth import CONFIGS, make_inputs
+    from synth import make_inputs
 
-    cfg = CONFIGS[args.config]
+    cfg = workload_config(args)
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     inp = make_inputs(cfg)
@@ -530,8 +538,8 @@ def main():
 
 def run_reference(args):
     """The oracle as the reference arm, on the host cores, each step a bounded token sample."""
-    from synth import CONFIGS, make_inputs
-    cfg = CONFIGS[args.config]
+    from synth import make_inputs
+    cfg = workload_config(args)
     inp = make_inputs(cfg)
     chunk = CPU_CHUNK.get(args.config, 256)
     per_step = []

@@ -28,6 +28,12 @@ class MoeHierDesc(ctypes.Structure):
                 ("route_mode", ctypes.c_int32)]
 
 
+class MoeHierCompressDesc(ctypes.Structure):
+    _fields_ = [("E", ctypes.c_int32), ("G", ctypes.c_int32), ("d_out", ctypes.c_int32),
+                ("d_in", ctypes.c_int32), ("rank", ctypes.c_int32), ("sketch", ctypes.c_int32),
+                ("power_iters", ctypes.c_int32)]
+
+
 class MoeHierResid(ctypes.Structure):
     _fields_ = [("A", ctypes.c_void_p * 3), ("B", ctypes.c_void_p * 3),
                 ("sA", ctypes.c_void_p * 3), ("sB", ctypes.c_void_p * 3)]
@@ -36,7 +42,8 @@ class MoeHierResid(ctypes.Structure):
 EXPORTS = ["moe_hier_workspace_size", "moe_hier_route", "moe_hier_permute", "moe_hier_ffn",
            "moe_hier_combine", "moe_hier_forward", "moe_hier_get_status", "moe_hier_status_string",
            "moe_hier_last_cuda_error", "moe_hier_profile_begin", "moe_hier_profile_end",
-           "moe_hier_debug_set_wait", "moe_hier_debug_route_tc", "moe_hier_permute_noalloc"]
+           "moe_hier_debug_set_wait", "moe_hier_debug_route_tc", "moe_hier_permute_noalloc",
+           "moe_hier_compress_workspace_size", "moe_hier_compress", "moe_hier_quantise_int4"]
 
 
 class MoeError(RuntimeError):
@@ -67,13 +74,19 @@ def _load() -> ctypes.CDLL:
     lib.moe_hier_profile_end.argtypes = [ctypes.POINTER(ctypes.c_char_p), I]
     lib.moe_hier_status_string.argtypes = [I]
     lib.moe_hier_status_string.restype = ctypes.c_char_p
+    C = ctypes.POINTER(MoeHierCompressDesc)
+    lib.moe_hier_compress_workspace_size.argtypes = [C, ctypes.POINTER(ctypes.c_int)]
+    lib.moe_hier_compress_workspace_size.restype = S
+    lib.moe_hier_compress.argtypes = [C] + [P] * 13 + [S, P]
+    lib.moe_hier_quantise_int4.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P, P, P]
     lib.moe_hier_debug_set_wait.argtypes = [ctypes.c_uint64, I]
     lib.moe_hier_debug_route_tc.argtypes = [D, P, P, P, P, P, P, P, S, P]
     lib.moe_hier_permute_noalloc.argtypes = [D] + [P] * 11
     lib.moe_hier_last_cuda_error.argtypes = []
     lib.moe_hier_last_cuda_error.restype = ctypes.c_char_p
     for name in EXPORTS:
-        if name not in ("moe_hier_workspace_size", "moe_hier_status_string", "moe_hier_last_cuda_error"):
+        if name not in ("moe_hier_workspace_size", "moe_hier_status_string", "moe_hier_last_cuda_error",
+                        "moe_hier_compress_workspace_size"):
             getattr(lib, name).restype = I
     return lib
 
@@ -169,6 +182,24 @@ def moe_hier_debug_route_tc(desc, x, w_group, b_group, w_expert, group_map_host,
     _check("moe_hier_debug_route_tc", lib.moe_hier_debug_route_tc(
         ctypes.byref(desc), _p(x), _p(w_group), _p(b_group), _p(w_expert), _p(group_map_host), _p(out),
         _p(ws), ws_bytes, stream))
+
+
+def moe_hier_compress_workspace_size(desc: MoeHierCompressDesc) -> int:
+    st = ctypes.c_int(0)
+    n = lib.moe_hier_compress_workspace_size(ctypes.byref(desc), ctypes.byref(st))
+    _check("moe_hier_compress_workspace_size", st.value)
+    return n
+
+
+def moe_hier_compress(desc, w, group_map_host, omega, base, A_codes, A_scales, B_codes, B_scales, sigma, err,
+                      At_f32, Bt_f32, ws, ws_bytes, stream):
+    _check("moe_hier_compress", lib.moe_hier_compress(
+        ctypes.byref(desc), _p(w), _p(group_map_host), _p(omega), _p(base), _p(A_codes), _p(A_scales),
+        _p(B_codes), _p(B_scales), _p(sigma), _p(err), _p(At_f32), _p(Bt_f32), _p(ws), ws_bytes, stream))
+
+
+def moe_hier_quantise_int4(v, rows: int, n: int, codes, scales, stream):
+    _check("moe_hier_quantise_int4", lib.moe_hier_quantise_int4(_p(v), rows, n, _p(codes), _p(scales), stream))
 
 
 def moe_hier_get_status(ws, stream) -> int:

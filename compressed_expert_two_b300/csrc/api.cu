@@ -104,6 +104,8 @@ static int validate(const moe_hier_desc* desc, const int32_t* group_map, LayerAr
   a->int4 = D.resid_fmt == MOE_RESID_INT4_G64;
   a->R = a->T * a->kg;
   a->across = D.route_mode == MOE_ROUTE_ACROSS;
+  a->wslots = D.G;
+  for (int g = 0; g < D.G; ++g) a->tab.wslot[g] = (uint8_t)g;
   a->tab.E = D.E; a->tab.G = D.G; a->tab.K = K;
   if (group_map) {
     int fill[kMaxE];
@@ -355,6 +357,61 @@ int moe_hier_forward(const moe_hier_desc* desc, const void* x, const void* w_gro
     if (e == cudaSuccess) e = j;
   }
   return cuda_status(e);
+}
+
+static int compress_args(const moe_hier_compress_desc* d, const int32_t* group_map, CmpArgs* c) {
+  if (!d) return MOE_ERR_INVALID;
+  if (d->E <= 0 || d->G <= 0 || d->E % d->G != 0 || d->E > kMaxE) return MOE_ERR_INVALID;
+  if (d->d_in <= 0 || d->d_out <= 0 || d->d_in % 128 != 0 || d->d_out % 128 != 0) return MOE_ERR_INVALID;
+  if (d->rank < 1 || d->rank > 32 || d->sketch <= d->rank || d->sketch > 64) return MOE_ERR_INVALID;
+  if (d->power_iters < 0 || d->power_iters > 16) return MOE_ERR_INVALID;
+  memset(c, 0, sizeof(*c));
+  c->E = d->E; c->G = d->G; c->d_out = d->d_out; c->d_in = d->d_in; c->r = d->rank; c->l = d->sketch;
+  c->power_iters = d->power_iters;
+  if (group_map) {
+    const int K = d->E / d->G;
+    int fill[kMaxE] = {0};
+    for (int e = 0; e < d->E; ++e) {
+      const int g = group_map[e];
+      if (g < 0 || g >= d->G || fill[g] >= K) return MOE_ERR_INVALID;
+      c->member[g * K + fill[g]++] = (uint8_t)e;
+      c->group_of[e] = (uint8_t)g;
+    }
+  }
+  return MOE_OK;
+}
+
+size_t moe_hier_compress_workspace_size(const moe_hier_compress_desc* desc, int* status_out) {
+  CmpArgs c;
+  const int st = compress_args(desc, nullptr, &c);
+  if (status_out) *status_out = st;
+  return st == MOE_OK ? cmp_workspace_bytes(c) : 0;
+}
+
+int moe_hier_compress(const moe_hier_compress_desc* desc, const void* w, const int32_t* group_map_host,
+                      const float* omega, void* base, void* A_codes, void* A_scales, void* B_codes, void* B_scales,
+                      float* sigma, double* err, float* At_f32, float* Bt_f32, void* ws, size_t ws_bytes,
+                      void* stream) {
+  CmpArgs c;
+  if (!group_map_host) return MOE_ERR_INVALID;
+  int st = compress_args(desc, group_map_host, &c);
+  if (st != MOE_OK) return st;
+  if (!w || !omega || !base || !A_codes || !A_scales || !B_codes || !B_scales || !sigma) return MOE_ERR_INVALID;
+  if (!aligned16(w) || !aligned16(omega) || !aligned16(base) || !aligned16(A_codes) || !aligned16(B_codes) ||
+      ((uintptr_t)A_scales & 1) || ((uintptr_t)B_scales & 1) || ((uintptr_t)sigma & 3) || ((uintptr_t)err & 7) ||
+      !aligned16(At_f32) || !aligned16(Bt_f32))
+    return MOE_ERR_INVALID;
+  if (!ws || ((uintptr_t)ws & 255) != 0 || ws_bytes < cmp_workspace_bytes(c)) return MOE_ERR_WORKSPACE;
+  prof_start((cudaStream_t)stream);
+  return cuda_status(launch_compress(c, w, omega, base, (uint8_t*)A_codes, (__half*)A_scales, (uint8_t*)B_codes,
+                                     (__half*)B_scales, sigma, err, At_f32, Bt_f32, ws, (cudaStream_t)stream));
+}
+
+int moe_hier_quantise_int4(const float* v, int64_t rows, int32_t n, void* codes, void* scales, void* stream) {
+  if (rows < 0 || n <= 0 || n % 64 != 0) return MOE_ERR_INVALID;
+  if (rows > 0 && (!v || !codes || !scales || ((uintptr_t)v & 7) || ((uintptr_t)scales & 1))) return MOE_ERR_INVALID;
+  prof_start((cudaStream_t)stream);
+  return cuda_status(launch_quant_int4(v, (size_t)rows, n, (uint8_t*)codes, (__half*)scales, (cudaStream_t)stream));
 }
 
 int moe_hier_debug_set_wait(uint64_t wait_ns, int phantom_arrivals) {

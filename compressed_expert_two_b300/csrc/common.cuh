@@ -77,6 +77,8 @@ struct GroupTable {
   uint8_t member[kMaxE];    // member[g*K + i] = i-th expert (ascending id) of group g
   uint8_t group_of[kMaxE];  // group of expert e
   uint8_t local_of[kMaxE];  // position of expert e inside its group
+  uint8_t wslot[kMaxE];     // slot of group g's base matrices in the base arrays (g, unless the
+                            // bases are offloaded and group g sits in cache slot wslot[g])
 };
 
 // Device status word at the start of every workspace (bounded waits report here).

@@ -387,13 +387,22 @@ __global__ void __launch_bounds__(256, 2) u_simt_kernel(const __nv_bfloat16* __r
 // 3/6. Generic grouped GEMM: out[row] = [A0 | A1][i] [B0_g | B1_g]^T (BF16 in, FP32 acc, BF16,
 //      FP32 or FP16 out).  Group g's B rows start at g*b_stride in B0 and at g*b_stride + b1_off in B1.
 enum OutKind { kOutBf16 = 0, kOutF32 = 1, kOutF16 = 2 };
+// Slot of group g's rows in B0 (g itself unless B0 is a cache of offloaded group bases).
+struct SlotMap {
+  uint8_t s[kMaxE];
+};
+static SlotMap identity_slots() {
+  SlotMap m;
+  for (int i = 0; i < kMaxE; ++i) m.s[i] = (uint8_t)i;
+  return m;
+}
 // ------------------------------------------------------------------------------------------
 template <int BN, int STAGES, int OUT>
 __global__ void __launch_bounds__(192, 1) tc_gemm_kernel(
     const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
     const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1, int nk0, int nk1,
     const int32_t* __restrict__ row_begin, int G, int b_stride, int b1_off, void* __restrict__ out, int out_ld,
-    const int32_t* __restrict__ scatter, DevStatus* status) {
+    const int32_t* __restrict__ scatter, DevStatus* status, SlotMap b0s) {
   pdl_wait();
   pdl_trigger();
   constexpr uint32_t A_BYTES = kTile * 128, B_BYTES = BN * 128;
@@ -438,7 +447,8 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_kernel(
       const bool first = kb < nk0;
       const int kx = (first ? kb : kb - nk0) * 64;
       tc::tma_load_2d(sA + s * A_BYTES, first ? &mA0 : &mA1, &full[s], kx, r0);
-      tc::tma_load_2d(sB + s * B_BYTES, first ? &mB0 : &mB1, &full[s], kx, g * b_stride + (first ? 0 : b1_off) + n0);
+      tc::tma_load_2d(sB + s * B_BYTES, first ? &mB0 : &mB1, &full[s], kx,
+                      (first ? (int)b0s.s[g] : g) * b_stride + (first ? 0 : b1_off) + n0);
     }
     if (abort_flag) tc::drain_copies();
   } else if (warp == 1 && lane == 0) {
@@ -516,7 +526,7 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_persist_kernel(
     const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
     const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1, int nk0, int nk1,
     const int32_t* __restrict__ row_begin, int G, int b_stride, int b1_off, int tiles, int n_tiles,
-    void* __restrict__ out, int out_ld, const int32_t* __restrict__ scatter, DevStatus* status) {
+    void* __restrict__ out, int out_ld, const int32_t* __restrict__ scatter, DevStatus* status, SlotMap b0s) {
   pdl_wait();
   pdl_trigger();
   constexpr uint32_t A_BYTES = kTile * 128, B_BYTES = BN * 128;
@@ -564,7 +574,8 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_persist_kernel(
         const bool first = kb < nk0;
         const int kx = (first ? kb : kb - nk0) * 64;
         tc::tma_load_2d(sA + s * A_BYTES, first ? &mA0 : &mA1, &full[s], kx, r0);
-        tc::tma_load_2d(sB + s * B_BYTES, first ? &mB0 : &mB1, &full[s], kx, g * b_stride + (first ? 0 : b1_off) + n0);
+        tc::tma_load_2d(sB + s * B_BYTES, first ? &mB0 : &mB1, &full[s], kx,
+                        (first ? (int)b0s.s[g] : g) * b_stride + (first ? 0 : b1_off) + n0);
       }
     }
     if (abort_flag) tc::drain_copies();
@@ -692,7 +703,7 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_pair_kernel(
     const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
     const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1, int nk0, int nk1,
     const int32_t* __restrict__ row_begin, int G, int b_stride, int b1_off, void* __restrict__ out, int out_ld,
-    const int32_t* __restrict__ scatter, DevStatus* status, int dense_rows) {
+    const int32_t* __restrict__ scatter, DevStatus* status, int dense_rows, SlotMap b0s) {
   constexpr int BH = BN / 2;                                  // B rows held by each CTA
   constexpr uint32_t A_BYTES = kTile * 128, B_BYTES = BH * 128, STAGE_BYTES = A_BYTES + B_BYTES;
   extern __shared__ uint8_t smem_raw[];
@@ -750,7 +761,7 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_pair_kernel(
       uint8_t* st = smem + s * STAGE_BYTES;
       tc::tma_load_2d_pair(st, first ? &mA0 : &mA1, full0 + 8 * s, kx, r0);
       tc::tma_load_2d_pair(st + A_BYTES, first ? &mB0 : &mB1, full0 + 8 * s, kx,
-                           g * b_stride + (first ? 0 : b1_off) + n0 + (int)rank * BH);
+                           (first ? (int)b0s.s[g] : g) * b_stride + (first ? 0 : b1_off) + n0 + (int)rank * BH);
     }
     // every commit rank 0 sends to this CTA's stage barriers has landed before the CTA exits
     if (ok) {
@@ -947,8 +958,8 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
           uint8_t* st = sStage + s * STAGE_BYTES;
           tc::bar_expect_tx(&full[s], STAGE_BYTES);
           tc::tma_load_2d(st, &mX, &full[s], kb * 64, r0);
-          tc::tma_load_2d(st + X_BYTES, &mWg, &full[s], kb * 64, g * f + n0);
-          tc::tma_load_2d(st + X_BYTES + kNf * 128, &mWu, &full[s], kb * 64, g * f + n0);
+          tc::tma_load_2d(st + X_BYTES, &mWg, &full[s], kb * 64, (int)p.tab.wslot[g] * f + n0);
+          tc::tma_load_2d(st + X_BYTES + kNf * 128, &mWu, &full[s], kb * 64, (int)p.tab.wslot[g] * f + n0);
         }
       }
       if (abort_flag) tc::drain_copies();
@@ -1375,8 +1386,8 @@ __global__ void __launch_bounds__(kUp3Warps * 32, 1) ffn_up3_kernel(
           uint8_t* st = sStage + s * STAGE_BYTES;
           tc::bar_expect_tx(&full[s], STAGE_BYTES);
           tc::tma_load_2d(st, &mX, &full[s], kb * 64, r0);
-          tc::tma_load_2d(st + X_BYTES, &mWg, &full[s], kb * 64, g * f + n0);
-          tc::tma_load_2d(st + X_BYTES + NF * 128, &mWu, &full[s], kb * 64, g * f + n0);
+          tc::tma_load_2d(st + X_BYTES, &mWg, &full[s], kb * 64, (int)p.tab.wslot[g] * f + n0);
+          tc::tma_load_2d(st + X_BYTES + NF * 128, &mWu, &full[s], kb * 64, (int)p.tab.wslot[g] * f + n0);
         }
       }
       if (abort_flag) tc::drain_copies();
@@ -1789,7 +1800,8 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up4p_kernel(
           uint8_t* st = sStage + s * STAGE_BYTES;
           if (rank == 0) tc::bar_expect_tx(&full[s], 2 * STAGE_BYTES);
           tc::tma_load_2d_pair(st, &mX, full0 + 8 * s, kb * 64, r0);
-          tc::tma_load_2d_pair(st + X_BYTES, rank == 0 ? &mWg : &mWu, full0 + 8 * s, kb * 64, g * f + n0);
+          tc::tma_load_2d_pair(st + X_BYTES, rank == 0 ? &mWg : &mWu, full0 + 8 * s, kb * 64,
+                               (int)p.tab.wslot[g] * f + n0);
         }
       }
       // every commit rank 0 sends to this CTA's stage barriers has landed before the CTA exits
@@ -2172,14 +2184,14 @@ template <int BN, int OUT>
 static cudaError_t launch_gemm(const CUtensorMap& A0, const CUtensorMap& A1, const CUtensorMap& B0,
                                const CUtensorMap& B1, int nk0, int nk1, const int32_t* row_begin, int G,
                                int n_out, int b_stride, int b1_off, int tiles, void* out, int out_ld,
-                               const int32_t* scatter, DevStatus* st, cudaStream_t stream) {
+                               const int32_t* scatter, DevStatus* st, cudaStream_t stream, const SlotMap& b0s) {
   constexpr int STAGES = BN >= 256 ? 4 : 6;
   const size_t smem = 1024 + (size_t)STAGES * (kTile * 128 + BN * 128);
   static std::atomic<uint64_t> attr{0};
   if (const cudaError_t e = smem_attr_once(tc_gemm_kernel<BN, STAGES, OUT>, smem, attr); e != cudaSuccess) return e;
   dim3 grid(n_out / BN, tiles);
   return launch_pdl(tc_gemm_kernel<BN, STAGES, OUT>, grid, dim3(192), smem, stream, A0, A1, B0, B1, nk0, nk1,
-                    row_begin, G, b_stride, b1_off, out, out_ld, scatter, st);
+                    row_begin, G, b_stride, b1_off, out, out_ld, scatter, st, b0s);
 }
 
 // Persistent version: one CTA per SM over all (row tile, N tile) items.
@@ -2187,7 +2199,8 @@ template <int BN, int OUT>
 static cudaError_t launch_gemm_persist(const CUtensorMap& A0, const CUtensorMap& A1, const CUtensorMap& B0,
                                        const CUtensorMap& B1, int nk0, int nk1, const int32_t* row_begin, int G,
                                        int n_out, int b_stride, int b1_off, int tiles, void* out, int out_ld,
-                                       const int32_t* scatter, DevStatus* st, cudaStream_t stream) {
+                                       const int32_t* scatter, DevStatus* st, cudaStream_t stream,
+                                       const SlotMap& b0s) {
   constexpr int STAGES = BN >= 256 ? 4 : 6;
   const size_t smem = 1024 + (size_t)STAGES * (kTile * 128 + BN * 128);
   static std::atomic<uint64_t> attr{0};
@@ -2198,7 +2211,8 @@ static cudaError_t launch_gemm_persist(const CUtensorMap& A0, const CUtensorMap&
   if (cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev); e != cudaSuccess) return e;
   const int n_tiles = n_out / BN, items = tiles * n_tiles;
   return launch_pdl(tc_gemm_persist_kernel<BN, STAGES, OUT>, dim3(items < sms ? items : sms), dim3(192), smem, stream,
-                    A0, A1, B0, B1, nk0, nk1, row_begin, G, b_stride, b1_off, tiles, n_tiles, out, out_ld, scatter, st);
+                    A0, A1, B0, B1, nk0, nk1, row_begin, G, b_stride, b1_off, tiles, n_tiles, out, out_ld, scatter, st,
+                    b0s);
 }
 
 // CTA-pair version: grid.x = 2 x (an upper bound of the row-tile pairs), clusters of two CTAs
@@ -2207,14 +2221,15 @@ template <int BN, int OUT>
 static cudaError_t launch_gemm_pair(const CUtensorMap& A0, const CUtensorMap& A1, const CUtensorMap& B0,
                                     const CUtensorMap& B1, int nk0, int nk1, const int32_t* row_begin, int G,
                                     int n_out, int b_stride, int b1_off, int pairs, void* out, int out_ld,
-                                    const int32_t* scatter, DevStatus* st, cudaStream_t stream, int dense_rows = 0) {
+                                    const int32_t* scatter, DevStatus* st, cudaStream_t stream, const SlotMap& b0s,
+                                    int dense_rows = 0) {
   constexpr int STAGES = BN >= 256 ? 6 : 8;
   const size_t smem = 1024 + (size_t)STAGES * (kTile * 128 + (BN / 2) * 128);
   static std::atomic<uint64_t> attr{0};
   if (const cudaError_t e = smem_attr_once(tc_gemm_pair_kernel<BN, STAGES, OUT>, smem, attr); e != cudaSuccess) return e;
   return launch_pdl_cluster(tc_gemm_pair_kernel<BN, STAGES, OUT>, dim3(2 * pairs, n_out / BN), dim3(192),
                             dim3(2, 1, 1), smem, stream, A0, A1, B0, B1, nk0, nk1, row_begin, G, b_stride, b1_off,
-                            out, out_ld, scatter, st, dense_rows);
+                            out, out_ld, scatter, st, dense_rows, b0s);
 }
 
 template <int KRP, int KE>
@@ -2300,7 +2315,7 @@ cudaError_t launch_resid_prep(const LayerArgs& a, const ResidPtrs& rp, const TcB
     return cudaErrorInvalidValue;
   e = launch_gemm_pair<128, kOutF16>(mXt, mXt, mA, mA, d / 64, d / 64, nullptr, G, G * 2 * KRP, 4 * KRP, 2 * KRP,
                                      (a.T + 2 * kTile - 1) / (2 * kTile), b.Ud, G * 2 * KRP, nullptr, status, st,
-                                     a.T);
+                                     identity_slots(), a.T);
   prof_mark("u_gemm", st);
   return e;
 }
@@ -2340,13 +2355,13 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   const bool down_pair = d % 256 == 0 && f >= 2048 && R >= 2048;
   bool ok = make_map(&mX, b.X, Rp, d, kTile) &&
             make_map(&mAhi, b.Ain, (uint64_t)G * 4 * KRP, d, KRP) &&
-            make_map(&mWg, wg, (uint64_t)G * f, d, nf_up) && make_map(&mWu, wu, (uint64_t)G * f, d, nf_up) &&
+            make_map(&mWg, wg, (uint64_t)a.wslots * f, d, nf_up) && make_map(&mWu, wu, (uint64_t)a.wslots * f, d, nf_up) &&
             make_map(&mBg, b.Bgs, (uint64_t)G * f, KRP, nf_up) && make_map(&mBu, b.Bus, (uint64_t)G * f, KRP, nf_up) &&
             make_map(&mAd, b.Adn, (uint64_t)G * KRP, f, KRP) && make_map(&mH, b.hsum, Rp, f, kTile) &&
             make_map(&mVt, b.Vt, Rp, 2 * KRP, kTile);
   mAlo = mAhi;
   const int BN2 = down_pair ? 128 : (d % 256 == 0 ? 256 : 128);   // B box rows: half of N = 256 for pairs
-  ok = ok && make_map(&mWd, wd, (uint64_t)G * d, f, BN2) && make_map(&mBd, b.Bdn, (uint64_t)G * d, 2 * KRP, BN2);
+  ok = ok && make_map(&mWd, wd, (uint64_t)a.wslots * d, f, BN2) && make_map(&mBd, b.Bdn, (uint64_t)G * d, 2 * KRP, BN2);
   if (up4) ok = ok && make_map_plain(&mAdt, b.Adt, (uint64_t)G * f, KRP, kNf3);
   if (!ok) return cudaErrorInvalidValue;
 
@@ -2361,9 +2376,9 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   } else {
     e = (2 * KRP == 256)
             ? launch_gemm_pair<256, kOutF16>(mX, mX, mAhi, mAlo, d / 64, d / 64, row_begin, G, 2 * KRP, 4 * KRP,
-                                             2 * KRP, pairs, b.U, 2 * KRP, nullptr, status, st)
+                                             2 * KRP, pairs, b.U, 2 * KRP, nullptr, status, st, identity_slots())
             : launch_gemm_pair<128, kOutF16>(mX, mX, mAhi, mAlo, d / 64, d / 64, row_begin, G, 2 * KRP, 4 * KRP,
-                                             2 * KRP, pairs, b.U, 2 * KRP, nullptr, status, st);
+                                             2 * KRP, pairs, b.U, 2 * KRP, nullptr, status, st, identity_slots());
     prof_mark("u_gemm", st);
   }
   if (e != cudaSuccess) return e;
@@ -2405,14 +2420,16 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   // many waves of single-CTA tiles: the persistent form overlaps each tile's epilogue with the
   // next tile's K loop
   const bool down_persist = !down_pair && BN2 == 256 && tiles * (d / 256) > 2 * 148;
+  SlotMap wd_slots;                              // W_down rows of group g start at wslot[g] * d
+  for (int i = 0; i < kMaxE; ++i) wd_slots.s[i] = a.tab.wslot[i];
   e = down_pair ? launch_gemm_pair<256, kOutBf16>(mH, mVt, mWd, mBd, f / 64, 2 * KRP / 64, row_begin, G, d, d, 0,
-                                                  pairs, y_rows, d, row_asg, status, st)
+                                                  pairs, y_rows, d, row_asg, status, st, wd_slots)
       : down_persist ? launch_gemm_persist<256, kOutBf16>(mH, mVt, mWd, mBd, f / 64, 2 * KRP / 64, row_begin, G, d,
-                                                          d, 0, tiles, y_rows, d, row_asg, status, st)
+                                                          d, 0, tiles, y_rows, d, row_asg, status, st, wd_slots)
                 : (BN2 == 256 ? launch_gemm<256, kOutBf16>(mH, mVt, mWd, mBd, f / 64, 2 * KRP / 64, row_begin, G, d,
-                                                           d, 0, tiles, y_rows, d, row_asg, status, st)
+                                                           d, 0, tiles, y_rows, d, row_asg, status, st, wd_slots)
                               : launch_gemm<128, kOutBf16>(mH, mVt, mWd, mBd, f / 64, 2 * KRP / 64, row_begin, G, d,
-                                                           d, 0, tiles, y_rows, d, row_asg, status, st));
+                                                           d, 0, tiles, y_rows, d, row_asg, status, st, wd_slots));
   prof_mark("ffn_down_tc", st);
   return e;
 }

@@ -15,6 +15,7 @@ struct LayerArgs {
   bool int4;        // residual INT4 group-64 (else FP32)
   int R;            // rows = T * kg
   bool across;      // MOE_ROUTE_ACROSS: top k_e over the union of the chosen groups
+  int wslots;       // group slots in the base arrays w_gate / w_up / w_down (G, or the cache size)
   GroupTable tab;
 };
 
@@ -108,5 +109,17 @@ cudaError_t launch_resid_prep(const LayerArgs& a, const ResidPtrs& rp, const TcB
 bool tc_u_dense(const LayerArgs& a);
 
 cudaError_t launch_combine(const LayerArgs& a, const void* y_rows, void* y, cudaStream_t st);
+
+// Compression step (compress.cu): one matrix kind of every expert.
+struct CmpArgs {
+  int E, G, d_out, d_in, r, l, power_iters;
+  uint8_t member[kMaxE];     // member[g*K + i]: i-th expert (ascending id) of group g
+  uint8_t group_of[kMaxE];
+};
+size_t cmp_workspace_bytes(const CmpArgs& c);
+cudaError_t launch_compress(const CmpArgs& c, const void* W, const float* omega, void* base_out, uint8_t* Aq,
+                            __half* As, uint8_t* Bq, __half* Bs, float* sigma, double* err, float* At_out,
+                            float* Bt_out, void* ws, cudaStream_t st);
+cudaError_t launch_quant_int4(const float* v, size_t rows, int n, uint8_t* codes, __half* scales, cudaStream_t st);
 
 }  // namespace moe

@@ -182,6 +182,45 @@ const char* moe_hier_last_cuda_error(void);
 int moe_hier_profile_begin(void* const* events, int n_events);
 int moe_hier_profile_end(const char** names, int max_names);
 
+/* ---------------------------------------------------------------------------------------------
+ * Compression: the step that produces a layer's weights from dense experts ("Breaking the MoE
+ * LLM Trilemma", key design 2: the group's shared base is the mean of its experts' weights, each
+ * expert keeps a rank-r residual initialised by a truncated SVD of W_i - W_base^g, quality is the
+ * Frobenius reconstruction error; key design 4: 16-bit base, INT4 residual).  One call handles
+ * one matrix kind (gate, up or down) of every expert.
+ *   base[g] = bf16(fl32(sum over the group's members, ascending id, of W_i) / K) (FP32 adds,
+ *     round to nearest even);
+ *   R_i = W_i - base[g(i)] (the stored base); its best rank-r approximation B_i A_i^T, computed by a
+ *     randomised range finder with `power_iters` subspace iterations on `sketch` columns (the
+ *     Gaussian test matrix omega is an input), split evenly: B = U_r S^{1/2}, A = V_r S^{1/2};
+ *   A^T [E][r][d_in] and B^T [E][r][d_out] stored in the layer's INT4 group-64 format: scale =
+ *     fp16(absmax/7), code = clamp(rint(w/scale), -7, 7) + 8 (FP32 decisions), element 2j in the
+ *     high nibble of byte j -- the moe_hier_resid layout of that matrix kind;
+ *   sigma [E][r] the singular values kept; err [E] (nullable) ||W_i - (base + B A^T)||_F / ||W_i||_F
+ *     with A, B dequantised from the stored codes (FP64).
+ * Shapes: W [E][d_out][d_in] BF16 (device), omega [d_in][sketch] FP32 (device), group_map_host
+ * [E] int32 (host, exactly E/G experts per group), base [G][d_out][d_in] BF16 (device);
+ * At_f32 [E][r][d_in], Bt_f32 [E][r][d_out] FP32 (device, nullable): the factors before
+ * quantisation.  Limits: E % G == 0, E <= 256, d_in and d_out multiples of 128, 1 <= rank <= 32,
+ * rank < sketch <= 64, 0 <= power_iters <= 16.  MOE_ERR_INVALID / _WORKSPACE as elsewhere. */
+typedef struct {
+  int32_t E, G;
+  int32_t d_out, d_in;   /* the matrix kind's shape: W_i is [d_out][d_in]                        */
+  int32_t rank;          /* r kept                                                               */
+  int32_t sketch;        /* l = r + oversampling, columns of the test matrix                      */
+  int32_t power_iters;   /* subspace iterations                                                  */
+} moe_hier_compress_desc;
+
+size_t moe_hier_compress_workspace_size(const moe_hier_compress_desc* desc, int* status_out);
+int moe_hier_compress(const moe_hier_compress_desc* desc, const void* w, const int32_t* group_map_host,
+                      const float* omega, void* base, void* A_codes, void* A_scales, void* B_codes,
+                      void* B_scales, float* sigma, double* err, float* At_f32, float* Bt_f32,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/* INT4 group-64 quantisation alone (the rule of moe_hier_compress): v [rows][n] FP32 (device,
+ * n % 64 == 0) -> codes [rows][n/2] uint8, scales [rows][n/64] FP16 (device). */
+int moe_hier_quantise_int4(const float* v, int64_t rows, int32_t n, void* codes, void* scales, void* stream);
+
 /* Test aids.  The pages have no counterpart; neither changes a result of the calls above.
  *
  * moe_hier_debug_set_wait sets, for the calling process, the limit of the grid-wide wait inside

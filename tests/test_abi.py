@@ -100,3 +100,15 @@ def test_test_aids_validate_on_the_host(L):
     rc = L.lib.moe_hier_debug_route_tc(ctypes.byref(d), fake, fake, None, fake, gm.ctypes.data, fake, fake,
                                        1 << 30, None)
     assert rc == L.MOE_ERR_UNSUPPORTED
+
+
+def test_binding_arity_matches_header(L):
+    """Every ctypes binding declares as many arguments as the header's prototype (a missing one
+    shifts the stream handle and crashes the host)."""
+    src = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "moehier.h")).read(), flags=re.S)
+    protos = re.findall(r"\b(?:int|size_t|const char\*)\s+(moe_hier_\w+)\s*\(([^;]*?)\);", src, flags=re.S)
+    assert len(protos) >= 14
+    for name, params in protos:
+        params = params.strip()
+        n = 0 if params in ("", "void") else len(params.split(","))
+        assert len(getattr(L.lib, name).argtypes) == n, name
