@@ -505,6 +505,201 @@ def run_ours(args, rank, world, local_rank):
     return res, inp
 
 
+# ------------------------------------------------------------------ the compression step (--config compress_*)
+def run_compress(args):
+    """Times moe_hier_compress on every matrix kind of the dense experts (gate, up, down), inputs
+    resident; reports matrices compressed per second and the FP32 rate of the tall-skinny
+    products (the bulk of the work) against the CUDA cores' FP32 peak (148 SMs x 128 FMA lanes x 2
+    FLOP x the maximum SM clock)."""
+    import torch
+
+    from compressed_expert_two_b300 import _lib as L
+    from synth import COMPRESS_CONFIGS, make_dense_experts
+    cfg = COMPRESS_CONFIGS[args.config]
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    peaks, peak_src = load_peaks()
+    sm_mhz = peaks.get("sm_max_mhz", 2032.0)
+    fp32_peak = 148 * 128 * 2 * sm_mhz * 1e6 / 1e12
+    inp = make_dense_experts(cfg)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    per_kind, kern_ms, tot_ms, tsmm_flops, errs = {}, {}, 0.0, 0.0, []
+    for kind in ("gate", "up", "down"):
+        d_in, d_out = (cfg.d, cfg.f) if kind != "down" else (cfg.f, cfg.d)
+        E, G, r = cfg.E, cfg.G, cfg.r
+        desc = L.MoeHierCompressDesc(E=E, G=G, d_out=d_out, d_in=d_in, rank=r, sketch=cfg.l,
+                                     power_iters=cfg.power_iters)
+        W = inp[kind]["W"].to(dev)
+        om = inp[kind]["omega"].to(dev)
+        gm = inp["group_map"].to(torch.int32)
+        o = [torch.empty(G, d_out, d_in, dtype=torch.bfloat16, device=dev),
+             torch.empty(E, r, d_in // 2, dtype=torch.uint8, device=dev),
+             torch.empty(E, r, d_in // 64, dtype=torch.float16, device=dev),
+             torch.empty(E, r, d_out // 2, dtype=torch.uint8, device=dev),
+             torch.empty(E, r, d_out // 64, dtype=torch.float16, device=dev),
+             torch.empty(E, r, dtype=torch.float32, device=dev), torch.empty(E, dtype=torch.float64, device=dev)]
+        nws = L.moe_hier_compress_workspace_size(desc)
+        ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+
+        def call():
+            L.moe_hier_compress(desc, W, gm, om, *o, None, None, ws, nws, stream.cuda_stream)
+
+        for _ in range(max(args.warmup, 3)):
+            call()
+        torch.cuda.synchronize(dev)
+        probe = [torch.cuda.Event(enable_timing=True) for _ in range(64)]
+        for e in probe:
+            e.record(stream)
+        arr = L.moe_hier_profile_begin([e.cuda_event for e in probe])
+        call()
+        names = L.moe_hier_profile_end()
+        del arr
+        torch.cuda.synchronize(dev)
+        for j, nm in enumerate(names[:63]):
+            kern_ms[nm] = kern_ms.get(nm, 0.0) + probe[j].elapsed_time(probe[j + 1])
+        K = max(1, min(args.steps, 20))
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            call()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        tot_ms += ms
+        passes = 2 * cfg.power_iters + 2
+        tsmm_flops += passes * 2.0 * 64 * d_out * d_in * E
+        errs += o[6].cpu().tolist()
+        per_kind[kind] = {"ms": round(ms, 3), "d_out": d_out, "d_in": d_in}
+    tsmm_ms = sum(v for k, v in kern_ms.items() if k.startswith("cmp_tsmm"))
+    achieved = tsmm_flops / (tsmm_ms / 1e3) / 1e12 if tsmm_ms > 0 else 0.0
+    n_mat = 3 * cfg.E
+    res = {"metric": "compression: dense expert matrices compressed per second (group-mean base, rank-r TSVD, "
+                     "INT4 g64 factors)",
+           "value": round(n_mat / (tot_ms / 1e3), 2), "unit": "matrices/s", "n_gpus": 1,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_ms, 3), "higher_is_better": True,
+           "dtype": "f32", "data": "synthetic dense experts (shared group part + rank-r deviation + 1% noise)",
+           "config": {"workload": f"{cfg.name}: E={cfg.E} G={cfg.G} d_model={cfg.d} d_ff={cfg.f} r={cfg.r} "
+                                  f"sketch={cfg.l} power_iters={cfg.power_iters}", "per_kind": per_kind,
+                      "l2": "flushed between timed calls (256 MiB write)"},
+           "roofline": {"bound": "alu", "kernel": "cmp_tsmm (tall-skinny products, FP32 CUDA cores)",
+                        "achieved": round(achieved, 2), "peak": round(fp32_peak, 1), "unit": "TFLOP/s",
+                        "frac": round(achieved / fp32_peak, 4),
+                        "peak_source": "148 SMs x 128 FP32 lanes x 2 FLOP x sm_max_mhz (derived, not measured)"},
+           "kernels_ms": {k: round(v, 4) for k, v in kern_ms.items()},
+           "reconstruction_error": {"mean": round(statistics.mean(errs), 5), "max": round(max(errs), 5)},
+           "gpu_launches": len(names)}
+    if not args.no_cpu_baseline:
+        import numpy as np
+
+        from oracle import compress as C
+        W0 = inp["gate"]["W"][:cfg.K].float().numpy()
+        t0 = time.perf_counter()
+        C.compress_matrix(W0, np.zeros(cfg.K, dtype=np.int64), 1, cfg.r)
+        el = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": round(cfg.K / el, 3), "unit": "matrices/s", "cores": cpu_cores(),
+                               "kind": "oracle", "sample": f"the gate matrices of one group ({cfg.K} experts, "
+                                                           f"FP64 SVD each) in {el:.1f} s"}
+    return res
+
+
+# ------------------------------------------------------------------ idle-group offload (--config decode_offload)
+def run_offload(args, slots: int = 4):
+    """Steps of a few tokens each over distinct inputs, the group bases in pinned host memory and
+    `slots` of the G groups cached on the device; batch i+1 is routed and its missing groups
+    copied while batch i's FFN runs.  Reports tokens/s (wall clock over the steps, the host's
+    per-step synchronisation included), the resident-weight rate on the same inputs, the cache hit
+    rate, bytes copied per step and the host-to-device rate against a pinned 1 GiB copy."""
+    import torch
+
+    from compressed_expert_two_b300 import _lib as L
+    from compressed_expert_two_b300.layer import DeviceLayer
+    from synth import CONFIGS, make_inputs
+    cfg = CONFIGS[args.config]
+    dev = torch.device("cuda", 0)
+    inp = make_inputs(cfg)
+    layer = DeviceLayer(inp, device=dev)
+    host = {m: inp["w_" + m].contiguous().pin_memory() for m in ("gate", "up", "down")}
+    cache = {m: torch.empty((slots,) + tuple(inp["w_" + m].shape[1:]), dtype=torch.bfloat16, device=dev)
+             for m in ("gate", "up", "down")}
+    off = L.Offload(layer.desc, host["gate"], host["up"], host["down"], cache["gate"], cache["up"],
+                    cache["down"], slots)
+    gen = torch.Generator().manual_seed(99)
+    n = max(args.steps, 8)
+    xs = [torch.randn(cfg.T, cfg.d, generator=gen).to(torch.bfloat16).to(dev) for _ in range(n + args.warmup)]
+    copy = torch.cuda.Stream(dev)
+    streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    wss = [layer.ws, torch.zeros_like(layer.ws)]
+    keep = []
+
+    def step(i, x):
+        s = streams[i & 1]
+        ws = wss[i & 1]
+        o = layer.new_outputs()
+        pr = {"row_asg": torch.empty(cfg.T * cfg.kg, dtype=torch.int32, device=dev),
+              "row_begin": torch.empty(cfg.G + 1, dtype=torch.int32, device=dev)}
+        y = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dev)
+        L.moe_hier_route(layer.desc, x, layer.w_group, layer.b_group, layer.w_expert, layer.group_map, o["gidx"],
+                         o["eidx"], o["gate"], ws, layer.ws_bytes, s.cuda_stream)
+        L.moe_hier_permute(layer.desc, layer.group_map, o["eidx"], None, None, None, None, None, pr["row_asg"],
+                           None, pr["row_begin"], ws, layer.ws_bytes, s.cuda_stream)
+        hit = off.groups_hit(pr["row_begin"], s.cuda_stream)
+        off.require(hit, copy.cuda_stream)
+        off.ffn(layer.desc, x, layer.group_map, layer.resid, o["eidx"], o["gate"], pr["row_asg"], pr["row_begin"],
+                y, ws, layer.ws_bytes, s.cuda_stream)
+        keep.append((o, pr, y))
+        return int(hit.sum())
+
+    for i in range(args.warmup):
+        step(i, xs[n + i])
+    torch.cuda.synchronize(dev)
+    st0 = off.stats()
+    t0 = time.perf_counter()
+    hits_per_step = [step(i, xs[i]) for i in range(n)]
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t0
+    st1 = off.stats()
+    keep.clear()
+    # the same inputs with every base resident (the layer's own forward, graph-free, same host loop)
+    for i in range(3):
+        layer.forward(x=xs[i])
+    torch.cuda.synchronize(dev)
+    t1 = time.perf_counter()
+    for i in range(n):
+        layer.forward(x=xs[i], routing_out=False)
+    torch.cuda.synchronize(dev)
+    wall_res = time.perf_counter() - t1
+    # pinned host -> device copy rate (1 GiB, best of 3)
+    hbuf = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    best = 0.0
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        dbuf.copy_(hbuf, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize(dev)
+        best = max(best, (1 << 30) / (a.elapsed_time(b) / 1e3) / 1e9)
+    off.close()
+    copied = st1["bytes_copied"] - st0["bytes_copied"]
+    misses, hits = st1["misses"] - st0["misses"], st1["hits"] - st0["hits"]
+    group_bytes = 3 * cfg.d * cfg.f * 2
+    return {"metric": "idle-group offload: MoE-layer fwd tokens/s with the group bases in pinned host memory",
+            "value": round(cfg.T * n / wall, 1), "unit": "tokens/s", "n_gpus": 1, "steps": n, "warmup": args.warmup,
+            "ms_per_step": round(wall / n * 1e3, 3), "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic (seeded; distinct inputs per step)",
+            "config": {"workload": workload_name(cfg) + f", {slots} of {cfg.G} group bases cached on the device",
+                       "T": cfg.T, "slots": slots, "G": cfg.G,
+                       "device_bytes_bases": slots * group_bytes, "resident_bytes_bases": cfg.G * group_bytes},
+            "resident": {"value": round(cfg.T * n / wall_res, 1), "unit": "tokens/s",
+                         "ms_per_step": round(wall_res / n * 1e3, 3)},
+            "cache": {"groups_hit_per_step": round(statistics.mean(hits_per_step), 2),
+                      "hit_rate": round(hits / max(hits + misses, 1), 4),
+                      "bytes_copied_per_step": round(copied / n), "h2d_gbs": round(copied / wall / 1e9, 2),
+                      "pinned_h2d_peak_gbs": round(best, 2), "h2d_frac": round(copied / wall / 1e9 / best, 4)},
+            "timing": "wall clock over the steps (host synchronisation per step for the hit groups included)"}
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", 0))
@@ -515,6 +710,13 @@ def main():
         if rank != 0:
             return 0
         return run_reference(args)
+
+    if args.config.startswith("compress_") or args.config == "decode_offload":
+        if world > 1 and rank != 0:
+            return 0
+        res = run_compress(args) if args.config.startswith("compress_") else run_offload(args)
+        print(json.dumps(res), flush=True)
+        return 0
 
     import torch
     import torch.distributed as dist

@@ -43,7 +43,9 @@ EXPORTS = ["moe_hier_workspace_size", "moe_hier_route", "moe_hier_permute", "moe
            "moe_hier_combine", "moe_hier_forward", "moe_hier_get_status", "moe_hier_status_string",
            "moe_hier_last_cuda_error", "moe_hier_profile_begin", "moe_hier_profile_end",
            "moe_hier_debug_set_wait", "moe_hier_debug_route_tc", "moe_hier_permute_noalloc",
-           "moe_hier_compress_workspace_size", "moe_hier_compress", "moe_hier_quantise_int4"]
+           "moe_hier_compress_workspace_size", "moe_hier_compress", "moe_hier_quantise_int4",
+           "moe_hier_offload_create", "moe_hier_offload_destroy", "moe_hier_groups_hit",
+           "moe_hier_offload_require", "moe_hier_ffn_offload", "moe_hier_offload_stats"]
 
 
 class MoeError(RuntimeError):
@@ -79,6 +81,13 @@ def _load() -> ctypes.CDLL:
     lib.moe_hier_compress_workspace_size.restype = S
     lib.moe_hier_compress.argtypes = [C] + [P] * 13 + [S, P]
     lib.moe_hier_quantise_int4.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P, P, P]
+    lib.moe_hier_offload_create.argtypes = [D, P, P, P, P, P, P, ctypes.c_int32, ctypes.POINTER(P)]
+    lib.moe_hier_offload_destroy.argtypes = [P]
+    lib.moe_hier_groups_hit.argtypes = [D, P, P, P]
+    lib.moe_hier_offload_require.argtypes = [P, P, P, P]
+    lib.moe_hier_ffn_offload.argtypes = [P, D, P, P, Rp, P, P, P, P, P, P, S, P]
+    U64p = ctypes.POINTER(ctypes.c_uint64)
+    lib.moe_hier_offload_stats.argtypes = [P, U64p, U64p, U64p, P]
     lib.moe_hier_debug_set_wait.argtypes = [ctypes.c_uint64, I]
     lib.moe_hier_debug_route_tc.argtypes = [D, P, P, P, P, P, P, P, S, P]
     lib.moe_hier_permute_noalloc.argtypes = [D] + [P] * 11
@@ -200,6 +209,52 @@ def moe_hier_compress(desc, w, group_map_host, omega, base, A_codes, A_scales, B
 
 def moe_hier_quantise_int4(v, rows: int, n: int, codes, scales, stream):
     _check("moe_hier_quantise_int4", lib.moe_hier_quantise_int4(_p(v), rows, n, _p(codes), _p(scales), stream))
+
+
+class Offload:
+    """Handle of the idle-group offload manager (moe_hier_offload_*): the caller's pinned host
+    bases and device cache, passed through unchanged."""
+
+    def __init__(self, desc, w_gate_host, w_up_host, w_down_host, cache_gate, cache_up, cache_down, slots):
+        self.h = ctypes.c_void_p()
+        self.desc = desc
+        _check("moe_hier_offload_create", lib.moe_hier_offload_create(
+            ctypes.byref(desc), _p(w_gate_host), _p(w_up_host), _p(w_down_host), _p(cache_gate), _p(cache_up),
+            _p(cache_down), slots, ctypes.byref(self.h)))
+        self.slots = slots
+
+    def groups_hit(self, row_begin, stream):
+        import numpy as np
+        hit = np.zeros(self.desc.G, dtype=np.int32)
+        _check("moe_hier_groups_hit", lib.moe_hier_groups_hit(ctypes.byref(self.desc), _p(row_begin),
+                                                              hit.ctypes.data, stream))
+        return hit
+
+    def require(self, hit, copy_stream) -> int:
+        import numpy as np
+        hit = np.ascontiguousarray(hit, dtype=np.int32)
+        n = ctypes.c_int32(0)
+        _check("moe_hier_offload_require", lib.moe_hier_offload_require(self.h, hit.ctypes.data, ctypes.byref(n),
+                                                                        copy_stream))
+        return n.value
+
+    def ffn(self, desc, x, group_map_host, resid, eidx, gate, row_asg, row_begin, y_rows, ws, ws_bytes, stream):
+        _check("moe_hier_ffn_offload", lib.moe_hier_ffn_offload(
+            self.h, ctypes.byref(desc), _p(x), _p(group_map_host), ctypes.byref(resid), _p(eidx), _p(gate),
+            _p(row_asg), _p(row_begin), _p(y_rows), _p(ws), ws_bytes, stream))
+
+    def stats(self):
+        import numpy as np
+        b, m, h = ctypes.c_uint64(), ctypes.c_uint64(), ctypes.c_uint64()
+        sg = np.zeros(self.slots, dtype=np.int32)
+        _check("moe_hier_offload_stats", lib.moe_hier_offload_stats(self.h, ctypes.byref(b), ctypes.byref(m),
+                                                                    ctypes.byref(h), sg.ctypes.data))
+        return {"bytes_copied": b.value, "misses": m.value, "hits": h.value, "slot_group": sg.tolist()}
+
+    def close(self):
+        if self.h:
+            _check("moe_hier_offload_destroy", lib.moe_hier_offload_destroy(self.h))
+            self.h = ctypes.c_void_p()
 
 
 def moe_hier_get_status(ws, stream) -> int:

@@ -485,6 +485,33 @@ const char* moe_hier_status_string(int status) {
 
 }  // extern "C"
 
+// FFN whose base matrices sit in `wslots` group slots (group g in slot wslot[g]): the offload
+// cache (offload.cu).  Tensor-core layers only.
+namespace moe {
+int ffn_with_slots(const moe_hier_desc* desc, const void* x, const int32_t* group_map_host, const void* w_gate,
+                   const void* w_up, const void* w_down, int wslots, const uint8_t* wslot,
+                   const moe_hier_resid* resid, const int32_t* eidx, const float* gate, const int32_t* row_asg,
+                   const int32_t* row_begin, void* y_rows, void* ws, size_t ws_bytes, void* stream) {
+  LayerArgs a;
+  if (!group_map_host) return MOE_ERR_INVALID;
+  int st = validate(desc, group_map_host, &a);
+  if (st != MOE_OK) return st;
+  if (a.T > 0 && (!x || !w_gate || !w_up || !w_down || !eidx || !gate || !row_asg || !row_begin || !y_rows ||
+                  !resid_ok(a, resid)))
+    return MOE_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) || !aligned16(y_rows))
+    return MOE_ERR_INVALID;
+  const Plan p = make_plan(a);
+  if (!p.tc) return MOE_ERR_UNSUPPORTED;
+  if ((st = check_ws(p, ws, ws_bytes)) != MOE_OK) return st;
+  a.wslots = wslots;
+  for (int g = 0; g < a.G; ++g) a.tab.wslot[g] = wslot[g];
+  prof_start((cudaStream_t)stream);
+  return cuda_status(run_ffn(a, p, ws, x, w_gate, w_up, w_down, resid, eidx, gate, row_asg, row_begin, y_rows,
+                             nullptr, (cudaStream_t)stream));
+}
+}  // namespace moe
+
 // ------------------------------------------------------------------------------------------
 // Permutation without a workspace argument.
 //

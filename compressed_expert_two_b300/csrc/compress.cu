@@ -17,7 +17,8 @@
 //      tall and skinny, l <= 64 columns, and the two BF16 streams bound them).
 //   3. INT4 group-64 codes and FP16 scales of the rank-major rows A^T, B^T (cmp_quant_kernel).
 //   4. ||W_i - (base + B_dq A_dq^T)||_F / ||W_i||_F from the stored codes (cmp_err_kernel).
-// The small eigenproblems (l x l, FP64) run as cyclic Jacobi sweeps in one CTA per expert.
+// The small eigenproblems (64 x 64, FP32 from FP64 Grams) run as cyclic Jacobi sweeps in one CTA
+// per expert.
 #include <math.h>
 
 #include "common.cuh"
@@ -226,11 +227,14 @@ __global__ void __launch_bounds__(256) cmp_gram_kernel(const float* __restrict__
 }
 
 // ------------------------------------------------------------------------------------------
-// 2c. Symmetric 64 x 64 eigenproblem (cyclic Jacobi, FP64, one CTA of 256 threads per expert).
-// Rotations of 32 disjoint index pairs (round-robin order) per step, 63 steps per sweep, until
-// the off-diagonal mass is below 1e-28 of the total (at most 30 sweeps).  Then, by mode:
-//   ORTH: M = V D^{-1/2} (columns of eigenvalues below 1e-12 of the largest set to zero), the
-//         transform that orthonormalises Y:  Q = Y M;
+// 2c. Symmetric 64 x 64 eigenproblem (cyclic Jacobi in FP32 -- the FP64 units of this part run at
+// a small fraction of the FP32 rate -- one CTA of 256 threads per expert; the Gram comes in FP64
+// and is rounded once).  Rotations of 32 disjoint index pairs (round-robin order) per step, 63
+// steps per sweep, until the off-diagonal mass is below 1e-13 of the total (at most 20 sweeps).
+// Then, by mode:
+//   ORTH: M = V D^{-1/2}, the transform that orthonormalises Y: Q = Y M (directions whose
+//         eigenvalue is below 1e-6 of the largest, which FP32 cannot resolve, are dropped: their
+//         columns of M are zero; the next orthonormalisation pass sees a clean basis);
 //   SVD:  eigenvalues descending, sigma_k = sqrt(lambda_k) for k < r, and the r-column transforms
 //         P_B = U_r S^{1/2} and P_A = U_r S^{-1/2}, each column's sign fixed so that its largest
 //         component is positive.
@@ -241,58 +245,50 @@ __global__ void __launch_bounds__(256) cmp_eig_kernel(const double* __restrict__
   pdl_wait();
   pdl_trigger();
   constexpr int N = kCL;
-  extern __shared__ double eig_smem[];                 // A [N][N + 1], V [N][N + 1] (66.5 KB)
-  double (*A)[N + 1] = reinterpret_cast<double (*)[N + 1]>(eig_smem);
-  double (*V)[N + 1] = reinterpret_cast<double (*)[N + 1]>(eig_smem + N * (N + 1));
-  __shared__ double cs[N / 2][2];
+  __shared__ float A[N][N + 1];
+  __shared__ float V[N][N + 1];
+  __shared__ float cs[N / 2][2];
   __shared__ int pr[N / 2][2];
-  __shared__ double red[256];
+  __shared__ float red[2][256];
   __shared__ int order[N];
-  __shared__ double lam[N];
+  __shared__ float lam[N];
   const int e = blockIdx.x, tid = threadIdx.x;
   const double* ge = gram + (size_t)e * N * N;
   for (int i = tid; i < N * N; i += 256) {
     const int a = i / N, b = i % N;
-    A[a][b] = 0.5 * (ge[a * N + b] + ge[b * N + a]);   // exact symmetry
-    V[a][b] = a == b ? 1.0 : 0.0;
+    A[a][b] = (float)(0.5 * (ge[a * N + b] + ge[b * N + a]));   // exact symmetry
+    V[a][b] = a == b ? 1.f : 0.f;
   }
   __syncthreads();
-  for (int sweep = 0; sweep < 30; ++sweep) {
-    double off = 0.0, tot = 0.0;
+  for (int sweep = 0; sweep < 20; ++sweep) {
+    float off = 0.f, tot = 0.f;
     for (int i = tid; i < N * N; i += 256) {
-      const double v = A[i / N][i % N] * A[i / N][i % N];
+      const float v = A[i / N][i % N] * A[i / N][i % N];
       tot += v;
       if (i / N != i % N) off += v;
     }
-    red[tid] = off;
+    red[0][tid] = off;
+    red[1][tid] = tot;
     __syncthreads();
     for (int s = 128; s > 0; s >>= 1) {
-      if (tid < s) red[tid] += red[tid + s];
+      if (tid < s) { red[0][tid] += red[0][tid + s]; red[1][tid] += red[1][tid + s]; }
       __syncthreads();
     }
-    const double off_all = red[0];
+    const float off_all = red[0][0], tot_all = red[1][0];
     __syncthreads();
-    red[tid] = tot;
-    __syncthreads();
-    for (int s = 128; s > 0; s >>= 1) {
-      if (tid < s) red[tid] += red[tid + s];
-      __syncthreads();
-    }
-    const double tot_all = red[0];
-    __syncthreads();
-    if (off_all <= 1e-28 * tot_all || tot_all == 0.0) break;
+    if (off_all <= 1e-13f * tot_all || tot_all == 0.f) break;
     for (int step = 0; step < N - 1; ++step) {
       if (tid < N / 2) {
         int p, q;
         if (tid == 0) { p = step; q = N - 1; }
         else { p = (step + tid) % (N - 1); q = (step - tid + (N - 1)) % (N - 1); }
         if (p > q) { const int t = p; p = q; q = t; }
-        const double apq = A[p][q], app = A[p][p], aqq = A[q][q];
-        double c = 1.0, s = 0.0;
-        if (apq != 0.0 && fabs(apq) > 1e-300) {
-          const double tau = (aqq - app) / (2.0 * apq);
-          const double t = (tau >= 0.0 ? 1.0 : -1.0) / (fabs(tau) + sqrt(1.0 + tau * tau));
-          c = 1.0 / sqrt(1.0 + t * t);
+        const float apq = A[p][q], app = A[p][p], aqq = A[q][q];
+        float c = 1.f, s = 0.f;
+        if (apq != 0.f) {
+          const float tau = (aqq - app) / (2.f * apq);
+          const float t = (tau >= 0.f ? 1.f : -1.f) / (fabsf(tau) + sqrtf(1.f + tau * tau));
+          c = rsqrtf(1.f + t * t);
           s = t * c;
         }
         pr[tid][0] = p; pr[tid][1] = q; cs[tid][0] = c; cs[tid][1] = s;
@@ -301,7 +297,7 @@ __global__ void __launch_bounds__(256) cmp_eig_kernel(const double* __restrict__
       // rows: A <- J^T A
       for (int i = tid; i < (N / 2) * N; i += 256) {
         const int k = i / N, col = i % N, p = pr[k][0], q = pr[k][1];
-        const double c = cs[k][0], s = cs[k][1], ap = A[p][col], aq = A[q][col];
+        const float c = cs[k][0], s = cs[k][1], ap = A[p][col], aq = A[q][col];
         A[p][col] = c * ap - s * aq;
         A[q][col] = s * ap + c * aq;
       }
@@ -309,11 +305,11 @@ __global__ void __launch_bounds__(256) cmp_eig_kernel(const double* __restrict__
       // columns: A <- A J, V <- V J
       for (int i = tid; i < (N / 2) * N; i += 256) {
         const int k = i / N, row = i % N, p = pr[k][0], q = pr[k][1];
-        const double c = cs[k][0], s = cs[k][1];
-        const double ap = A[row][p], aq = A[row][q];
+        const float c = cs[k][0], s = cs[k][1];
+        const float ap = A[row][p], aq = A[row][q];
         A[row][p] = c * ap - s * aq;
         A[row][q] = s * ap + c * aq;
-        const double vp = V[row][p], vq = V[row][q];
+        const float vp = V[row][p], vq = V[row][q];
         V[row][p] = c * vp - s * vq;
         V[row][q] = s * vp + c * vq;
       }
@@ -329,29 +325,29 @@ __global__ void __launch_bounds__(256) cmp_eig_kernel(const double* __restrict__
   }
   __syncthreads();
   float* xe = xform + (size_t)e * N * N;
-  const double lmax = fmax(lam[order[0]], 0.0);
+  const float lmax = fmaxf(lam[order[0]], 0.f);
   if (mode == 0) {
     for (int i = tid; i < N * N; i += 256) {
       const int row = i / N, col = i % N;
-      const double l = lam[col];
-      xe[i] = (float)(l > 1e-12 * lmax && l > 0.0 ? V[row][col] / sqrt(l) : 0.0);
+      const float l = lam[col];
+      xe[i] = l > 1e-6f * lmax && l > 0.f ? V[row][col] * rsqrtf(l) : 0.f;
     }
   } else {
     for (int i = tid; i < N * N; i += 256) xe[i] = 0.f;
     __syncthreads();
     if (tid < r) {
       const int col = order[tid];
-      const double sg = sqrt(fmax(lam[col], 0.0));
+      const float sg = sqrtf(fmaxf(lam[col], 0.f));
       int big = 0;
       for (int row = 1; row < N; ++row)
-        if (fabs(V[row][col]) > fabs(V[big][col])) big = row;
-      const double sgn = V[big][col] < 0.0 ? -1.0 : 1.0;
-      const double rb = sqrt(sg), ra = sg > 0.0 ? 1.0 / sqrt(sg) : 0.0;
+        if (fabsf(V[row][col]) > fabsf(V[big][col])) big = row;
+      const float sgn = V[big][col] < 0.f ? -1.f : 1.f;
+      const float rb = sqrtf(sg), ra = sg > 0.f ? rsqrtf(sg) : 0.f;
       for (int row = 0; row < N; ++row) {
-        xe[row * N + tid] = (float)(sgn * V[row][col] * rb);
-        xe[row * N + 32 + tid] = (float)(sgn * V[row][col] * ra);
+        xe[row * N + tid] = sgn * V[row][col] * rb;
+        xe[row * N + 32 + tid] = sgn * V[row][col] * ra;
       }
-      sigma[(size_t)e * r + tid] = (float)sg;
+      sigma[(size_t)e * r + tid] = sg;
     }
   }
 }
@@ -582,11 +578,8 @@ cudaError_t launch_compress(const CmpArgs& c, const void* W, const float* omega,
     prof_mark("cmp_gram", st);
     return cudaGetLastError();
   };
-  constexpr size_t eig_smem = 2 * kCL * (kCL + 1) * sizeof(double);
-  static std::atomic<uint64_t> eig_attr{0};
-  if ((e = smem_attr_once(cmp_eig_kernel, eig_smem, eig_attr)) != cudaSuccess) return e;
   auto eig = [&](int mode) {
-    launch_pdl(cmp_eig_kernel, dim3(E), dim3(256), eig_smem, st, (const double*)gram, mode, r, xf, sigma);
+    launch_pdl(cmp_eig_kernel, dim3(E), dim3(256), 0, st, (const double*)gram, mode, r, xf, sigma);
     prof_mark("cmp_eig", st);
     return cudaGetLastError();
   };

@@ -221,6 +221,50 @@ int moe_hier_compress(const moe_hier_compress_desc* desc, const void* w, const i
  * n % 64 == 0) -> codes [rows][n/2] uint8, scales [rows][n/64] FP16 (device). */
 int moe_hier_quantise_int4(const float* v, int64_t rows, int32_t n, void* codes, void* scales, void* stream);
 
+/* ---------------------------------------------------------------------------------------------
+ * Idle-group offload ("Breaking the MoE LLM Trilemma", key design 4: groups the current work does
+ * not use are moved to CPU memory and brought back when needed).  The caller keeps the three base
+ * arrays of every group in PINNED host memory (w_gate_host, w_up_host [G][f][d], w_down_host
+ * [G][d][f], BF16, e.g. from cudaHostAlloc or cudaHostRegister) and provides a device cache of
+ * `slots` groups (cache_gate, cache_up [slots][f][d], cache_down [slots][d][f]).  The handle is
+ * host memory only (plus 2 * slots CUDA events); it belongs to the device current at creation.
+ * BF16 layers with INT4 residuals (the tensor-core path) only: MOE_ERR_UNSUPPORTED otherwise.
+ *
+ * Per batch, with x, the routers and the residual factors resident as usual:
+ *   moe_hier_route, moe_hier_permute      (compute stream; row_begin as usual)
+ *   moe_hier_groups_hit                   copies row_begin to the host and synchronises that
+ *                                         stream: hit_host[g] = 1 if the batch has rows in g;
+ *   moe_hier_offload_require              every hit group not in the cache gets a slot (an empty
+ *                                         one, else the least recently used slot whose group is
+ *                                         not hit) and its three matrices are copied host->device
+ *                                         on copy_stream, after the last FFN that read that slot
+ *                                         has finished; *copied (nullable) = groups copied.
+ *                                         MOE_ERR_INVALID if the batch hits more groups than slots;
+ *   moe_hier_ffn_offload                  moe_hier_ffn with the bases read from the cache: the
+ *                                         stream waits for the hit groups' copies, then the FFN
+ *                                         kernels run; a group that was not required reads zeros.
+ *   moe_hier_combine                      as usual.
+ * The next batch's route / permute / groups_hit / require may be issued while this batch's FFN
+ * runs (the copy stream waits on the slots' last readers).  One handle is used from one host
+ * thread at a time.  Results equal moe_hier_ffn's on resident bases bit for bit. */
+typedef struct moe_hier_offload moe_hier_offload;
+
+int moe_hier_offload_create(const moe_hier_desc* desc, const void* w_gate_host, const void* w_up_host,
+                            const void* w_down_host, void* cache_gate, void* cache_up, void* cache_down,
+                            int32_t slots, moe_hier_offload** out);
+int moe_hier_offload_destroy(moe_hier_offload* handle);
+int moe_hier_groups_hit(const moe_hier_desc* desc, const int32_t* row_begin, int32_t* hit_host, void* stream);
+int moe_hier_offload_require(moe_hier_offload* handle, const int32_t* hit_host, int32_t* copied,
+                             void* copy_stream);
+int moe_hier_ffn_offload(moe_hier_offload* handle, const moe_hier_desc* desc, const void* x,
+                         const int32_t* group_map_host, const moe_hier_resid* resid, const int32_t* eidx,
+                         const float* gate, const int32_t* row_asg, const int32_t* row_begin, void* y_rows,
+                         void* ws, size_t ws_bytes, void* stream);
+/* Totals since creation: bytes copied host->device, groups copied (misses), hit groups found in
+ * the cache (hits); slot_group (nullable, [slots]) = the group each slot holds (-1: empty). */
+int moe_hier_offload_stats(const moe_hier_offload* handle, uint64_t* bytes_copied, uint64_t* misses,
+                           uint64_t* hits, int32_t* slot_group);
+
 /* Test aids.  The pages have no counterpart; neither changes a result of the calls above.
  *
  * moe_hier_debug_set_wait sets, for the calling process, the limit of the grid-wide wait inside

@@ -85,6 +85,10 @@ CONFIGS: Dict[str, MoEConfig] = {
                         dtype="bf16", resid="int4", group_map="contiguous", seed=4),
 }
 CONFIG_ORDER = ["tiny_f32", "small_bf16_int4", "mixtral_prefill", "finegrained_skewed", "decode"]
+# Decode with 4 tokens per step and skewed group loads: most groups sit idle in any one step,
+# the case the idle-group offload serves (bases of 4 of the 8 groups cached on the device).
+CONFIGS["decode_offload"] = MoEConfig("decode_offload", T=4, d=4096, f=14336, E=32, G=8, kg=1, ke=2, r=16,
+                                      dtype="bf16", resid="int4", group_map="contiguous", seed=4, zipf_s=1.2)
 # The other reading of the fine-grained workload: top-3 experts over the union of the 2 chosen groups.
 CONFIGS["finegrained_across"] = CONFIGS["finegrained_skewed"].replace(name="finegrained_across", route="across")
 
