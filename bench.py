@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--prepared", action="store_true",
+                    help="residual stacks built once (moe_hier_prepare), steps call moe_hier_forward_prepared")
     ap.add_argument("--tokens", type=int, default=0,
                     help="profiling aid: run the workload's layer on this many tokens instead of its T")
     return ap.parse_args()
@@ -317,6 +319,9 @@ def run_ours(args, rank, world, local_rank):
     layer = DeviceLayer(inp, device=dev)
     out = layer.new_outputs()
     stream = torch.cuda.current_stream(dev)
+    if args.prepared:
+        layer.prepare()
+        layer.forward = layer.forward_prepared       # every step below runs the prepared path
 
     for _ in range(max(args.warmup, 3)):
         layer.forward(out=out)
@@ -497,8 +502,9 @@ def run_ours(args, rank, world, local_rank):
                             "copies on their own streams overlap the neighbouring steps' forwards; L2 "
                             "flushed before every forward"},
         "gpu_launches": n_k * K,
-        "timing": "graph replay of one moe_hier_forward per step (kernels_ms: per-kernel device time, "
-                  "launches queued behind a sleep kernel)",
+        "timing": ("graph replay of one moe_hier_forward_prepared per step (residual stacks built once "
+                   "before the timed region)" if args.prepared else "graph replay of one moe_hier_forward per step")
+                  + " (kernels_ms: per-kernel device time, launches queued behind a sleep kernel)",
         "clocks": clk,
         "wall_s_timed": round(wall, 3),
     }

@@ -45,7 +45,8 @@ EXPORTS = ["moe_hier_workspace_size", "moe_hier_route", "moe_hier_permute", "moe
            "moe_hier_debug_set_wait", "moe_hier_debug_route_tc", "moe_hier_permute_noalloc",
            "moe_hier_compress_workspace_size", "moe_hier_compress", "moe_hier_quantise_int4",
            "moe_hier_offload_create", "moe_hier_offload_destroy", "moe_hier_groups_hit",
-           "moe_hier_offload_require", "moe_hier_ffn_offload", "moe_hier_offload_stats"]
+           "moe_hier_offload_require", "moe_hier_ffn_offload", "moe_hier_offload_stats",
+           "moe_hier_prepared_size", "moe_hier_prepare", "moe_hier_forward_prepared"]
 
 
 class MoeError(RuntimeError):
@@ -81,6 +82,10 @@ def _load() -> ctypes.CDLL:
     lib.moe_hier_compress_workspace_size.restype = S
     lib.moe_hier_compress.argtypes = [C] + [P] * 13 + [S, P]
     lib.moe_hier_quantise_int4.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P, P, P]
+    lib.moe_hier_prepared_size.argtypes = [D, ctypes.POINTER(ctypes.c_int)]
+    lib.moe_hier_prepared_size.restype = S
+    lib.moe_hier_prepare.argtypes = [D, P, Rp, P, S, P]
+    lib.moe_hier_forward_prepared.argtypes = [D, P, P, P, P, P, P, P, P, Rp, P, S, P, P, P, P, P, P, S, P]
     lib.moe_hier_offload_create.argtypes = [D, P, P, P, P, P, P, ctypes.c_int32, ctypes.POINTER(P)]
     lib.moe_hier_offload_destroy.argtypes = [P]
     lib.moe_hier_groups_hit.argtypes = [D, P, P, P]
@@ -95,7 +100,7 @@ def _load() -> ctypes.CDLL:
     lib.moe_hier_last_cuda_error.restype = ctypes.c_char_p
     for name in EXPORTS:
         if name not in ("moe_hier_workspace_size", "moe_hier_status_string", "moe_hier_last_cuda_error",
-                        "moe_hier_compress_workspace_size"):
+                        "moe_hier_compress_workspace_size", "moe_hier_prepared_size"):
             getattr(lib, name).restype = I
     return lib
 
@@ -160,6 +165,26 @@ def moe_hier_forward(desc, x, w_group, b_group, w_expert, group_map_host, w_gate
         ctypes.byref(desc), _p(x), _p(w_group), _p(b_group), _p(w_expert), _p(group_map_host),
         _p(w_gate), _p(w_up), _p(w_down), ctypes.byref(resid), _p(y), _p(gidx), _p(eidx),
         _p(gate), _p(perm), _p(ws), ws_bytes, stream))
+
+
+def moe_hier_prepared_size(desc: MoeHierDesc) -> int:
+    st = ctypes.c_int(0)
+    n = lib.moe_hier_prepared_size(ctypes.byref(desc), ctypes.byref(st))
+    _check("moe_hier_prepared_size", st.value)
+    return n
+
+
+def moe_hier_prepare(desc, group_map_host, resid, prep, prep_bytes, stream):
+    _check("moe_hier_prepare", lib.moe_hier_prepare(ctypes.byref(desc), _p(group_map_host), ctypes.byref(resid),
+                                                    _p(prep), prep_bytes, stream))
+
+
+def moe_hier_forward_prepared(desc, x, w_group, b_group, w_expert, group_map_host, w_gate, w_up, w_down, resid,
+                              prep, prep_bytes, y, gidx, eidx, gate, perm, ws, ws_bytes, stream):
+    _check("moe_hier_forward_prepared", lib.moe_hier_forward_prepared(
+        ctypes.byref(desc), _p(x), _p(w_group), _p(b_group), _p(w_expert), _p(group_map_host), _p(w_gate),
+        _p(w_up), _p(w_down), ctypes.byref(resid), _p(prep), prep_bytes, _p(y), _p(gidx), _p(eidx), _p(gate),
+        _p(perm), _p(ws), ws_bytes, stream))
 
 
 def moe_hier_profile_begin(event_handles) -> ctypes.Array:

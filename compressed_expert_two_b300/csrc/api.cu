@@ -151,21 +151,49 @@ static bool resid_ok(const LayerArgs& a, const moe_hier_resid* r) {
   return true;
 }
 
-static TcBufs tc_bufs(const Plan& p, void* ws) {
-  return TcBufs{at<__nv_bfloat16>(ws, p.X),   at<__nv_bfloat16>(ws, p.Ain),    at<__half>(ws, p.Bgs),
-                at<__half>(ws, p.Bus),        at<__half>(ws, p.Adt),           at<__nv_bfloat16>(ws, p.Adn),
-                at<__nv_bfloat16>(ws, p.Bdn),
-                at<__half>(ws, p.Ubf), at<__nv_bfloat16>(ws, p.hsum_bf), at<__nv_bfloat16>(ws, p.Vt),
-                at<float>(ws, p.Vpart), at<__half>(ws, p.Ud)};
+// The residual stacks of the tensor-core path (weights only) in a buffer of their own: the
+// regions a workspace would hold, at offsets relative to that buffer.
+struct StackLayout {
+  size_t Ain, Bgs, Bus, Adt, Adn, Bdn, total;
+};
+static StackLayout stack_layout(const Plan& p) {
+  StackLayout l;
+  l.Ain = 0;
+  l.Bgs = p.Bgs - p.Ain;
+  l.Bus = p.Bus - p.Ain;
+  l.Adt = p.Adt - p.Ain;
+  l.Adn = p.Adn - p.Ain;
+  l.Bdn = p.Bdn - p.Ain;
+  l.total = p.Ubf - p.Ain;          // the stacks are consecutive in the plan, Ubf follows them
+  return l;
+}
+
+// Workspace pointers of the tensor-core path; with `prep` the residual stacks come from there.
+static TcBufs tc_bufs(const Plan& p, void* ws, void* prep = nullptr) {
+  TcBufs b{at<__nv_bfloat16>(ws, p.X),   at<__nv_bfloat16>(ws, p.Ain),    at<__half>(ws, p.Bgs),
+           at<__half>(ws, p.Bus),        at<__half>(ws, p.Adt),           at<__nv_bfloat16>(ws, p.Adn),
+           at<__nv_bfloat16>(ws, p.Bdn),
+           at<__half>(ws, p.Ubf), at<__nv_bfloat16>(ws, p.hsum_bf), at<__nv_bfloat16>(ws, p.Vt),
+           at<float>(ws, p.Vpart), at<__half>(ws, p.Ud)};
+  if (prep) {
+    const StackLayout l = stack_layout(p);
+    b.Ain = at<__nv_bfloat16>(prep, l.Ain);
+    b.Bgs = at<__half>(prep, l.Bgs);
+    b.Bus = at<__half>(prep, l.Bus);
+    b.Adt = at<__half>(prep, l.Adt);
+    b.Adn = at<__nv_bfloat16>(prep, l.Adn);
+    b.Bdn = at<__nv_bfloat16>(prep, l.Bdn);
+  }
+  return b;
 }
 
 static cudaError_t run_ffn(const LayerArgs& a, const Plan& p, void* ws, const void* x, const void* wg,
                            const void* wu, const void* wd, const moe_hier_resid* resid, const int32_t* eidx,
                            const float* gate, const int32_t* row_asg, const int32_t* row_begin, void* y_rows,
-                           cudaEvent_t prep_done, cudaStream_t s) {
+                           cudaEvent_t prep_done, cudaStream_t s, void* prep = nullptr) {
   if (p.tc)
     return launch_ffn_tc(a, x, wg, wu, wd, resid_ptrs(a, resid), eidx, gate, row_asg, row_begin, y_rows,
-                         tc_bufs(p, ws), at<DevStatus>(ws, p.status), prep_done, s);
+                         tc_bufs(p, ws, prep), at<DevStatus>(ws, p.status), prep_done, s, prep != nullptr);
   FfnBufs b{at<float>(ws, p.U), at<float>(ws, p.H), at<float>(ws, p.hsum), at<float>(ws, p.V)};
   return launch_ffn_simt(a, x, wg, wu, wd, resid_ptrs(a, resid), eidx, gate, row_asg, row_begin, y_rows, b, s);
 }
@@ -220,6 +248,69 @@ static int cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return MOE_OK;
   g_last_cuda_error = e;
   return MOE_ERR_CUDA;
+}
+
+static int forward_impl(const moe_hier_desc* desc, const void* x, const void* w_group, const float* b_group,
+                        const void* w_expert, const int32_t* group_map_host, const void* w_gate, const void* w_up,
+                        const void* w_down, const moe_hier_resid* resid, void* prep, size_t prep_bytes, void* y,
+                        int32_t* gidx_opt, int32_t* eidx_opt, float* gate_opt, int32_t* perm_opt, void* ws,
+                        size_t ws_bytes, void* stream) {
+  LayerArgs a;
+  if (!group_map_host) return MOE_ERR_INVALID;
+  int st = validate(desc, group_map_host, &a);
+  if (st != MOE_OK) return st;
+  if (a.T > 0 && (!x || !w_group || !w_expert || !w_gate || !w_up || !w_down || !y ||
+                  !resid_ok(a, resid)))
+    return MOE_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(w_group) || !aligned16(w_expert) || !aligned16(w_gate) || !aligned16(w_up) ||
+      !aligned16(w_down) || !aligned16(y))
+    return MOE_ERR_INVALID;
+  const Plan p = make_plan(a);
+  if ((st = check_ws(p, ws, ws_bytes)) != MOE_OK) return st;
+  if (prep) {
+    if (!p.tc) return MOE_ERR_UNSUPPORTED;
+    if (((uintptr_t)prep & 255) != 0 || prep_bytes < stack_layout(p).total) return MOE_ERR_WORKSPACE;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t* gidx = gidx_opt ? gidx_opt : at<int32_t>(ws, p.gidx);
+  int32_t* eidx = eidx_opt ? eidx_opt : at<int32_t>(ws, p.eidx);
+  float* gate = gate_opt ? gate_opt : at<float>(ws, p.gate);
+  int32_t* perm = perm_opt ? perm_opt : at<int32_t>(ws, p.perm);
+  prof_start(s);
+  cudaError_t e = cudaMemsetAsync(at<DevStatus>(ws, p.status), 0, sizeof(DevStatus), s);
+  // residual stacks (unless prepared) and the dense U GEMM (when the layer uses it) on the side
+  // stream, concurrently with routing and permutation (in order, on `s`, when profiling per kernel)
+  cudaEvent_t prep_done = nullptr;
+  const bool side_work = p.tc && a.T > 0 && (!prep || tc_u_dense(a));
+  SideStream* side = (side_work && !g_prof_ev) ? side_stream() : nullptr;
+  if (e == cudaSuccess && side) {
+    e = cudaEventRecord(side->fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side->st, side->fork, 0);
+    if (e == cudaSuccess)
+      e = launch_resid_prep(a, resid_ptrs(a, resid), tc_bufs(p, ws, prep), x, at<DevStatus>(ws, p.status), side->st,
+                            prep == nullptr);
+    if (e == cudaSuccess) e = cudaEventRecord(side->join, side->st);
+    prep_done = side->join;
+  }
+  if (e == cudaSuccess)
+    e = launch_route(a, x, w_group, b_group, w_expert, at<float>(ws, p.logits), at<int32_t>(ws, p.redo), gidx,
+                     eidx, gate, at<DevStatus>(ws, p.status), true, s);
+  PermOut o{perm, at<int32_t>(ws, p.inv_pos), at<int32_t>(ws, p.ebeg), at<int32_t>(ws, p.ecnt),
+            at<int32_t>(ws, p.gbeg), at<int32_t>(ws, p.row_asg), at<int32_t>(ws, p.row_of),
+            at<int32_t>(ws, p.rbeg)};
+  if (e == cudaSuccess)
+    e = launch_permute(a, eidx, o, at<int32_t>(ws, p.cnt), at<int32_t>(ws, p.off), p.nblk,
+                       at<DevStatus>(ws, p.status), true, s);
+  void* yrows = a.kg > 1 ? at<void>(ws, p.yrows) : y;
+  if (e == cudaSuccess)
+    e = run_ffn(a, p, ws, x, w_gate, w_up, w_down, resid, eidx, gate, o.row_asg, o.rbeg, yrows, prep_done, s, prep);
+  if (e == cudaSuccess) e = launch_combine(a, yrows, y, s);
+  // the side stream's work rejoins `s` on every path (a capture must not end with it forked)
+  if (prep_done) {
+    const cudaError_t j = cudaStreamWaitEvent(s, prep_done, 0);
+    if (e == cudaSuccess) e = j;
+  }
+  return cuda_status(e);
 }
 
 }  // namespace moe
@@ -307,56 +398,44 @@ int moe_hier_forward(const moe_hier_desc* desc, const void* x, const void* w_gro
                      const void* w_gate, const void* w_up, const void* w_down,
                      const moe_hier_resid* resid, void* y, int32_t* gidx_opt, int32_t* eidx_opt,
                      float* gate_opt, int32_t* perm_opt, void* ws, size_t ws_bytes, void* stream) {
+  return forward_impl(desc, x, w_group, b_group, w_expert, group_map_host, w_gate, w_up, w_down, resid, nullptr, 0, y,
+                      gidx_opt, eidx_opt, gate_opt, perm_opt, ws, ws_bytes, stream);
+}
+
+size_t moe_hier_prepared_size(const moe_hier_desc* desc, int* status_out) {
+  LayerArgs a;
+  int st = validate(desc, nullptr, &a);
+  const Plan p = st == MOE_OK ? make_plan(a) : Plan{};
+  if (st == MOE_OK && !p.tc) st = MOE_ERR_UNSUPPORTED;
+  if (status_out) *status_out = st;
+  return st == MOE_OK ? stack_layout(p).total : 0;
+}
+
+int moe_hier_prepare(const moe_hier_desc* desc, const int32_t* group_map_host, const moe_hier_resid* resid,
+                     void* prep, size_t prep_bytes, void* stream) {
   LayerArgs a;
   if (!group_map_host) return MOE_ERR_INVALID;
   int st = validate(desc, group_map_host, &a);
   if (st != MOE_OK) return st;
-  if (a.T > 0 && (!x || !w_group || !w_expert || !w_gate || !w_up || !w_down || !y ||
-                  !resid_ok(a, resid)))
-    return MOE_ERR_INVALID;
-  if (!aligned16(x) || !aligned16(w_group) || !aligned16(w_expert) || !aligned16(w_gate) || !aligned16(w_up) ||
-      !aligned16(w_down) || !aligned16(y))
-    return MOE_ERR_INVALID;
   const Plan p = make_plan(a);
-  if ((st = check_ws(p, ws, ws_bytes)) != MOE_OK) return st;
-  cudaStream_t s = (cudaStream_t)stream;
-  int32_t* gidx = gidx_opt ? gidx_opt : at<int32_t>(ws, p.gidx);
-  int32_t* eidx = eidx_opt ? eidx_opt : at<int32_t>(ws, p.eidx);
-  float* gate = gate_opt ? gate_opt : at<float>(ws, p.gate);
-  int32_t* perm = perm_opt ? perm_opt : at<int32_t>(ws, p.perm);
-  prof_start(s);
-  cudaError_t e = cudaMemsetAsync(at<DevStatus>(ws, p.status), 0, sizeof(DevStatus), s);
-  // residual stacks on the side stream, concurrently with routing and permutation (in order,
-  // on `s`, when profiling per kernel)
-  cudaEvent_t prep_done = nullptr;
-  SideStream* side = (p.tc && a.T > 0 && !g_prof_ev) ? side_stream() : nullptr;
-  if (e == cudaSuccess && side) {
-    e = cudaEventRecord(side->fork, s);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(side->st, side->fork, 0);
-    if (e == cudaSuccess)
-      e = launch_resid_prep(a, resid_ptrs(a, resid), tc_bufs(p, ws), x, at<DevStatus>(ws, p.status), side->st);
-    if (e == cudaSuccess) e = cudaEventRecord(side->join, side->st);
-    prep_done = side->join;
-  }
-  if (e == cudaSuccess)
-    e = launch_route(a, x, w_group, b_group, w_expert, at<float>(ws, p.logits), at<int32_t>(ws, p.redo), gidx,
-                     eidx, gate, at<DevStatus>(ws, p.status), true, s);
-  PermOut o{perm, at<int32_t>(ws, p.inv_pos), at<int32_t>(ws, p.ebeg), at<int32_t>(ws, p.ecnt),
-            at<int32_t>(ws, p.gbeg), at<int32_t>(ws, p.row_asg), at<int32_t>(ws, p.row_of),
-            at<int32_t>(ws, p.rbeg)};
-  if (e == cudaSuccess)
-    e = launch_permute(a, eidx, o, at<int32_t>(ws, p.cnt), at<int32_t>(ws, p.off), p.nblk,
-                       at<DevStatus>(ws, p.status), true, s);
-  void* yrows = a.kg > 1 ? at<void>(ws, p.yrows) : y;
-  if (e == cudaSuccess)
-    e = run_ffn(a, p, ws, x, w_gate, w_up, w_down, resid, eidx, gate, o.row_asg, o.rbeg, yrows, prep_done, s);
-  if (e == cudaSuccess) e = launch_combine(a, yrows, y, s);
-  // the side stream's work rejoins `s` on every path (a capture must not end with it forked)
-  if (prep_done) {
-    const cudaError_t j = cudaStreamWaitEvent(s, prep_done, 0);
-    if (e == cudaSuccess) e = j;
-  }
-  return cuda_status(e);
+  if (!p.tc) return MOE_ERR_UNSUPPORTED;
+  if (!resid_ok(a, resid)) return MOE_ERR_INVALID;
+  if (!prep || ((uintptr_t)prep & 255) != 0 || prep_bytes < stack_layout(p).total) return MOE_ERR_WORKSPACE;
+  prof_start((cudaStream_t)stream);
+  // the stacks alone: no tokens are needed (x = null skips the dense U GEMM)
+  return cuda_status(launch_resid_prep(a, resid_ptrs(a, resid), tc_bufs(p, prep, prep), nullptr, nullptr,
+                                       (cudaStream_t)stream, true));
+}
+
+int moe_hier_forward_prepared(const moe_hier_desc* desc, const void* x, const void* w_group, const float* b_group,
+                              const void* w_expert, const int32_t* group_map_host, const void* w_gate,
+                              const void* w_up, const void* w_down, const moe_hier_resid* resid, const void* prep,
+                              size_t prep_bytes, void* y, int32_t* gidx_opt, int32_t* eidx_opt, float* gate_opt,
+                              int32_t* perm_opt, void* ws, size_t ws_bytes, void* stream) {
+  if (!prep) return MOE_ERR_WORKSPACE;
+  return forward_impl(desc, x, w_group, b_group, w_expert, group_map_host, w_gate, w_up, w_down, resid,
+                      const_cast<void*>(prep), prep_bytes, y, gidx_opt, eidx_opt, gate_opt, perm_opt, ws, ws_bytes,
+                      stream);
 }
 
 static int compress_args(const moe_hier_compress_desc* d, const int32_t* group_map, CmpArgs* c) {

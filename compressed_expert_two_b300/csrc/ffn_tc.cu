@@ -2300,16 +2300,20 @@ bool tc_u_dense(const LayerArgs& a) {
 //    routing either) -- a dense GEMM of x against all groups' stacked A^T, which the gate/up
 //    kernel then reads at (token, group)
 cudaError_t launch_resid_prep(const LayerArgs& a, const ResidPtrs& rp, const TcBufs& b, const void* x,
-                              DevStatus* status, cudaStream_t st) {
-  if (a.R == 0) return cudaSuccess;
+                              DevStatus* status, cudaStream_t st, bool stacks) {
+  if (a.R == 0 && stacks) return cudaSuccess;
   const PrepArgs pa = prep_args(a, rp, b);
   const int G = a.G, d = a.d, f = a.f, KRP = tc_krp(a);
-  launch_pdl(resid_prep_rows_kernel, dim3(148 * 4), dim3(256), 0, st, pa, a.tab);
-  launch_pdl(resid_prep_t_kernel, dim3(G * (2 * (f / 64) + d / 64 + (pa.Adt ? f / 64 : 0))), dim3(256), 0, st, pa,
-             a.tab);
-  prof_mark("resid_prep", st);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || !tc_u_dense(a)) return e;
+  cudaError_t e = cudaSuccess;
+  if (stacks) {
+    launch_pdl(resid_prep_rows_kernel, dim3(148 * 4), dim3(256), 0, st, pa, a.tab);
+    launch_pdl(resid_prep_t_kernel, dim3(G * (2 * (f / 64) + d / 64 + (pa.Adt ? f / 64 : 0))), dim3(256), 0, st, pa,
+               a.tab);
+    prof_mark("resid_prep", st);
+    e = cudaGetLastError();
+  }
+  // the dense U GEMM needs the tokens: a call that only prepares the stacks (x == null) stops here
+  if (e != cudaSuccess || !tc_u_dense(a) || a.T == 0 || x == nullptr || status == nullptr) return e;
   CUtensorMap mXt, mA;
   if (!make_map(&mXt, x, (uint64_t)a.T, d, kTile) || !make_map(&mA, b.Ain, (uint64_t)G * 4 * KRP, d, KRP))
     return cudaErrorInvalidValue;
@@ -2323,7 +2327,7 @@ cudaError_t launch_resid_prep(const LayerArgs& a, const ResidPtrs& rp, const TcB
 cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, const void* wu, const void* wd,
                           const ResidPtrs& rp, const int32_t* eidx, const float* gate, const int32_t* row_asg,
                           const int32_t* row_begin, void* y_rows, const TcBufs& b, DevStatus* status,
-                          cudaEvent_t prep_done, cudaStream_t st) {
+                          cudaEvent_t prep_done, cudaStream_t st, bool prepared) {
   if (a.R == 0) return cudaSuccess;
   const int KRP = tc_krp(a), G = a.G, d = a.d, f = a.f, R = a.R;
   const int tiles = (R + kTile - 1) / kTile + G;
@@ -2334,7 +2338,7 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   const bool u_simt = R <= kUSimtMaxRows;
   const bool up3 = up3_ok(a), up4 = up4_ok(a);
   const bool u_dense = tc_u_dense(a);
-  if (!prep_done && (e = launch_resid_prep(a, rp, b, x, status, st)) != cudaSuccess) return e;
+  if (!prep_done && (e = launch_resid_prep(a, rp, b, x, status, st, !prepared)) != cudaSuccess) return e;
 
   // 2. rows of x in (group, token) order (the CUDA-core U kernel writes them itself)
   if (!u_simt) {

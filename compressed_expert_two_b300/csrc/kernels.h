@@ -100,11 +100,13 @@ int tc_up_chunks(const LayerArgs& a);
 cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, const void* wu, const void* wd,
                           const ResidPtrs& rp, const int32_t* eidx, const float* gate, const int32_t* row_asg,
                           const int32_t* row_begin, void* y_rows, const TcBufs& b, DevStatus* status,
-                          cudaEvent_t prep_done, cudaStream_t st);
-// The weight-only first step of launch_ffn_tc (residual stacks); launch_ffn_tc skips it when
-// given prep_done, an event recorded after this call's work (it then waits for the event).
+                          cudaEvent_t prep_done, cudaStream_t st, bool prepared = false);
+// The first step of launch_ffn_tc: the residual stacks (weights only; skipped with stacks = false,
+// when the caller prepared them once) and, when tc_u_dense, U = A^T x of every token for every
+// group.  launch_ffn_tc skips it when given prep_done, an event recorded after this call's work
+// (it then waits for the event); with prepared = true it runs only the dense U GEMM itself.
 cudaError_t launch_resid_prep(const LayerArgs& a, const ResidPtrs& rp, const TcBufs& b, const void* x,
-                              DevStatus* status, cudaStream_t st);
+                              DevStatus* status, cudaStream_t st, bool stacks = true);
 // Whether U is computed densely, in token order for every group, with the residual stacks.
 bool tc_u_dense(const LayerArgs& a);
 

@@ -76,6 +76,23 @@ class DeviceLayer:
                            self.ws, self.ws_bytes, self.stream)
         return o
 
+    def prepare(self):
+        """Builds the residual stacks once (moe_hier_prepare); forward(prepared=True) then reads them."""
+        self.prep_bytes = L.moe_hier_prepared_size(self.desc)
+        self.prep = torch.empty(max(self.prep_bytes, 256), dtype=torch.uint8, device=self.device)
+        L.moe_hier_prepare(self.desc, self.group_map, self.resid, self.prep, self.prep_bytes, self.stream)
+        return self
+
+    def forward_prepared(self, x=None, out=None, routing_out: bool = True):
+        x = self.x if x is None else x
+        o = self.new_outputs() if out is None else out
+        L.moe_hier_forward_prepared(self.desc, x, self.w_group, self.b_group, self.w_expert, self.group_map,
+                                    self.w_gate, self.w_up, self.w_down, self.resid, self.prep, self.prep_bytes,
+                                    o["y"], o["gidx"] if routing_out else None, o["eidx"] if routing_out else None,
+                                    o["gate"] if routing_out else None, o["perm"] if routing_out else None,
+                                    self.ws, self.ws_bytes, self.stream)
+        return o
+
     # ---- the stages one by one (same kernels as forward) ----
     def route(self, x=None):
         x = self.x if x is None else x

@@ -161,6 +161,26 @@ int moe_hier_forward(const moe_hier_desc* desc, const void* x, const void* w_gro
                      int32_t* gidx_opt, int32_t* eidx_opt, float* gate_opt, int32_t* perm_opt,
                      void* ws, size_t ws_bytes, void* stream);
 
+/* Prepared residual stacks.  The tensor-core path multiplies FP16/BF16 stacks of the residual
+ * factors that it builds from the INT4 codes (weights only: they do not depend on the tokens).
+ * moe_hier_forward rebuilds them on every call, overlapped with routing; a caller that runs the
+ * same layer many times (decode) builds them once with moe_hier_prepare into a buffer of
+ * moe_hier_prepared_size bytes (device, 256-byte aligned, owned by the caller) and calls
+ * moe_hier_forward_prepared, which reads them from there and skips the rebuild.  The stacks' form
+ * depends on the descriptor (which kernels a batch of T tokens uses), so prepare with the
+ * descriptor the forward calls use, and again after the residual factors change.  Results equal
+ * moe_hier_forward's bit for bit.  BF16 layers with INT4 residuals only (MOE_ERR_UNSUPPORTED
+ * otherwise); MOE_ERR_WORKSPACE if prep is missing, misaligned or too small. */
+size_t moe_hier_prepared_size(const moe_hier_desc* desc, int* status_out);
+int moe_hier_prepare(const moe_hier_desc* desc, const int32_t* group_map_host, const moe_hier_resid* resid,
+                     void* prep, size_t prep_bytes, void* stream);
+int moe_hier_forward_prepared(const moe_hier_desc* desc, const void* x, const void* w_group,
+                              const float* b_group, const void* w_expert, const int32_t* group_map_host,
+                              const void* w_gate, const void* w_up, const void* w_down,
+                              const moe_hier_resid* resid, const void* prep, size_t prep_bytes, void* y,
+                              int32_t* gidx_opt, int32_t* eidx_opt, float* gate_opt, int32_t* perm_opt,
+                              void* ws, size_t ws_bytes, void* stream);
+
 /* Synchronises `stream`, then returns the device status word of `ws` (MOE_OK or
  * MOE_ERR_TIMEOUT), or MOE_ERR_CUDA if the stream reported an error. */
 int moe_hier_get_status(const void* ws, void* stream);

@@ -324,3 +324,32 @@ def test_persistent_down_gemm_sampled():
     GEMM with double-buffered accumulators; sampled tokens against the oracle, ragged groups."""
     cfg = small(T=16384, d=1024, f=256, E=8, G=2, kg=1, ke=2, seed=47, resid_std=0.2)
     full_size_check("persist", 48, cfg)
+
+
+@pytest.mark.parametrize("name", ["bf16_ragged", "bf16_kg2_ke3", "bf16_rows2500_ke1", "small_bf16_int4",
+                                  "bf16_rows2200_krp128_ke3", "bf16_one_token"])
+def test_prepared_stacks_forward_is_identical(name):
+    """moe_hier_forward_prepared (residual stacks built once by moe_hier_prepare) returns exactly
+    what moe_hier_forward returns, twice in a row (the stacks are not consumed)."""
+    inp = make_inputs(CASES[name])
+    layer = device_layer(inp)
+    want = layer.forward()
+    layer.prepare()
+    for _ in range(2):
+        got = layer.forward_prepared()
+        torch.cuda.synchronize()
+        assert layer.status() == 0
+        for k in ("y", "gidx", "eidx", "gate", "perm"):
+            assert torch.equal(got[k], want[k]), k
+
+
+def test_prepared_stacks_decode_shape_sampled():
+    """A decode-shaped layer (64 tokens, d_model 4096) through the prepared path against the oracle."""
+    cfg = small(T=64, d=4096, f=1024, E=32, G=8, kg=1, ke=2, seed=58, resid_std=0.2, group_map="contiguous")
+    inp = make_inputs(cfg)
+    layer = device_layer(inp).prepare()
+    out = layer.forward_prepared()
+    torch.cuda.synchronize()
+    ref = oracle.forward(inp)
+    check_routing(out, ref)
+    check_y(out["y"], ref["y"], "prepared decode")
