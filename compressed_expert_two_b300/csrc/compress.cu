@@ -424,8 +424,12 @@ __global__ void __launch_bounds__(256) cmp_quant_kernel(const float* __restrict_
 // ------------------------------------------------------------------------------------------
 // 4. Reconstruction error: acc[e] += (sum over the expert's elements of (W - base - B A^T)^2,
 //    sum of W^2) with A, B dequantised from their codes; FP64 accumulators zeroed before.
-//    Thread: one row o and 8 consecutive columns; grid-stride over (e, o, column piece).
+//    CTA (column tile of 128, expert, row split): A^T's 128 columns of every rank, dequantised once
+//    into shared memory; each warp then takes rows of the split, lane j holding 4 consecutive
+//    columns, the row's r values of B dequantised by lanes 0..r-1 and shared by shuffles.
 // ------------------------------------------------------------------------------------------
+constexpr int kErrCols = 128;
+
 __device__ __forceinline__ float dq4(const uint8_t* codes, const __half* scales, size_t row, int n, int c) {
   const uint8_t b = codes[row * (n / 2) + (c >> 1)];
   const int u = (c & 1) ? (b & 0xF) : (b >> 4);
@@ -439,42 +443,54 @@ __global__ void __launch_bounds__(256) cmp_err_kernel(const __nv_bfloat16* __res
                                                       const __half* __restrict__ Bs, double* __restrict__ acc) {
   pdl_wait();
   pdl_trigger();
-  __shared__ double red[2][256];
-  const size_t per_e = (size_t)d_out * (d_in / 8);
-  const int e = blockIdx.y;                              // blockIdx.y: the expert
-  const int g = tab.group_of[e];
+  __shared__ __align__(16) float Asm[32][kErrCols];
+  __shared__ double red[2][8];
+  const int e = blockIdx.y, g = tab.group_of[e];
+  const int c_tile = blockIdx.x * kErrCols;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < r * kErrCols; i += blockDim.x) {
+    const int k = i / kErrCols, c = i % kErrCols;
+    Asm[k][c] = dq4(Aq, As, (size_t)e * r + k, d_in, c_tile + c);
+  }
+  __syncthreads();
+  const int rows_per = (d_out + gridDim.z - 1) / gridDim.z;
+  const int o_begin = blockIdx.z * rows_per, o_end = min(d_out, o_begin + rows_per);
+  const int c0 = c_tile + lane * 4;
   double num = 0.0, den = 0.0;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < per_e; i += (size_t)gridDim.x * blockDim.x) {
-    const int o = (int)(i / (d_in / 8)), c0 = (int)(i % (d_in / 8)) * 8;
-    float w[8], b[8];
-    bf16x8_to_f32(*reinterpret_cast<const uint4*>(W + ((size_t)e * d_out + o) * d_in + c0), w);
-    bf16x8_to_f32(*reinterpret_cast<const uint4*>(base + ((size_t)g * d_out + o) * d_in + c0), b);
-    float pred[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int o = o_begin + warp; o < o_end; o += 8) {
+    const float bk_lane = lane < r ? dq4(Bq, Bs, (size_t)e * r + lane, d_out, o) : 0.f;
+    const uint2 wv = *reinterpret_cast<const uint2*>(W + ((size_t)e * d_out + o) * d_in + c0);
+    const uint2 bv = *reinterpret_cast<const uint2*>(base + ((size_t)g * d_out + o) * d_in + c0);
+    const float w[4] = {__uint_as_float(wv.x << 16), __uint_as_float(wv.x & 0xffff0000u),
+                        __uint_as_float(wv.y << 16), __uint_as_float(wv.y & 0xffff0000u)};
+    const float b[4] = {__uint_as_float(bv.x << 16), __uint_as_float(bv.x & 0xffff0000u),
+                        __uint_as_float(bv.y << 16), __uint_as_float(bv.y & 0xffff0000u)};
+    float pred[4] = {0.f, 0.f, 0.f, 0.f};
     for (int k = 0; k < r; ++k) {
-      const float bk = dq4(Bq, Bs, (size_t)e * r + k, d_out, o);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) pred[u] = fmaf(bk, dq4(Aq, As, (size_t)e * r + k, d_in, c0 + u), pred[u]);
+      const float bk = __shfl_sync(0xffffffffu, bk_lane, k);
+      const float4 a0 = *reinterpret_cast<const float4*>(&Asm[k][lane * 4]);
+      pred[0] = fmaf(bk, a0.x, pred[0]); pred[1] = fmaf(bk, a0.y, pred[1]);
+      pred[2] = fmaf(bk, a0.z, pred[2]); pred[3] = fmaf(bk, a0.w, pred[3]);
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const double d = (double)w[u] - (double)b[u] - (double)pred[u];
-      num += d * d;
+    for (int u = 0; u < 4; ++u) {
+      const double dlt = (double)w[u] - (double)b[u] - (double)pred[u];
+      num += dlt * dlt;
       den += (double)w[u] * (double)w[u];
     }
   }
-  red[0][threadIdx.x] = num;
-  red[1][threadIdx.x] = den;
-  __syncthreads();
-  for (int s = 128; s > 0; s >>= 1) {
-    if (threadIdx.x < s) {
-      red[0][threadIdx.x] += red[0][threadIdx.x + s];
-      red[1][threadIdx.x] += red[1][threadIdx.x + s];
-    }
-    __syncthreads();
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    num += __shfl_xor_sync(0xffffffffu, num, o);
+    den += __shfl_xor_sync(0xffffffffu, den, o);
   }
+  if (lane == 0) { red[0][warp] = num; red[1][warp] = den; }
+  __syncthreads();
   if (threadIdx.x == 0) {
-    atomicAdd(acc + 2 * e, red[0][0]);
-    atomicAdd(acc + 2 * e + 1, red[1][0]);
+    double a = 0.0, b2 = 0.0;
+    for (int w8 = 0; w8 < 8; ++w8) { a += red[0][w8]; b2 += red[1][w8]; }
+    atomicAdd(acc + 2 * e, a);
+    atomicAdd(acc + 2 * e + 1, b2);
   }
 }
 
@@ -623,7 +639,11 @@ cudaError_t launch_compress(const CmpArgs& c, const void* W, const float* omega,
   // 4. reconstruction error
   if (err) {
     if ((e = cudaMemsetAsync(acc, 0, (size_t)E * 2 * 8, st)) != cudaSuccess) return e;
-    launch_pdl(cmp_err_kernel, dim3(148 * 4 / E > 0 ? 148 * 4 / E + 1 : 1, E), dim3(256), 0, st, Wb,
+    const int ctiles = d_in / kErrCols;
+    int splits = (148 * 4 + ctiles * E - 1) / (ctiles * E);
+    if (splits > d_out / 8) splits = d_out / 8;
+    if (splits < 1) splits = 1;
+    launch_pdl(cmp_err_kernel, dim3(ctiles, E, splits), dim3(256), 0, st, Wb,
                (const __nv_bfloat16*)base, tab, d_out, d_in, r, (const uint8_t*)Aq, (const __half*)As,
                (const uint8_t*)Bq, (const __half*)Bs, acc);
     prof_mark("cmp_err", st);
