@@ -292,12 +292,12 @@ static int forward_impl(const moe_hier_desc* desc, const void* x, const void* w_
     if (e == cudaSuccess) e = cudaEventRecord(side->join, side->st);
     prep_done = side->join;
   }
-  if (e == cudaSuccess)
-    e = launch_route(a, x, w_group, b_group, w_expert, at<float>(ws, p.logits), at<int32_t>(ws, p.redo), gidx,
-                     eidx, gate, at<DevStatus>(ws, p.status), true, s);
   PermOut o{perm, at<int32_t>(ws, p.inv_pos), at<int32_t>(ws, p.ebeg), at<int32_t>(ws, p.ecnt),
             at<int32_t>(ws, p.gbeg), at<int32_t>(ws, p.row_asg), at<int32_t>(ws, p.row_of),
             at<int32_t>(ws, p.rbeg)};
+  if (e == cudaSuccess)
+    e = launch_route(a, x, w_group, b_group, w_expert, at<float>(ws, p.logits), at<int32_t>(ws, p.redo), gidx,
+                     eidx, gate, at<DevStatus>(ws, p.status), true, s);
   if (e == cudaSuccess)
     e = launch_permute(a, eidx, o, at<int32_t>(ws, p.cnt), at<int32_t>(ws, p.off), p.nblk,
                        at<DevStatus>(ws, p.status), true, s);

@@ -353,3 +353,30 @@ def test_prepared_stacks_decode_shape_sampled():
     ref = oracle.forward(inp)
     check_routing(out, ref)
     check_y(out["y"], ref["y"], "prepared decode")
+
+
+@pytest.mark.parametrize("kw", [dict(T=64, d=512, f=256, E=32, G=8, kg=1, ke=2, seed=61),
+                                dict(T=200, d=256, f=192, E=64, G=8, kg=2, ke=3, seed=62, group_map="contiguous"),
+                                dict(T=129, d=256, f=192, E=64, G=16, kg=2, ke=2, seed=63),
+                                dict(T=256, d=384, f=128, E=16, G=4, kg=1, ke=2, seed=64, zipf_s=1.2)])
+def test_small_batches_forward_matches_stages_and_oracle(kw):
+    """Batches of at most 256 tokens (the decode shapes): moe_hier_forward and the stage-by-stage
+    calls (route, permute, ffn, combine) give the same routing, permutation and output bit for
+    bit, and both match the oracle."""
+    cfg = small(resid_std=0.2, **kw)
+    inp = make_inputs(cfg)
+    layer = device_layer(inp)
+    fwd = layer.forward()
+    r = layer.route()
+    pm = layer.permute(r["eidx"])
+    y = layer.combine(layer.ffn(layer.x, r["eidx"], r["gate"], pm["row_asg"], pm["row_begin"]))
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    for k in ("gidx", "eidx", "gate"):
+        assert torch.equal(fwd[k], r[k]), k
+    assert torch.equal(fwd["perm"], pm["perm"])
+    assert torch.equal(fwd["y"], y)
+    ref = oracle.forward(inp)
+    check_routing(fwd, ref)
+    assert np.array_equal(fwd["perm"].cpu().numpy(), ref["perm"])
+    check_y(fwd["y"], ref["y"], "small batch")
