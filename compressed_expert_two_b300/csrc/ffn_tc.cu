@@ -691,7 +691,10 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_pair_kernel(
 // ------------------------------------------------------------------------------------------
 // 4. Fused gate/up tile: base once, per-slot residual, SwiGLU, gated sum, down-residual partials
 //
-// One CTA owns a 128-row tile of one group and a chunk of 64-column d_ff tiles.  Warp roles
+// A work item is a 128-row tile of one group and a chunk of 64-column d_ff tiles; one CTA per SM
+// walks the items w = blockIdx.x, blockIdx.x + gridDim.x, ... (persistent: the stage ring, the
+// double-buffered accumulator and the slot phases run on across items, so the next item's K loop
+// overlaps this item's slots, and small items balance the SMs).  Warp roles
 // (12 warps): 0 TMA producer of the base stages (X, W_gate, W_up); 1 base MMA issuer (owns TMEM);
 // 2 residual/V MMA issuer; 3 TMA producer of the residual tiles (B_gate, B_up, A_down^T codes);
 // 4..11 epilogue, two warps per TMEM lane quarter, warp group h in {0,1} handling the tile's d_ff
@@ -727,6 +730,7 @@ struct UpArgs {
   DevStatus* status;
   GroupTable tab;
   int G, d, f, kg, ke, R, n_ftiles, ftiles_per_chunk;
+  int n_row_tiles, n_chunks;   // work items of the 128-column kernel: row tile x chunk
 };
 
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
@@ -760,12 +764,17 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
-  int g, r0, r1;
-  if (!tile_of(p.row_begin, p.G, blockIdx.y, g, r0, r1)) return;
-  const int ft0 = blockIdx.x * p.ftiles_per_chunk;
-  const int ft1 = min(ft0 + p.ftiles_per_chunk, p.n_ftiles);
-  if (ft0 >= ft1) return;
-  const int nft = ft1 - ft0;
+  // work items w = row tile * n_chunks + chunk, taken w = blockIdx.x, blockIdx.x + gridDim.x, ...
+  // (one CTA per item, or one per SM walking several); every role walks the same items and skips
+  // the unused ones alike, and the stage ring, accumulator parity and slot phases run on across
+  // items (glt: tiles, sig: slots, counted over the CTA's items)
+  const int n_items = p.n_row_tiles * p.n_chunks;
+  auto item = [&](int w, int& g, int& r0, int& r1, int& ft0, int& nft) -> bool {
+    if (!tile_of(p.row_begin, p.G, w / p.n_chunks, g, r0, r1)) return false;
+    ft0 = (w % p.n_chunks) * p.ftiles_per_chunk;
+    nft = min(ft0 + p.ftiles_per_chunk, p.n_ftiles) - ft0;
+    return nft > 0;
+  };
   const int nkb = p.d / 64;
   const int f = p.f, fg = f / 64;
 
@@ -808,6 +817,9 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
       tc::prefetch_map(&mX); tc::prefetch_map(&mWg); tc::prefetch_map(&mWu);
       int kc = 0;
       bool ok = true;
+      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      int g, r0, r1, ft0, nft;
+      if (!item(w, g, r0, r1, ft0, nft)) continue;
       for (int lt = 0; lt < nft && ok; ++lt) {
         const int n0 = (ft0 + lt) * kNf;
         for (int kb = 0; kb < nkb; ++kb, ++kc) {
@@ -820,25 +832,32 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
           tc::tma_load_2d(st + X_BYTES + kNf * 128, &mWu, &full[s], kb * 64, (int)p.tab.wslot[g] * f + n0);
         }
       }
+      }
       if (abort_flag) tc::drain_copies();
     }
   } else if (warp == 3) {
     if (lane == 0) {
       // ---------------- TMA producer of the residual tiles (one set per d_ff tile)
       tc::prefetch_map(&mBg); tc::prefetch_map(&mBu); tc::prefetch_map(&mAd);
-      for (int lt = 0; lt < nft; ++lt) {
-        const int n0 = (ft0 + lt) * kNf, rb = lt % RBUF, use = lt / RBUF;
+      int glt = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      int g, r0, r1, ft0, nft;
+      if (!item(w, g, r0, r1, ft0, nft)) continue;
+      for (int lt = 0; lt < nft; ++lt, ++glt) {
+        const int n0 = (ft0 + lt) * kNf, rb = glt % RBUF, use = glt / RBUF;
         uint8_t* sr = sRes + rb * RES_BYTES;
-        if (use > 0 && !tc::bar_wait(&rb_empty[rb], (use - 1) & 1, ab, 13)) break;
+        if (use > 0 && !tc::bar_wait(&rb_empty[rb], (use - 1) & 1, ab, 13)) { ok = false; break; }
         tc::bar_expect_tx(&rb_full[rb], 2 * BRES_BYTES);
 #pragma unroll
         for (int a = 0; a < KATOM; ++a) {
           tc::tma_load_2d(sr + a * kNf * 128, &mBg, &rb_full[rb], a * 64, g * f + n0);
           tc::tma_load_2d(sr + BRES_BYTES + a * kNf * 128, &mBu, &rb_full[rb], a * 64, g * f + n0);
         }
-        if (use > 0 && !tc::bar_wait(&ad_empty[rb], (use - 1) & 1, ab, 14)) break;
+        if (use > 0 && !tc::bar_wait(&ad_empty[rb], (use - 1) & 1, ab, 14)) { ok = false; break; }
         tc::bar_expect_tx(&ad_full[rb], AD_BYTES);
         tc::tma_load_2d(sr + 2 * BRES_BYTES, &mAd, &ad_full[rb], n0, g * KRP);
+      }
       }
       if (abort_flag) tc::drain_copies();
     }
@@ -846,11 +865,14 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
     if (lane == 0) {
       // ---------------- base MMA issuer: [Hg | Hu] = X [Wg | Wu]^T into acc[lt & 1]
       constexpr uint32_t id_base = tc::idesc_bf16(kTile, 2 * kNf);
-      int kc = 0;
+      int kc = 0, glt = 0;
       bool ok = true;
-      for (int lt = 0; lt < nft && ok; ++lt) {
-        const int b = lt & 1;
-        if (lt >= 2 && !tc::bar_wait(&acc_empty[b], ((lt >> 1) - 1) & 1, ab, 21)) break;
+      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      int g, r0, r1, ft0, nft;
+      if (!item(w, g, r0, r1, ft0, nft)) continue;
+      for (int lt = 0; lt < nft && ok; ++lt, ++glt) {
+        const int b = glt & 1;
+        if (glt >= 2 && !tc::bar_wait(&acc_empty[b], ((glt >> 1) - 1) & 1, ab, 21)) { ok = false; break; }
         tc::fence_after();
         const uint32_t dcol = tmem + b * 2 * kNf;
         for (int kb = 0; kb < nkb; ++kb, ++kc) {
@@ -867,6 +889,7 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
         if (!ok) break;
         tc::mma_commit(&base_full[b]);
       }
+      }
       tc::mma_commit(&fin1);
       const uint64_t t0 = tc::now_ns();
       while (!tc::bar_test(&fin1, 0) && tc::now_ns() - t0 < tc::kWaitNs) {}
@@ -878,10 +901,9 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
       constexpr uint32_t id_res = tc::idesc_f16(kTile, kNf);     // FP16 U~ x FP16 B
       constexpr uint32_t id_v = tc::idesc_bf16(kTile, KRP);
       const uint32_t ug = tc::smem_u32(sUg), uu = tc::smem_u32(sUu), hh = tc::smem_u32(sH);
-      const int n_slots = nft * KE;
-      // V MMA of slot index tau (tile tau / KE, slot tau % KE)
+      // V MMA of slot index tau (CTA-wide tile tau / KE, slot tau % KE)
       auto issue_v = [&](int tau) -> bool {
-        const int lt = tau / KE, s = tau % KE, rb = lt % RBUF, use = lt / RBUF;
+        const int glt = tau / KE, s = tau % KE, rb = glt % RBUF, use = glt / RBUF;
         if (s == 0 && !tc::bar_wait(&ad_full[rb], use & 1, ab, 26)) return false;
         if (!tc::bar_wait(&h_ready, tau & 1, ab, 27)) return false;
         if (tau >= 1 && !tc::bar_wait(&v_empty, (tau - 1) & 1, ab, 28)) return false;
@@ -895,11 +917,15 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
         return true;
       };
       bool ok = true;
-      for (int sig = 0; sig < n_slots && ok; ++sig) {
-        const int lt = sig / KE, s = sig % KE, b = lt & 1, rb = lt % RBUF, use = lt / RBUF;
+      int sig = 0;
+      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      int g, r0, r1, ft0, nft;
+      if (!item(w, g, r0, r1, ft0, nft)) continue;
+      for (int ls = 0; ls < nft * KE && ok; ++ls, ++sig) {
+        const int glt = sig / KE, s = sig % KE, b = glt & 1, rb = glt % RBUF, use = glt / RBUF;
         if (sig >= 1 && !issue_v(sig - 1)) { ok = false; break; }
         if (s == 0) {
-          if (!tc::bar_wait(&base_full[b], (lt >> 1) & 1, ab, 23)) { ok = false; break; }
+          if (!tc::bar_wait(&base_full[b], (glt >> 1) & 1, ab, 23)) { ok = false; break; }
           if (!tc::bar_wait(&rb_full[rb], use & 1, ab, 24)) { ok = false; break; }
         }
         if (!tc::bar_wait(&u_ready, sig & 1, ab, 25)) { ok = false; break; }
@@ -917,18 +943,39 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
         tc::mma_commit(&acc_full);
         if (s == KE - 1) tc::mma_commit(&rb_empty[rb]);
       }
-      if (ok && n_slots > 0) issue_v(n_slots - 1);
+      }
+      if (ok && sig > 0) issue_v(sig - 1);
       tc::mma_commit(&fin2);
       const uint64_t t0 = tc::now_ns();
       while (!tc::bar_test(&fin2, 0) && tc::now_ns() - t0 < tc::kWaitNs) {}
     }
   } else {
     // ---------------- epilogue: one thread per (tile row, column half)
-    const int q = warp & 3, half = (warp - kUpEpiWarp0) >> 2, row = q * 32 + lane, i = r0 + row;
-    const bool valid = i < r1;
+    const int q = warp & 3, half = (warp - kUpEpiWarp0) >> 2, row = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const int c_half = half * 32;                    // this group's first column of the tile
     uint8_t* sU = half == 0 ? sUg : sUu;             // U~ half this group writes
+    // this row of this half's U~ starts at zero (later items find the previous item's last delta
+    // there, which the first delta of the item clears)
+#pragma unroll
+    for (int a = 0; a < KATOM; ++a) {
+      uint4* z = reinterpret_cast<uint4*>(sU + a * kTile * 128 + (row >> 3) * 1024 + (row & 7) * 128);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) z[c] = make_uint4(0, 0, 0, 0);
+    }
+    // U~ holds the last delta: +values in block nz_pos, -values in block nz_neg (or none).
+    int nz_pos = -1, nz_neg = -1;
+    uint32_t unext[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) unext[c] = 0u;
+    __half2 sc_ad[kRank / 2];                        // A_down scales of the slot V is pending for
+    bool ok = true;
+    int sig = 0, glt = 0;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+    int g, r0, r1, ft0, nft;
+    if (!item(w, g, r0, r1, ft0, nft)) continue;
+    const int i = r0 + row, chunk = w % p.n_chunks;
+    const bool valid = i < r1;
     int le[KE], eid[KE];
     float gt[KE];
 #pragma unroll
@@ -944,13 +991,6 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
         gt[s] = p.gate[(size_t)t * k + j * KE + s];
       }
       urow = p.U + (size_t)i * 2 * KRP + half * KRP;
-    }
-    // this row of this half's U~ starts at zero
-#pragma unroll
-    for (int a = 0; a < KATOM; ++a) {
-      uint4* z = reinterpret_cast<uint4*>(sU + a * kTile * 128 + (row >> 3) * 1024 + (row & 7) * 128);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) z[c] = make_uint4(0, 0, 0, 0);
     }
     // V accumulators: half h keeps the slots s with s % 2 == h (vacc[s / 2])
     constexpr int KV = (KE + 1) / 2;
@@ -980,11 +1020,6 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
       *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, blk * kRank, kTile)) = z;
       *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, blk * kRank + 8, kTile)) = z;
     };
-    // U~ holds the last delta: +values in block nz_pos, -values in block nz_neg (or none).
-    int nz_pos = -1, nz_neg = -1;
-    uint32_t unext[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) unext[c] = 0u;
     // Writes the delta of slot s (first slot of a tile: no subtraction) from unext.
     auto build_delta = [&](int s) {
       if (!valid) return;
@@ -1011,19 +1046,17 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
     if (KE > 1) load_u(0, KE > 1 ? 1 : 0, unext);
     else if (nft > 1) load_u(1, 0, unext);
 
-    __half2 sc_ad[kRank / 2];                        // A_down scales of the slot V is pending for
-    bool ok = true;
-    int sig = 0;
-    for (int lt = 0; lt < nft && ok; ++lt) {
-      const int bsel = lt & 1;
+    for (int lt = 0; lt < nft && ok; ++lt, ++glt) {
+      const int bsel = glt & 1;
       const uint32_t acc_col = bsel * 2 * kNf;
       float hs[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) hs[c] = 0.f;
 #pragma unroll
       for (int s = 0; s < KE; ++s, ++sig) {
-        // (A) V of the previous slot: wait (this also frees sH), read the row's block, scale
-        if (sig >= 1) {
+        // (A) V of the previous slot of this item: wait (this also frees sH), read the row's
+        // block, scale (the previous item's last V was read at that item's end)
+        if (lt * KE + s >= 1) {
           if (!tc::bar_wait(&v_full, (sig - 1) & 1, ab, 30)) { ok = false; break; }
           tc::fence_after();
           const int ps = s > 0 ? s - 1 : KE - 1;
@@ -1103,8 +1136,9 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
                                   tc::pack_bf16(hs[c + 4], hs[c + 5]), tc::pack_bf16(hs[c + 6], hs[c + 7]));
       }
     }
-    // V of the last slot
-    if (ok && sig >= 1) {
+    if (!ok) break;
+    // V of the item's last slot; then V is free for the next item's first V MMA
+    {
       if (!tc::bar_wait(&v_full, (sig - 1) & 1, ab, 33)) ok = false;
       tc::fence_after();
       constexpr int ps = KE - 1;
@@ -1125,8 +1159,10 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
         }
       }
     }
+    tc::fence_before();
+    tc::bar_arrive(&v_empty);
     if (ok && valid) {
-      float* vp = p.Vpart + ((size_t)blockIdx.x * p.R + i) * KE * kRank;
+      float* vp = p.Vpart + ((size_t)chunk * p.R + i) * KE * kRank;
 #pragma unroll
       for (int s = 0; s < KE; ++s)
         if (half == (s & 1)) {
@@ -1136,6 +1172,7 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
                 make_float4(gt[s] * vacc[s / 2][k], gt[s] * vacc[s / 2][k + 1], gt[s] * vacc[s / 2][k + 2],
                             gt[s] * vacc[s / 2][k + 3]);
         }
+    }
     }
   }
   tc::fence_before();
@@ -2014,14 +2051,17 @@ int tc_krp(const LayerArgs& a) { return ((a.K * a.r + 63) / 64) * 64; }
 
 // Number of d_ff chunks per row tile.  Row tiles are only known on the device, so the host
 // estimates them (full tiles plus about half a partial tile per group, or one tile per group
-// when groups hold fewer than 128 rows) and picks the chunk count whose waves of one CTA per SM
-// cost least: ceil(CTAs / SMs) x (tiles per chunk + a fixed per-CTA overhead of half a tile).
+// when groups hold fewer than 128 rows) and picks the chunk count whose waves of one item per SM
+// cost least: ceil(items / SMs) x (tiles per chunk + a fixed per-item overhead).
 // Which fused gate/up kernel runs: the 256-column one (4b) when K r fits 64 columns, at most
 // two slots and d_ff is a multiple of 128; otherwise the 128-column one (4).
 static bool up3_ok(const LayerArgs& a) { return tc_krp(a) == 64 && a.ke <= 2 && a.f % kNf3 == 0; }
 
 int tc_up_chunks(const LayerArgs& a) {
   const int n_ft = a.f / (up3_ok(a) ? kNf3 : kNf);
+  // the 128-column kernel is persistent: an item boundary costs about a tenth of a tile (the next
+  // item's K loop runs under the previous item's slots); the others pay half a tile per CTA
+  const double item_cost = up3_ok(a) ? 0.5 : 0.1;
   const int full = (a.R + kTile - 1) / kTile;
   int tiles = a.R >= kTile * a.G ? full + (a.G + 1) / 2 : (a.R < a.G ? a.R : a.G);
   if (tiles < 1) tiles = 1;
@@ -2032,7 +2072,7 @@ int tc_up_chunks(const LayerArgs& a) {
     const int per = (n_ft + c - 1) / c;
     if (c > 1 && (n_ft + per - 1) / per != c) continue;     // same split as a smaller count
     const double waves = (double)((tiles * c + sms - 1) / sms);
-    const double cost = waves * (per + 0.5);
+    const double cost = waves * (per + item_cost);
     if (cost < best_cost - 1e-9) { best_cost = cost; best = c; }
   }
   return best;
@@ -2098,9 +2138,13 @@ static cudaError_t launch_up_ke(const CUtensorMap* maps, const UpArgs& p, int nc
                       (size_t)RBUF * (2 * (KRP * kNf * 2) + KRP * 128) + 2 * (kTile * KRP * 2) + kTile * 128;
   static std::atomic<uint64_t> attr{0};
   if (const cudaError_t e = smem_attr_once(ffn_up_tc_kernel<KRP, STAGES, KE, RBUF>, smem, attr); e != cudaSuccess) return e;
-  dim3 grid(nchunks, tiles);
-  return launch_pdl(ffn_up_tc_kernel<KRP, STAGES, KE, RBUF>, grid, dim3(kUpWarps * 32), smem, stream, maps[0],
-                    maps[1], maps[2], maps[3], maps[4], maps[5], p);
+  // one CTA per SM walks the (row tile, chunk) items (fewer CTAs when there are fewer items)
+  int dev = 0, sms = 0;
+  if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return e;
+  if (cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev); e != cudaSuccess) return e;
+  const int items = nchunks * tiles;
+  return launch_pdl(ffn_up_tc_kernel<KRP, STAGES, KE, RBUF>, dim3(items < sms ? items : sms), dim3(kUpWarps * 32),
+                    smem, stream, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
 }
 
 template <int KE>
@@ -2256,6 +2300,8 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   p.R = R; p.n_ftiles = f / nf_up;
   const int nchunks = tc_up_chunks(a);
   p.ftiles_per_chunk = (p.n_ftiles + nchunks - 1) / nchunks;
+  p.n_row_tiles = tiles;
+  p.n_chunks = nchunks;
   if (up4) {
     CUtensorMap mBgP, mBuP;     // halves of the B_gate / B_up tiles (64 rows per CTA of a pair)
     if (!make_map(&mBgP, b.Bgs, (uint64_t)G * f, KRP, kNf3 / 2) || !make_map(&mBuP, b.Bus, (uint64_t)G * f, KRP, kNf3 / 2))
