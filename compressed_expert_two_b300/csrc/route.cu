@@ -363,14 +363,8 @@ static void launch_select_any(const LayerArgs& a, const float* logits, const int
 // group's top-k_e members, which hold every member of the union's top k_e), the k_e best by
 // canonical expert logit (ties to the lower id) get gate = softmax over their logits (in pick
 // order, as the within-group gates), every other slot gate 0.  One thread per token.
-__global__ void __launch_bounds__(256) router_across_kernel(const float* __restrict__ logits, int Tn, int G, int E,
-                                                            int k, int ke, const int32_t* __restrict__ eidx,
-                                                            float* __restrict__ gate) {
-  pdl_wait();
-  pdl_trigger();
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= Tn) return;
-  const float* se = logits + (size_t)t * (G + E) + G;
+__device__ __forceinline__ void across_token(const float* __restrict__ se, int t, int k, int ke,
+                                             const int32_t* __restrict__ eidx, float* __restrict__ gate) {
   int id[kMaxK];
   float v[kMaxK], q[kMaxK];
   int slot[kMaxK];
@@ -410,6 +404,19 @@ __global__ void __launch_bounds__(256) router_across_kernel(const float* __restr
 #pragma unroll
   for (int s = 0; s < kMaxK; ++s)
     if (s < k) gate[(size_t)t * k + s] = g[s];
+}
+
+// With a list (the tokens the tensor-core router left over), logits row p belongs to token
+// list[p], p < *list_n, grid-stride; without one, row p is token p.
+__global__ void __launch_bounds__(256) router_across_kernel(const float* __restrict__ logits, int Tn, int G, int E,
+                                                            int k, int ke, const int32_t* __restrict__ eidx,
+                                                            float* __restrict__ gate, const int32_t* __restrict__ list,
+                                                            const int* list_n) {
+  pdl_wait();
+  pdl_trigger();
+  const int n = list ? *(volatile const int*)list_n : Tn;
+  for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < n; p += gridDim.x * blockDim.x)
+    across_token(logits + (size_t)p * (G + E) + G, list ? list[p] : p, k, ke, eidx, gate);
 }
 
 // Canonical-order BF16 logits of the listed tokens (the ones the tensor-core router could not
@@ -573,14 +580,14 @@ cudaError_t launch_route(const LayerArgs& a, const void* x, const void* wg, cons
                          float* gate, DevStatus* status, bool status_zeroed, cudaStream_t st) {
   if (a.T == 0) return cudaSuccess;
   cudaError_t err = cudaSuccess;
-  if (a.across) {
+  if (a.across && (fused_route_ok(a) || !route_tc_ok(a))) {
     // canonical logits of every token stay in the workspace: the within-group selection gives the
     // candidate slots, then the picks over their union set the gates
     if ((err = launch_logits(a, a.bf16, x, wg, bg, we, logits, a.T, a.d, a.G, a.E, st)) != cudaSuccess) return err;
     launch_select_any(a, logits, nullptr, nullptr, gidx, eidx, gate, st);
     prof_mark("router_select", st);
     launch_pdl(router_across_kernel, dim3((a.T + 255) / 256), dim3(256), 0, st, (const float*)logits, a.T, a.G, a.E,
-               a.k, a.ke, (const int32_t*)eidx, gate);
+               a.k, a.ke, (const int32_t*)eidx, gate, (const int32_t*)nullptr, (const int*)nullptr);
     prof_mark("router_across", st);
     return cudaGetLastError();
   }
@@ -595,6 +602,12 @@ cudaError_t launch_route(const LayerArgs& a, const void* x, const void* wg, cons
     prof_mark("router_exact_list", st);
     launch_select_any(a, logits, redo, n, gidx, eidx, gate, st);
     prof_mark("router_select_list", st);
+    if (a.across) {
+      // the tensor-core router set the verified tokens' gates itself; the listed ones here
+      launch_pdl(router_across_kernel, dim3(148), dim3(256), 0, st, (const float*)logits, a.T, a.G, a.E, a.k, a.ke,
+                 (const int32_t*)eidx, gate, (const int32_t*)redo, n);
+      prof_mark("router_across_list", st);
+    }
     return cudaGetLastError();
   }
   if (launch_fused_route(a, x, wg, bg, we, gidx, eidx, gate, st, &err)) return err != cudaSuccess ? err : cudaGetLastError();

@@ -41,6 +41,7 @@ struct RtcArgs {
   int32_t* redo;        // tokens left to the canonical kernels
   DevStatus* status;    // status->route_redo counts them
   float* dbg;           // null, or [T][2 (G + E)]: each token's logits (groups, then experts) and deltas
+  int across;           // MOE_ROUTE_ACROSS: gates from the top k_e over the union of the chosen groups
 };
 
 // Sum of squares of one 64-element row of a 128-byte-swizzled tile, into two pairs of partial
@@ -262,6 +263,32 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(
           for (int e = 0; e < E; ++e) { o[G + e] = lv[Gp + e]; o[2 * G + E + e] = delta(Gp + e); }
         }
         const int K = tab.K, kg = p.kg, ke = p.ke, k = kg * ke;
+        // The across-groups reading: the top k_e over the union of the chosen groups' members
+        // (candidate i: member i % K of chosen group i / K), verified like the other picks; gates
+        // = softmax over them in pick order on their slots (the within-group candidates already
+        // written to eidx), zero on the other slots.
+        auto across_gates = [&](const int (&gsel)[kRtcMaxPick]) -> bool {
+          auto eid = [&](int i) { return (int)s_member[gsel[i / K] * K + i % K]; };
+          int pidx[kRtcMaxPick];
+          float pv[kRtcMaxPick];
+          if (!pick_verified(
+                  kg * K, ke, [&](int i) { return lv[Gp + eid(i)]; }, [&](int i) { return delta(Gp + eid(i)); }, eid,
+                  pidx, pv))
+            return false;
+          float q[kRtcMaxPick], den = 0.f;
+#pragma unroll
+          for (int j = 0; j < kRtcMaxPick; ++j)
+            if (j < ke) { q[j] = expf(pv[j] - pv[0]); den += q[j]; }
+          for (int s2 = 0; s2 < k; ++s2) {
+            const int e = p.eidx[(size_t)t * k + s2];
+            float gv2 = 0.f;
+#pragma unroll
+            for (int j = 0; j < kRtcMaxPick; ++j)
+              if (j < ke && eid(pidx[j]) == e) gv2 = q[j] / den;
+            p.gate[(size_t)t * k + s2] = gv2;
+          }
+          return true;
+        };
         if (G <= 8 && K <= 8) {
           // register path
           float v8[8], d8[8], gv[kRtcMaxPick];
@@ -305,6 +332,7 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(
               p.gate[(size_t)t * k + j * ke + s2] = pj * (qe[s2] / qden);
             }
           }
+          if (ok && p.across) ok = across_gates(gsel);
           unsafe = !ok;
         } else {
         int gsel[kRtcMaxPick];
@@ -341,6 +369,7 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(
             p.gate[(size_t)t * k + j * ke + s2] = pj * (qe[s2] / qden);
           }
         }
+        if (ok && p.across) ok = across_gates(gsel);
         unsafe = !ok;
         }
       }
@@ -394,6 +423,7 @@ cudaError_t launch_route_tc(const LayerArgs& a, const void* x, const void* wg, c
   p.bg = bg; p.T = a.T; p.nk = a.d / 64; p.N = route_tc_columns(a); p.Gp = (a.G + 7) / 8 * 8;
   p.c_err = route_tc_c_err(a.d); p.kg = a.kg; p.ke = a.ke;
   p.gidx = gidx; p.eidx = eidx; p.gate = gate; p.redo = redo; p.status = status; p.dbg = dbg;
+  p.across = a.across ? 1 : 0;
   const size_t stage = (size_t)(kRtcTile + p.N) * 128;
   p.stages = (int)((kRtcSmem - 1024) / stage);
   if (p.stages > kRtcMaxStages) p.stages = kRtcMaxStages;
