@@ -365,45 +365,47 @@ static void launch_select_any(const LayerArgs& a, const float* logits, const int
 // order, as the within-group gates), every other slot gate 0.  One thread per token.
 __device__ __forceinline__ void across_token(const float* __restrict__ se, int t, int k, int ke,
                                              const int32_t* __restrict__ eidx, float* __restrict__ gate) {
+  // every array index below is a compile-time constant (unrolled loops), so all stays in registers
   int id[kMaxK];
-  float v[kMaxK], q[kMaxK];
-  int slot[kMaxK];
+  float v[kMaxK];
 #pragma unroll
   for (int s = 0; s < kMaxK; ++s) {
     id[s] = s < k ? eidx[(size_t)t * k + s] : 0;
     v[s] = s < k ? se[id[s]] : 0.f;
-    slot[s] = 0;
   }
   uint32_t picked = 0;
+  float q[kMaxK];
+  uint32_t pick_mask[kMaxK];
   float den = 0.f, v0 = 0.f;
 #pragma unroll
   for (int j = 0; j < kMaxK; ++j) {
-    if (j >= ke) break;
-    int bi = -1;
-#pragma unroll
-    for (int s = 0; s < kMaxK; ++s) {
-      const bool cand = s < k && !((picked >> s) & 1u);
-      if (cand && (bi < 0 || v[s] > v[bi] || (v[s] == v[bi] && id[s] < id[bi]))) bi = s;
-    }
-    picked |= 1u << bi;
-    slot[j] = bi;
-    if (j == 0) v0 = v[bi];
-    q[j] = expf(v[bi] - v0);
-    den += q[j];
-  }
-  float g[kMaxK];
-#pragma unroll
-  for (int s = 0; s < kMaxK; ++s) g[s] = 0.f;
-#pragma unroll
-  for (int j = 0; j < kMaxK; ++j)
+    q[j] = 0.f;
+    pick_mask[j] = 0u;
     if (j < ke) {
+      float bv = 0.f;
+      int bid = 0;
+      uint32_t bmask = 0u;
 #pragma unroll
-      for (int s = 0; s < kMaxK; ++s)
-        if (s == slot[j]) g[s] = q[j] / den;
+      for (int s = 0; s < kMaxK; ++s) {
+        const bool cand = s < k && !((picked >> s) & 1u);
+        if (cand && (bmask == 0u || v[s] > bv || (v[s] == bv && id[s] < bid))) { bv = v[s]; bid = id[s]; bmask = 1u << s; }
+      }
+      picked |= bmask;
+      pick_mask[j] = bmask;
+      if (j == 0) v0 = bv;
+      q[j] = expf(bv - v0);
+      den += q[j];
     }
+  }
 #pragma unroll
-  for (int s = 0; s < kMaxK; ++s)
-    if (s < k) gate[(size_t)t * k + s] = g[s];
+  for (int s = 0; s < kMaxK; ++s) {
+    if (s >= k) break;
+    float g = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+      if ((pick_mask[j] >> s) & 1u) g = q[j] / den;
+    gate[(size_t)t * k + s] = g;
+  }
 }
 
 // With a list (the tokens the tensor-core router left over), logits row p belongs to token
