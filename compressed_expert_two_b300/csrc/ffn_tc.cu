@@ -990,7 +990,8 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up_tc_kernel(
         eid[s] = e;
         gt[s] = p.gate[(size_t)t * k + j * KE + s];
       }
-      urow = p.U + (size_t)i * 2 * KRP + half * KRP;
+      urow = p.U + (p.u_by_token ? (size_t)t * p.G * 2 * KRP + (size_t)g * 2 * KRP : (size_t)i * 2 * KRP) +
+             half * KRP;
     }
     // V accumulators: half h keeps the slots s with s % 2 == h (vacc[s / 2])
     constexpr int KV = (KE + 1) / 2;
@@ -2194,7 +2195,7 @@ static PrepArgs prep_args(const LayerArgs& a, const ResidPtrs& rp, const TcBufs&
 }
 
 bool tc_u_dense(const LayerArgs& a) {
-  return tc_path_ok(a) && a.R > kUSimtMaxRows && up3_ok(a) && a.G * 2 * tc_krp(a) <= 512;
+  return tc_path_ok(a) && a.R > kUSimtMaxRows && a.G * 2 * tc_krp(a) <= 512;
 }
 
 // 1. residual stacks (weights only: may run on another stream, concurrently with the routing),
