@@ -687,6 +687,12 @@ def run_offload(args, slots: int = 4):
         torch.cuda.synchronize(dev)
         best = max(best, (1 << 30) / (a.elapsed_time(b) / 1e3) / 1e9)
     off.close()
+    cpu = None
+    if not args.no_cpu_baseline:
+        tps, n_tok, el = oracle_tokens_per_s(inp, args.cpu_seconds, cfg.T)
+        cpu = {"value": round(tps, 3), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{n_tok} tokens of the same layer ({cfg.T} per step; route + FP64 FFN with every W~ "
+                         f"materialised) in {el:.1f} s"}
     copied = st1["bytes_copied"] - st0["bytes_copied"]
     misses, hits = st1["misses"] - st0["misses"], st1["hits"] - st0["hits"]
     group_bytes = 3 * cfg.d * cfg.f * 2
@@ -703,7 +709,8 @@ def run_offload(args, slots: int = 4):
                       "hit_rate": round(hits / max(hits + misses, 1), 4),
                       "bytes_copied_per_step": round(copied / n), "h2d_gbs": round(copied / wall / 1e9, 2),
                       "pinned_h2d_peak_gbs": round(best, 2), "h2d_frac": round(copied / wall / 1e9 / best, 4)},
-            "timing": "wall clock over the steps (host synchronisation per step for the hit groups included)"}
+            "timing": "wall clock over the steps (host synchronisation per step for the hit groups included)",
+            "cpu_baseline": cpu}
 
 
 def main():

@@ -94,6 +94,12 @@ CASES = {
     "bf16_across_few_tokens": small(T=300, E=32, G=4, kg=2, ke=2, seed=56, resid_std=0.2, route="across"),
     "f32_across": small(T=130, dtype="f32", resid="f32", r=4, kg=2, ke=2, E=12, G=3, seed=57, resid_std=0.2,
                         route="across"),
+    # the descriptor's limits: 256 experts, 32 per group, 16 routed experts per token (2 x 8), rank 64
+    "bf16_max_experts_k16": small(T=130, d=256, f=128, E=256, G=8, kg=2, ke=8, group_map="perm", seed=65,
+                                  resid_std=0.2),
+    "bf16_max_experts_k16_many_tokens": small(T=1100, d=256, f=128, E=256, G=8, kg=2, ke=8, group_map="contiguous",
+                                            seed=66, resid_std=0.2),
+    "f32_rank64": small(T=70, dtype="f32", resid="f32", r=64, kg=1, ke=2, E=8, G=2, seed=67, resid_std=0.05),
 }
 
 
