@@ -1608,6 +1608,16 @@ __global__ void __launch_bounds__(kUp3Warps * 32, 1) ffn_up3_kernel(
 // ------------------------------------------------------------------------------------------
 constexpr int kUp4EpiWarps = 8;
 constexpr int kStages4p = 5;
+// registers per thread: at launch (the __launch_bounds__ limit for 384 threads, one CTA per SM),
+// and after the split between warpgroup 0 (producers, issuers) and the two epilogue warpgroups
+// (the counts at which neither side spills, per number of slots)
+constexpr int kUp4RegsLaunch = 168;
+template <int KE> constexpr int kUp4RegsLow = KE == 1 ? 88 : 120;
+template <int KE> constexpr int kUp4RegsHigh = KE == 1 ? 208 : 192;
+static_assert(kUpWarps == 12 && kUpEpiWarp0 == 4 && kUp4EpiWarps == 8, "one producer warpgroup, two epilogue");
+static_assert(4 * kUp4RegsLow<1> + 8 * kUp4RegsHigh<1> <= 12 * kUp4RegsLaunch &&
+                  4 * kUp4RegsLow<2> + 8 * kUp4RegsHigh<2> <= 12 * kUp4RegsLaunch,
+              "the split must not exceed the launch's registers");
 
 template <int KE>
 __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up4p_kernel(
@@ -1632,13 +1642,19 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up4p_kernel(
   __shared__ int abort_flag;
 
   const uint32_t rank = tc::cluster_rank();
-  int g, r0, r1;
-  if (!pair_tile_of(p.row_begin, p.G, blockIdx.x >> 1, (int)rank, g, r0, r1)) return;   // same for both CTAs
-  const int chunk = blockIdx.y;
-  const int ft0 = chunk * p.ftiles_per_chunk;
-  const int ft1 = min(ft0 + p.ftiles_per_chunk, p.n_ftiles);
-  if (ft0 >= ft1) return;
-  const int nft = ft1 - ft0;
+  // work items w = chunk * n_row_tiles + pair tile, chunk-major so that the clusters running at
+  // once share a chunk's W tiles and keep re-reading the same X rows; cluster c takes items
+  // c, c + clusters, ...  Both CTAs of a cluster walk the same items (a pair tile is empty for
+  // both or for neither), every role skips the empty ones alike, and the stage ring, accumulator
+  // parity and slot phases run on across items (glt: tiles, sig: slots over the cluster's items).
+  const int cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
+  const int n_items = p.n_row_tiles * p.n_chunks;
+  auto item = [&](int w, int& g, int& r0, int& r1, int& ft0, int& nft) -> bool {
+    if (!pair_tile_of(p.row_begin, p.G, w % p.n_row_tiles, (int)rank, g, r0, r1)) return false;
+    ft0 = (w / p.n_row_tiles) * p.ftiles_per_chunk;
+    nft = min(ft0 + p.ftiles_per_chunk, p.n_ftiles) - ft0;
+    return nft > 0;
+  };
   const int nkb = p.d / 64;
   const int f = p.f;
 
@@ -1680,269 +1696,302 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up4p_kernel(
     __syncwarp();
     if (lane == 0) tc::bar_arrive(b);
   };
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer (both CTAs): own X rows and own W tile (rank 0 gate, rank 1 up)
-      tc::prefetch_map(&mX); tc::prefetch_map(rank == 0 ? &mWg : &mWu);
-      const uint32_t full0 = tc::map_shared(tc::smem_u32(&full[0]), 0);
-      int kc = 0;
-      bool ok = true;
-      for (int lt = 0; lt < nft && ok; ++lt) {
-        const int n0 = (ft0 + lt) * NF;
-        for (int kb = 0; kb < nkb; ++kb, ++kc) {
-          const int s = kc % STAGES, it = kc / STAGES;
-          if (kc >= STAGES && !tc::bar_wait_cluster(&empty[s], (it - 1) & 1, ab, 91)) { ok = false; break; }
-          uint8_t* st = sStage + s * STAGE_BYTES;
-          if (rank == 0) tc::bar_expect_tx(&full[s], 2 * STAGE_BYTES);
-          tc::tma_load_2d_pair(st, &mX, full0 + 8 * s, kb * 64, r0);
-          tc::tma_load_2d_pair(st + X_BYTES, rank == 0 ? &mWg : &mWu, full0 + 8 * s, kb * 64,
-                               (int)p.tab.wslot[g] * f + n0);
+  // the single-lane producer and issuer roles (warpgroup 0) hand registers to the epilogue
+  // warpgroups, whose per-thread V partials, gated h sums and TMEM reads do not fit in the
+  // launch's even share: 4 x 32 x low + 8 x 32 x high <= 384 x kUp4RegsLaunch
+  if (warp < kUpEpiWarp0) {
+    tc::setmaxnreg_dec<kUp4RegsLow<KE>>();
+    if (warp == 0) {
+      if (lane == 0) {
+        // ---------------- TMA producer (both CTAs): own X rows and own W tile (rank 0 gate, rank 1 up)
+        tc::prefetch_map(&mX); tc::prefetch_map(rank == 0 ? &mWg : &mWu);
+        const uint32_t full0 = tc::map_shared(tc::smem_u32(&full[0]), 0);
+        int kc = 0;
+        bool ok = true;
+        for (int w = cluster; w < n_items && ok; w += clusters) {
+          int g, r0, r1, ft0, nft;
+          if (!item(w, g, r0, r1, ft0, nft)) continue;
+          for (int lt = 0; lt < nft && ok; ++lt) {
+            const int n0 = (ft0 + lt) * NF;
+            for (int kb = 0; kb < nkb; ++kb, ++kc) {
+              const int s = kc % STAGES, it = kc / STAGES;
+              if (kc >= STAGES && !tc::bar_wait_cluster(&empty[s], (it - 1) & 1, ab, 91)) { ok = false; break; }
+              uint8_t* st = sStage + s * STAGE_BYTES;
+              if (rank == 0) tc::bar_expect_tx(&full[s], 2 * STAGE_BYTES);
+              tc::tma_load_2d_pair(st, &mX, full0 + 8 * s, kb * 64, r0);
+              tc::tma_load_2d_pair(st + X_BYTES, rank == 0 ? &mWg : &mWu, full0 + 8 * s, kb * 64,
+                                   (int)p.tab.wslot[g] * f + n0);
+            }
+          }
         }
+        // every commit rank 0 sends to this CTA's stage barriers has landed before the CTA exits
+        if (ok) {
+          for (int s = 0; s < STAGES && s < kc; ++s)
+            if (!tc::bar_wait_cluster(&empty[s], ((kc - 1 - s) / STAGES) & 1, ab, 92)) break;
+        }
+        if (abort_flag) tc::drain_copies();
       }
-      // every commit rank 0 sends to this CTA's stage barriers has landed before the CTA exits
-      if (ok) {
-        for (int s = 0; s < STAGES && s < kc; ++s)
-          if (!tc::bar_wait_cluster(&empty[s], ((kc - 1 - s) / STAGES) & 1, ab, 92)) break;
+    } else if (warp == 3) {
+      if (lane == 0) {
+        // ---------------- TMA producer of the residual tiles: this CTA's halves of B_gate / B_up
+        //                  (pair loads, counted on rank 0) and the whole A_down^T tile (local)
+        tc::prefetch_map(&mBg); tc::prefetch_map(&mBu); tc::prefetch_map(&mAdt);
+        const uint32_t rb0 = tc::map_shared(tc::smem_u32(&rb_full), 0);
+        bool ok = true;
+        int glt = 0;
+        for (int w = cluster; w < n_items && ok; w += clusters) {
+          int g, r0, r1, ft0, nft;
+          if (!item(w, g, r0, r1, ft0, nft)) continue;
+          for (int lt = 0; lt < nft; ++lt, ++glt) {
+            const int n0 = (ft0 + lt) * NF;
+            if (glt > 0 && !tc::bar_wait_cluster(&rb_empty, (glt - 1) & 1, ab, 93)) { ok = false; break; }
+            if (rank == 0) tc::bar_expect_tx(&rb_full, 4 * BRES_BYTES);
+            tc::tma_load_2d_pair(sBg, &mBg, rb0, 0, g * f + n0 + (int)rank * (NF / 2));
+            tc::tma_load_2d_pair(sBu, &mBu, rb0, 0, g * f + n0 + (int)rank * (NF / 2));
+            if (glt > 0 && !tc::bar_wait(&ad_empty, (glt - 1) & 1, ab, 94)) { ok = false; break; }
+            tc::bar_expect_tx(&ad_full, ADT_BYTES);
+            tc::tma_load_2d(sAdt, &mAdt, &ad_full, 0, g * f + n0);
+          }
+        }
+        // rank 0's last release of the residual tiles has landed before the CTA exits
+        if (ok && glt > 0) tc::bar_wait_cluster(&rb_empty, (glt - 1) & 1, ab, 95);
+        if (abort_flag) tc::drain_copies();
       }
-      if (abort_flag) tc::drain_copies();
-    }
-  } else if (warp == 3) {
-    if (lane == 0) {
-      // ---------------- TMA producer of the residual tiles: this CTA's halves of B_gate / B_up
-      //                  (pair loads, counted on rank 0) and the whole A_down^T tile (local)
-      tc::prefetch_map(&mBg); tc::prefetch_map(&mBu); tc::prefetch_map(&mAdt);
-      const uint32_t rb0 = tc::map_shared(tc::smem_u32(&rb_full), 0);
-      bool ok = true;
-      for (int lt = 0; lt < nft; ++lt) {
-        const int n0 = (ft0 + lt) * NF;
-        if (lt > 0 && !tc::bar_wait_cluster(&rb_empty, (lt - 1) & 1, ab, 93)) { ok = false; break; }
-        if (rank == 0) tc::bar_expect_tx(&rb_full, 4 * BRES_BYTES);
-        tc::tma_load_2d_pair(sBg, &mBg, rb0, 0, g * f + n0 + (int)rank * (NF / 2));
-        tc::tma_load_2d_pair(sBu, &mBu, rb0, 0, g * f + n0 + (int)rank * (NF / 2));
-        if (lt > 0 && !tc::bar_wait(&ad_empty, (lt - 1) & 1, ab, 94)) { ok = false; break; }
-        tc::bar_expect_tx(&ad_full, ADT_BYTES);
-        tc::tma_load_2d(sAdt, &mAdt, &ad_full, 0, g * f + n0);
-      }
-      // rank 0's last release of the residual tiles has landed before the CTA exits
-      if (ok && nft > 0) tc::bar_wait_cluster(&rb_empty, (nft - 1) & 1, ab, 95);
-      if (abort_flag) tc::drain_copies();
-    }
-  } else if (warp == 1) {
-    if (lane == 0 && rank == 0) {
-      // ---------------- base MMA issuer (rank 0): acc[lt & 1] = X [Wg | Wu]^T, M = 256, N = 256
-      constexpr uint32_t id_base = tc::idesc_bf16(2 * kTile, 2 * NF);
-      int kc = 0;
-      bool ok = true;
-      for (int lt = 0; lt < nft && ok; ++lt) {
-        const int b = lt & 1;
-        if (lt >= 2 && !tc::bar_wait_cluster(&acc_empty[b], ((lt >> 1) - 1) & 1, ab, 96)) break;
-        tc::fence_after();
-        const uint32_t dcol = tmem + b * 2 * NF;
-        for (int kb = 0; kb < nkb; ++kb, ++kc) {
-          const int s = kc % STAGES, it = kc / STAGES;
-          if (!tc::bar_wait_cluster(&full[s], it & 1, ab, 97)) { ok = false; break; }
-          tc::fence_after();
-          const uint32_t a0 = tc::smem_u32(sStage + s * STAGE_BYTES);
-          const uint32_t b0 = a0 + X_BYTES;
+    } else if (warp == 1) {
+      if (lane == 0 && rank == 0) {
+        // ---------------- base MMA issuer (rank 0): acc[lt & 1] = X [Wg | Wu]^T, M = 256, N = 256
+        constexpr uint32_t id_base = tc::idesc_bf16(2 * kTile, 2 * NF);
+        int kc = 0, glt = 0;
+        bool ok = true;
+        for (int w = cluster; w < n_items && ok; w += clusters) {
+          int g, r0, r1, ft0, nft;
+          if (!item(w, g, r0, r1, ft0, nft)) continue;
+          for (int lt = 0; lt < nft && ok; ++lt, ++glt) {
+            const int b = glt & 1;
+            if (glt >= 2 && !tc::bar_wait_cluster(&acc_empty[b], ((glt >> 1) - 1) & 1, ab, 96)) { ok = false; break; }
+            tc::fence_after();
+            const uint32_t dcol = tmem + b * 2 * NF;
+            for (int kb = 0; kb < nkb; ++kb, ++kc) {
+              const int s = kc % STAGES, it = kc / STAGES;
+              if (!tc::bar_wait_cluster(&full[s], it & 1, ab, 97)) { ok = false; break; }
+              tc::fence_after();
+              const uint32_t a0 = tc::smem_u32(sStage + s * STAGE_BYTES);
+              const uint32_t b0 = a0 + X_BYTES;
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            tc::mma_bf16_pair(dcol, tc::sdesc(a0 + 32 * k), tc::sdesc(b0 + 32 * k), id_base, (kb | k) != 0);
-          tc::mma_commit_pair(&empty[s], 3);
+              for (int k = 0; k < 4; ++k)
+                tc::mma_bf16_pair(dcol, tc::sdesc(a0 + 32 * k), tc::sdesc(b0 + 32 * k), id_base, (kb | k) != 0);
+              tc::mma_commit_pair(&empty[s], 3);
+            }
+            if (!ok) break;
+            tc::mma_commit_pair(&base_full[b], 1);
+          }
         }
-        if (!ok) break;
-        tc::mma_commit_pair(&base_full[b], 1);
+        tc::mma_commit_pair(&fin1, 1);
+        const uint64_t t0 = tc::now_ns();
+        while (!tc::bar_test(&fin1, 0) && tc::now_ns() - t0 < tc::kWaitNs) {}
       }
-      tc::mma_commit_pair(&fin1, 1);
-      const uint64_t t0 = tc::now_ns();
-      while (!tc::bar_test(&fin1, 0) && tc::now_ns() - t0 < tc::kWaitNs) {}
-    }
-  } else if (warp == 2) {
-    if (lane == 0 && rank == 0) {
-      // ---------------- residual issuer (rank 0): acc[b] += D_s [Bg | Bu]^T, M = 256, two N = 128
-      constexpr uint32_t id_res = tc::idesc_f16(2 * kTile, NF);
-      const uint32_t ug = tc::smem_u32(sUg), uu = tc::smem_u32(sUu);
-      const uint32_t bg = tc::smem_u32(sBg), bu = tc::smem_u32(sBu);
-      const int n_slots = nft * KE;
-      bool ok = true;
-      for (int sig = 0; sig < n_slots && ok; ++sig) {
-        const int lt = sig / KE, s = sig % KE, b = lt & 1;
-        if (s == 0) {
-          if (!tc::bar_wait(&base_full[b], (lt >> 1) & 1, ab, 98)) { ok = false; break; }
-          if (!tc::bar_wait_cluster(&rb_full, lt & 1, ab, 99)) { ok = false; break; }
-        }
-        if (!tc::bar_wait_cluster(&u_ready, sig & 1, ab, 100)) { ok = false; break; }
-        if (s > 0 && !tc::bar_wait_cluster(&acc_read, (sig - 1) & 1, ab, 101)) { ok = false; break; }
-        tc::fence_after();
-        const uint32_t dcol = tmem + b * 2 * NF;
+    } else if (warp == 2) {
+      if (lane == 0 && rank == 0) {
+        // ---------------- residual issuer (rank 0): acc[b] += D_s [Bg | Bu]^T, M = 256, two N = 128
+        constexpr uint32_t id_res = tc::idesc_f16(2 * kTile, NF);
+        const uint32_t ug = tc::smem_u32(sUg), uu = tc::smem_u32(sUu);
+        const uint32_t bg = tc::smem_u32(sBg), bu = tc::smem_u32(sBu);
+        bool ok = true;
+        int sig = 0;
+        for (int w = cluster; w < n_items && ok; w += clusters) {
+          int g, r0, r1, ft0, nft;
+          if (!item(w, g, r0, r1, ft0, nft)) continue;
+          for (int ls = 0; ls < nft * KE && ok; ++ls, ++sig) {
+            const int glt = sig / KE, s = sig % KE, b = glt & 1;
+            if (s == 0) {
+              if (!tc::bar_wait(&base_full[b], (glt >> 1) & 1, ab, 98)) { ok = false; break; }
+              if (!tc::bar_wait_cluster(&rb_full, glt & 1, ab, 99)) { ok = false; break; }
+            }
+            if (!tc::bar_wait_cluster(&u_ready, sig & 1, ab, 100)) { ok = false; break; }
+            if (s > 0 && !tc::bar_wait_cluster(&acc_read, (sig - 1) & 1, ab, 101)) { ok = false; break; }
+            tc::fence_after();
+            const uint32_t dcol = tmem + b * 2 * NF;
 #pragma unroll
-        for (int kk = 0; kk < KRP / 16; ++kk) {
-          const uint32_t off = (kk & 3) * 32;
-          tc::mma_bf16_pair(dcol, tc::sdesc(ug + off), tc::sdesc(bg + off), id_res, 1u);
-          tc::mma_bf16_pair(dcol + NF, tc::sdesc(uu + off), tc::sdesc(bu + off), id_res, 1u);
+            for (int kk = 0; kk < KRP / 16; ++kk) {
+              const uint32_t off = (kk & 3) * 32;
+              tc::mma_bf16_pair(dcol, tc::sdesc(ug + off), tc::sdesc(bg + off), id_res, 1u);
+              tc::mma_bf16_pair(dcol + NF, tc::sdesc(uu + off), tc::sdesc(bu + off), id_res, 1u);
+            }
+            tc::mma_commit_pair(&acc_full, 3);
+            if (s == KE - 1) tc::mma_commit_pair(&rb_empty, 3);
+          }
         }
-        tc::mma_commit_pair(&acc_full, 3);
-        if (s == KE - 1) tc::mma_commit_pair(&rb_empty, 3);
+        tc::mma_commit_pair(&fin2, 1);
+        const uint64_t t0 = tc::now_ns();
+        while (!tc::bar_test(&fin2, 0) && tc::now_ns() - t0 < tc::kWaitNs) {}
       }
-      tc::mma_commit_pair(&fin2, 1);
-      const uint64_t t0 = tc::now_ns();
-      while (!tc::bar_test(&fin2, 0) && tc::now_ns() - t0 < tc::kWaitNs) {}
     }
-  } else if (warp >= kUpEpiWarp0) {
+  } else {
+    tc::setmaxnreg_inc<kUp4RegsHigh<KE>>();
     // ---------------- epilogue (both CTAs): one thread per (tile row, half of 64 d_ff columns)
-    const int q = warp & 3, half = (warp - kUpEpiWarp0) >> 2, row = q * 32 + lane, i = r0 + row;
+    const int q = warp & 3, half = (warp - kUpEpiWarp0) >> 2, row = q * 32 + lane;
     auto ewait = [&](uint64_t* b, uint32_t par, int where) -> bool {
       const bool r = tc::bar_wait_cluster(b, par, ab, where);
       return __all_sync(0xffffffffu, r);
     };
-    const bool valid = i < r1;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const int c0 = half * 64;
     uint8_t* sU = half == 0 ? sUg : sUu;
-    int le[KE];
-    float gt[KE];
-#pragma unroll
-    for (int s = 0; s < KE; ++s) { le[s] = 0; gt[s] = 0.f; }
-    const __half* urow = p.U;
-    if (valid) {
-      const int b = p.row_asg[i], t = b / p.kg, j = b % p.kg, k = p.kg * KE;
-#pragma unroll
-      for (int s = 0; s < KE; ++s) {
-        const int e = p.eidx[(size_t)t * k + j * KE + s];
-        le[s] = p.tab.local_of[e];
-        gt[s] = p.gate[(size_t)t * k + j * KE + s];
-      }
-      urow = p.U + (p.u_by_token ? (size_t)t * p.G * 2 * KRP + (size_t)g * 2 * KRP : (size_t)i * 2 * KRP) +
-             half * KRP;
-    }
+    // this row of this half's U~ starts at zero (later items find the previous item's last delta
+    // there, which the first delta of the item clears)
     {
       uint4* z = reinterpret_cast<uint4*>(sU + (row >> 3) * 1024 + (row & 7) * 128);
 #pragma unroll
       for (int c = 0; c < 8; ++c) z[c] = make_uint4(0, 0, 0, 0);
     }
-    auto load_u = [&](int s, uint32_t (&pk)[8]) {
-      if (!valid) return;
-      const uint4* u4 = reinterpret_cast<const uint4*>(urow + le[s] * kRank);
-      const uint4 a = u4[0], b = u4[1];
-      pk[0] = a.x; pk[1] = a.y; pk[2] = a.z; pk[3] = a.w;
-      pk[4] = b.x; pk[5] = b.y; pk[6] = b.z; pk[7] = b.w;
-    };
-    auto zero_block = [&](int blk) {
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, blk * kRank, kTile)) = z;
-      *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, blk * kRank + 8, kTile)) = z;
-    };
+    // U~ holds the last delta: +values in block nz_pos, -values in block nz_neg (or none)
     int nz_pos = -1, nz_neg = -1;
     uint32_t unext[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) unext[c] = 0u;
-    auto build_delta = [&](int s) {
-      if (!valid) return;
-      const int pos = le[s], neg = s > 0 ? le[s - 1] : -1;
-      if (neg >= 0) {
-        uint4* b0 = reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, neg * kRank, kTile));
-        uint4* b1 = reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, neg * kRank + 8, kTile));
-        const uint4 v0 = *b0, v1 = *b1;
-        constexpr uint32_t F = 0x80008000u;          // exact FP16 negation
-        *b0 = make_uint4(v0.x ^ F, v0.y ^ F, v0.z ^ F, v0.w ^ F);
-        *b1 = make_uint4(v1.x ^ F, v1.y ^ F, v1.z ^ F, v1.w ^ F);
-      }
-      if (nz_neg >= 0 && nz_neg != pos && nz_neg != neg) zero_block(nz_neg);
-      if (nz_pos >= 0 && nz_pos != pos && nz_pos != neg) zero_block(nz_pos);
-      *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, pos * kRank, kTile)) =
-          make_uint4(unext[0], unext[1], unext[2], unext[3]);
-      *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, pos * kRank + 8, kTile)) =
-          make_uint4(unext[4], unext[5], unext[6], unext[7]);
-      nz_pos = pos; nz_neg = neg;
-    };
-
-    load_u(0, unext);
-    build_delta(0);
-    tc::fence_async_smem();
-    warp_arrive0(&u_ready);
-    if (KE > 1) load_u(KE > 1 ? 1 : 0, unext);
-    else if (nft > 1) load_u(0, unext);
-
-    // V partials of this row over this thread's columns, per slot, as FP32 pairs (k, k + 1)
-    float2 vacc[KE][kRank / 2];
-#pragma unroll
-    for (int s = 0; s < KE; ++s)
-#pragma unroll
-      for (int k = 0; k < kRank / 2; ++k) vacc[s][k] = make_float2(0.f, 0.f);
-
     bool ok = true;
-    int sig = 0;
-    for (int lt = 0; lt < nft && ok; ++lt) {
-      const int bsel = lt & 1;
-      const uint32_t acc_col = bsel * 2 * NF;
-      if (!ewait(&ad_full, lt & 1, 102)) { ok = false; break; }
-      float hs[64];
+    int sig = 0, glt = 0;
+    for (int w = cluster; w < n_items && ok; w += clusters) {
+      int g, r0, r1, ft0, nft;
+      if (!item(w, g, r0, r1, ft0, nft)) continue;
+      const int i = r0 + row, chunk = w / p.n_row_tiles;
+      const bool valid = i < r1;
+      int le[KE];
+      float gt[KE];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) hs[c] = 0.f;
-#pragma unroll
-      for (int s = 0; s < KE; ++s, ++sig) {
-        if (!ewait(&acc_full, sig & 1, 103)) { ok = false; break; }
-        tc::fence_after();
-        const uint8_t* arow = sAdt + le[s] * kRank * 2;       // this row's expert block, column stride KRP
-#pragma unroll
-        for (int bt = 0; bt < 4; ++bt) {
-          uint32_t av[16], bv[16];
-          tc::tmem_ld16(tmem + lane_off + acc_col + c0 + 16 * bt, av);
-          tc::tmem_ld16(tmem + lane_off + acc_col + NF + c0 + 16 * bt, bv);
-          tc::tmem_ld_wait();
-          if (bt == 3) {
-            // this thread has read acc for this slot: the next slot's residual may land
-            tc::fence_before();
-            warp_arrive0(&acc_read);
-            if (s == KE - 1) warp_arrive0(&acc_empty[bsel]);
-          }
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float h = silu_fast(__uint_as_float(av[e])) * __uint_as_float(bv[e]);
-            hs[16 * bt + e] += gt[s] * h;
-            // v_k += h * A_down^T[k][c] for the 16 ranks of the row's expert
-            const int c = c0 + 16 * bt + e;
-            const uint4* ap = reinterpret_cast<const uint4*>(arow + (size_t)c * KRP * 2);
-            const uint4 w0 = ap[0], w1 = ap[1];
-            const uint32_t ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-            const float2 h2 = make_float2(h, h);
-#pragma unroll
-            for (int k2 = 0; k2 < 8; ++k2) {
-              const float2 a2 = __half22float2(*reinterpret_cast<const __half2*>(&ww[k2]));
-              vacc[s][k2] = fma2(h2, a2, vacc[s][k2]);
-            }
-          }
-        }
-        const bool more = s + 1 < KE || lt + 1 < nft;
-        if (more) {
-          build_delta(s + 1 < KE ? s + 1 : 0);
-          tc::fence_async_smem();
-          warp_arrive0(&u_ready);
-          const int s2 = (s + 2) % KE;
-          const int lt2 = lt + (s + 2) / KE;
-          if (lt2 < nft) load_u(s2, unext);
-        }
-      }
-      if (!ok) break;
-      warp_arrive(&ad_empty);                        // done with this tile's A_down^T (local)
+      for (int s = 0; s < KE; ++s) { le[s] = 0; gt[s] = 0.f; }
+      const __half* urow = p.U;
       if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(p.hsum + (size_t)i * f + (ft0 + lt) * NF + c0);
+        const int b = p.row_asg[i], t = b / p.kg, j = b % p.kg, k = p.kg * KE;
 #pragma unroll
-        for (int c = 0; c < 64; c += 8)
-          dst[c / 8] = make_uint4(tc::pack_bf16(hs[c], hs[c + 1]), tc::pack_bf16(hs[c + 2], hs[c + 3]),
-                                  tc::pack_bf16(hs[c + 4], hs[c + 5]), tc::pack_bf16(hs[c + 6], hs[c + 7]));
+        for (int s = 0; s < KE; ++s) {
+          const int e = p.eidx[(size_t)t * k + j * KE + s];
+          le[s] = p.tab.local_of[e];
+          gt[s] = p.gate[(size_t)t * k + j * KE + s];
+        }
+        urow = p.U + (p.u_by_token ? (size_t)t * p.G * 2 * KRP + (size_t)g * 2 * KRP : (size_t)i * 2 * KRP) +
+               half * KRP;
       }
-    }
-    if (ok && valid) {
-      // partial over this half's columns: V parts [chunk][half]
-      float* vp = p.Vpart + (((size_t)chunk * 2 + half) * p.R + i) * KE * kRank;
+      auto load_u = [&](int s, uint32_t (&pk)[8]) {
+        if (!valid) return;
+        const uint4* u4 = reinterpret_cast<const uint4*>(urow + le[s] * kRank);
+        const uint4 a = u4[0], b = u4[1];
+        pk[0] = a.x; pk[1] = a.y; pk[2] = a.z; pk[3] = a.w;
+        pk[4] = b.x; pk[5] = b.y; pk[6] = b.z; pk[7] = b.w;
+      };
+      auto zero_block = [&](int blk) {
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, blk * kRank, kTile)) = z;
+        *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, blk * kRank + 8, kTile)) = z;
+      };
+      // writes the delta of slot s (first slot of a tile: no subtraction) from unext
+      auto build_delta = [&](int s) {
+        if (!valid) return;
+        const int pos = le[s], neg = s > 0 ? le[s - 1] : -1;
+        if (neg >= 0) {
+          uint4* b0 = reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, neg * kRank, kTile));
+          uint4* b1 = reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, neg * kRank + 8, kTile));
+          const uint4 v0 = *b0, v1 = *b1;
+          constexpr uint32_t F = 0x80008000u;          // exact FP16 negation
+          *b0 = make_uint4(v0.x ^ F, v0.y ^ F, v0.z ^ F, v0.w ^ F);
+          *b1 = make_uint4(v1.x ^ F, v1.y ^ F, v1.z ^ F, v1.w ^ F);
+        }
+        if (nz_neg >= 0 && nz_neg != pos && nz_neg != neg) zero_block(nz_neg);
+        if (nz_pos >= 0 && nz_pos != pos && nz_pos != neg) zero_block(nz_pos);
+        *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, pos * kRank, kTile)) =
+            make_uint4(unext[0], unext[1], unext[2], unext[3]);
+        *reinterpret_cast<uint4*>(sU + tc::sw128_offset(row, pos * kRank + 8, kTile)) =
+            make_uint4(unext[4], unext[5], unext[6], unext[7]);
+        nz_pos = pos; nz_neg = neg;
+      };
+
+      // U~ is free here: the residual MMA of the previous item's last slot has completed
+      load_u(0, unext);
+      build_delta(0);
+      tc::fence_async_smem();
+      warp_arrive0(&u_ready);
+      if (KE > 1) load_u(KE > 1 ? 1 : 0, unext);
+      else if (nft > 1) load_u(0, unext);
+
+      // V partials of this row over this thread's columns, per slot, as FP32 pairs (k, k + 1)
+      float2 vacc[KE][kRank / 2];
 #pragma unroll
       for (int s = 0; s < KE; ++s)
 #pragma unroll
-        for (int k = 0; k < kRank; k += 4)
-          *reinterpret_cast<float4*>(vp + s * kRank + k) =
-              make_float4(gt[s] * vacc[s][k / 2].x, gt[s] * vacc[s][k / 2].y, gt[s] * vacc[s][k / 2 + 1].x,
-                          gt[s] * vacc[s][k / 2 + 1].y);
+        for (int k = 0; k < kRank / 2; ++k) vacc[s][k] = make_float2(0.f, 0.f);
+
+      for (int lt = 0; lt < nft && ok; ++lt, ++glt) {
+        const int bsel = glt & 1;
+        const uint32_t acc_col = bsel * 2 * NF;
+        if (!ewait(&ad_full, glt & 1, 102)) { ok = false; break; }
+        float hs[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) hs[c] = 0.f;
+#pragma unroll
+        for (int s = 0; s < KE; ++s, ++sig) {
+          if (!ewait(&acc_full, sig & 1, 103)) { ok = false; break; }
+          tc::fence_after();
+          const uint8_t* arow = sAdt + le[s] * kRank * 2;       // this row's expert block, column stride KRP
+#pragma unroll
+          for (int bt = 0; bt < 4; ++bt) {
+            uint32_t av[16], bv[16];
+            tc::tmem_ld16(tmem + lane_off + acc_col + c0 + 16 * bt, av);
+            tc::tmem_ld16(tmem + lane_off + acc_col + NF + c0 + 16 * bt, bv);
+            tc::tmem_ld_wait();
+            if (bt == 3) {
+              // this thread has read acc for this slot: the next slot's residual may land
+              tc::fence_before();
+              warp_arrive0(&acc_read);
+              if (s == KE - 1) warp_arrive0(&acc_empty[bsel]);
+            }
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float h = silu_fast(__uint_as_float(av[e])) * __uint_as_float(bv[e]);
+              hs[16 * bt + e] += gt[s] * h;
+              // v_k += h * A_down^T[k][c] for the 16 ranks of the row's expert
+              const int c = c0 + 16 * bt + e;
+              const uint4* ap = reinterpret_cast<const uint4*>(arow + (size_t)c * KRP * 2);
+              const uint4 w0 = ap[0], w1 = ap[1];
+              const uint32_t ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+              const float2 h2 = make_float2(h, h);
+#pragma unroll
+              for (int k2 = 0; k2 < 8; ++k2) {
+                const float2 a2 = __half22float2(*reinterpret_cast<const __half2*>(&ww[k2]));
+                vacc[s][k2] = fma2(h2, a2, vacc[s][k2]);
+              }
+            }
+          }
+          const bool more = s + 1 < KE || lt + 1 < nft;
+          if (more) {
+            build_delta(s + 1 < KE ? s + 1 : 0);
+            tc::fence_async_smem();
+            warp_arrive0(&u_ready);
+            const int s2 = (s + 2) % KE;
+            const int lt2 = lt + (s + 2) / KE;
+            if (lt2 < nft) load_u(s2, unext);
+          }
+        }
+        if (!ok) break;
+        warp_arrive(&ad_empty);                        // done with this tile's A_down^T (local)
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(p.hsum + (size_t)i * f + (ft0 + lt) * NF + c0);
+#pragma unroll
+          for (int c = 0; c < 64; c += 8)
+            dst[c / 8] = make_uint4(tc::pack_bf16(hs[c], hs[c + 1]), tc::pack_bf16(hs[c + 2], hs[c + 3]),
+                                    tc::pack_bf16(hs[c + 4], hs[c + 5]), tc::pack_bf16(hs[c + 6], hs[c + 7]));
+        }
+      }
+      if (ok && valid) {
+        // partial over this half's columns: V parts [chunk][half]
+        float* vp = p.Vpart + (((size_t)chunk * 2 + half) * p.R + i) * KE * kRank;
+#pragma unroll
+        for (int s = 0; s < KE; ++s)
+#pragma unroll
+          for (int k = 0; k < kRank; k += 4)
+            *reinterpret_cast<float4*>(vp + s * kRank + k) =
+                make_float4(gt[s] * vacc[s][k / 2].x, gt[s] * vacc[s][k / 2].y, gt[s] * vacc[s][k / 2 + 1].x,
+                            gt[s] * vacc[s][k / 2 + 1].y);
+      }
     }
   }
   tc::fence_before();
@@ -2058,22 +2107,31 @@ int tc_krp(const LayerArgs& a) { return ((a.K * a.r + 63) / 64) * 64; }
 // two slots and d_ff is a multiple of 128; otherwise the 128-column one (4).
 static bool up3_ok(const LayerArgs& a) { return tc_krp(a) == 64 && a.ke <= 2 && a.f % kNf3 == 0; }
 
+static bool up4_ok(const LayerArgs& a);
+
 int tc_up_chunks(const LayerArgs& a) {
   const int n_ft = a.f / (up3_ok(a) ? kNf3 : kNf);
-  // the 128-column kernel is persistent: an item boundary costs about a tenth of a tile (the next
-  // item's K loop runs under the previous item's slots); the others pay half a tile per CTA
-  const double item_cost = up3_ok(a) ? 0.5 : 0.1;
+  const bool pair = up4_ok(a);
+  // The 128-column kernel is persistent: an item boundary costs about a tenth of a tile (the next
+  // item's K loop runs under the previous item's slots).  The 256-column kernel pays half a tile
+  // per CTA; so, in effect, does the pair kernel: it walks items as well, but every SM it adds
+  // draws power from the same cap (measured on the Mixtral shape: 2 chunks on 132 SMs beat 56
+  // chunks on all 148 by 3%), so more, smaller items do not pay.
+  const double item_cost = up3_ok(a) || pair ? 0.5 : 0.1;
   const int full = (a.R + kTile - 1) / kTile;
-  int tiles = a.R >= kTile * a.G ? full + (a.G + 1) / 2 : (a.R < a.G ? a.R : a.G);
-  if (tiles < 1) tiles = 1;
-  const int sms = 148;
+  // units per chunk that find rows (a group's last tile is ragged: about half of them add one),
+  // and how many run at once (a CTA per SM, or a pair of CTAs per two SMs)
+  int units = a.R >= kTile * a.G ? full + (a.G + 1) / 2 : (a.R < a.G ? a.R : a.G);
+  if (pair) units = a.R >= 2 * kTile * a.G ? (a.R + 2 * kTile - 1) / (2 * kTile) + (a.G + 1) / 2 : units;
+  if (units < 1) units = 1;
+  const int slots = pair ? 148 / 2 : 148;
   int best = 1;
   double best_cost = 1e30;
   for (int c = 1; c <= n_ft; ++c) {
     const int per = (n_ft + c - 1) / c;
     if (c > 1 && (n_ft + per - 1) / per != c) continue;     // same split as a smaller count
-    const double waves = (double)((tiles * c + sms - 1) / sms);
-    const double cost = waves * (per + item_cost);
+    const double rounds = (double)((units * c + slots - 1) / slots);
+    const double cost = rounds * (per + item_cost);
     if (cost < best_cost - 1e-9) { best_cost = cost; best = c; }
   }
   return best;
@@ -2149,12 +2207,43 @@ static cudaError_t launch_up_ke(const CUtensorMap* maps, const UpArgs& p, int nc
 }
 
 template <int KE>
-static cudaError_t launch_up4p(const CUtensorMap* maps, const UpArgs& p, int nchunks, int pairs, cudaStream_t stream) {
+static cudaError_t launch_up4p(const CUtensorMap* maps, const UpArgs& p, cudaStream_t stream) {
   const size_t smem = 1024 + (size_t)kStages4p * (kTile * 128 + kNf3 * 128) + 2 * (size_t)((kNf3 / 2) * 64 * 2) +
                       (size_t)kNf3 * 64 * 2 + 2 * (size_t)(kTile * 64 * 2);
   static std::atomic<uint64_t> attr{0};
   if (const cudaError_t e = smem_attr_once(ffn_up4p_kernel<KE>, smem, attr); e != cudaSuccess) return e;
-  return launch_pdl_cluster(ffn_up4p_kernel<KE>, dim3(2 * pairs, nchunks), dim3(kUpWarps * 32), dim3(2, 1, 1), smem,
+  // the kernel's warpgroups trade registers on the assumption that it launches with
+  // kUp4RegsLaunch per thread; with any other count the epilogue's increase could never be met
+  static std::atomic<int> regs_checked{0};
+  if (!regs_checked.load(std::memory_order_acquire)) {
+    cudaFuncAttributes fa;
+    if (const cudaError_t e = cudaFuncGetAttributes(&fa, ffn_up4p_kernel<KE>); e != cudaSuccess) return e;
+    if (fa.numRegs != kUp4RegsLaunch) return cudaErrorInvalidConfiguration;
+    regs_checked.store(1, std::memory_order_release);
+  }
+  // one cluster per pair of SMs that can hold one at once, walking the (pair tile, chunk) items
+  // (fewer clusters when there are fewer items)
+  static std::atomic<int> max_clusters[64];
+  int dev = 0;
+  if (const cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return e;
+  int mc = dev >= 0 && dev < 64 ? max_clusters[dev].load(std::memory_order_acquire) : 0;
+  if (mc <= 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kUpWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = 2; at.val.clusterDim.y = 1; at.val.clusterDim.z = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    if (const cudaError_t e = cudaOccupancyMaxActiveClusters(&mc, ffn_up4p_kernel<KE>, &cfg); e != cudaSuccess) return e;
+    if (mc <= 0) return cudaErrorInvalidConfiguration;
+    if (dev >= 0 && dev < 64) max_clusters[dev].store(mc, std::memory_order_release);
+  }
+  const int items = p.n_row_tiles * p.n_chunks;
+  const int clusters = items < mc ? items : mc;
+  return launch_pdl_cluster(ffn_up4p_kernel<KE>, dim3(2 * clusters), dim3(kUpWarps * 32), dim3(2, 1, 1), smem,
                             stream, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
 }
 
@@ -2301,14 +2390,14 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   p.R = R; p.n_ftiles = f / nf_up;
   const int nchunks = tc_up_chunks(a);
   p.ftiles_per_chunk = (p.n_ftiles + nchunks - 1) / nchunks;
-  p.n_row_tiles = tiles;
+  p.n_row_tiles = up4 ? pairs : tiles;         // the pair kernel's items are 256-row pair tiles
   p.n_chunks = nchunks;
   if (up4) {
     CUtensorMap mBgP, mBuP;     // halves of the B_gate / B_up tiles (64 rows per CTA of a pair)
     if (!make_map(&mBgP, b.Bgs, (uint64_t)G * f, KRP, kNf3 / 2) || !make_map(&mBuP, b.Bus, (uint64_t)G * f, KRP, kNf3 / 2))
       return cudaErrorInvalidValue;
     const CUtensorMap mp[6] = {mX, mWg, mWu, mBgP, mBuP, mAdt};
-    e = a.ke == 1 ? launch_up4p<1>(mp, p, nchunks, pairs, st) : launch_up4p<2>(mp, p, nchunks, pairs, st);
+    e = a.ke == 1 ? launch_up4p<1>(mp, p, st) : launch_up4p<2>(mp, p, st);
   } else {
     const CUtensorMap maps[6] = {mX, mWg, mWu, mBg, mBu, mAd};
     if (up3)
