@@ -325,6 +325,15 @@ def test_long_k_gate_up_sampled(T, ke, seed):
     full_size_check("long_k", 40, cfg)
 
 
+@pytest.mark.parametrize("T,kg,ke,seed", [(1100, 2, 3, 61), (2100, 1, 3, 62), (2100, 1, 2, 63), (2300, 1, 1, 64)])
+def test_wide_residual_many_rows_sampled(T, kg, ke, seed):
+    """d_model = 2048 with 8 experts of rank 16 per group (a 128-column residual) and more than
+    2048 rows: the persistent 128-column gate/up kernel over many items with one to three slots,
+    ragged groups; sampled tokens against the oracle."""
+    cfg = small(T=T, d=2048, f=384, E=32, G=4, kg=kg, ke=ke, seed=seed, resid_std=0.2)
+    full_size_check("wide_residual", 48, cfg)
+
+
 def test_persistent_down_gemm_sampled():
     """Many waves of down-projection tiles with a short K loop (d_ff = 256): the persistent grouped
     GEMM with double-buffered accumulators; sampled tokens against the oracle, ragged groups."""
