@@ -561,7 +561,7 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_pair_kernel(
     const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
     const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1, int nk0, int nk1,
     const int32_t* __restrict__ row_begin, int G, int b_stride, int b1_off, void* __restrict__ out, int out_ld,
-    const int32_t* __restrict__ scatter, DevStatus* status, int dense_rows, SlotMap b0s) {
+    const int32_t* __restrict__ scatter, DevStatus* status, int dense_rows, SlotMap b0s, int band) {
   constexpr int BH = BN / 2;                                  // B rows held by each CTA
   constexpr uint32_t A_BYTES = kTile * 128, B_BYTES = BH * 128, STAGE_BYTES = A_BYTES + B_BYTES;
   extern __shared__ uint8_t smem_raw[];
@@ -573,19 +573,30 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_pair_kernel(
 
   const uint32_t rank = tc::cluster_rank();
   int g, r0, r1;
-  // dense_rows > 0: rows [0, dense_rows) of A against every group's B (N tile y = group y, its
-  // BN rows), output columns y * BN ..; else rows of each group against that group's B
+  // tile of this cluster: (pair tile P, N tile nt).  With band > 0 the clusters, numbered in
+  // launch order, take bands of `band` pair tiles across every N tile, so that the clusters
+  // resident at once share a few row slabs of A and N tiles of B in L2 instead of streaming all
+  // rows for one N tile at a time
+  int P = blockIdx.x >> 1, nt = blockIdx.y;
+  if (band > 0) {
+    const int np = gridDim.x >> 1, ntn = gridDim.y;
+    const int c = blockIdx.y * np + P, per = band * ntn, b = c / per, in = c % per;
+    const int rows = min(band, np - b * band);
+    P = b * band + in % rows;
+    nt = in / rows;
+  }
+  // dense_rows > 0: rows [0, dense_rows) of A against every group's B (N tile nt = group nt, its
+  // BN rows), output columns nt * BN ..; else rows of each group against that group's B
   if (dense_rows > 0) {
-    const int P = blockIdx.x >> 1;
     if (P * 2 * kTile >= dense_rows) return;                                      // same for both CTAs
-    g = blockIdx.y;
+    g = nt;
     r0 = (2 * P + (int)rank) * kTile;
     r1 = dense_rows;
-  } else if (!pair_tile_of(row_begin, G, blockIdx.x >> 1, (int)rank, g, r0, r1)) {
+  } else if (!pair_tile_of(row_begin, G, P, (int)rank, g, r0, r1)) {
     return;                                                                        // same for both CTAs
   }
-  const int n0 = dense_rows > 0 ? 0 : blockIdx.y * BN;         // B rows of the N tile inside group g
-  const int oc0 = blockIdx.y * BN;                             // output columns
+  const int n0 = dense_rows > 0 ? 0 : nt * BN;                 // B rows of the N tile inside group g
+  const int oc0 = nt * BN;                                     // output columns
   uint8_t* smem = align1024(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const tc::Abort ab{&abort_flag, status};
@@ -2179,14 +2190,14 @@ static cudaError_t launch_gemm_pair(const CUtensorMap& A0, const CUtensorMap& A1
                                     const CUtensorMap& B1, int nk0, int nk1, const int32_t* row_begin, int G,
                                     int n_out, int b_stride, int b1_off, int pairs, void* out, int out_ld,
                                     const int32_t* scatter, DevStatus* st, cudaStream_t stream, const SlotMap& b0s,
-                                    int dense_rows = 0) {
+                                    int dense_rows = 0, int band = 0) {
   constexpr int STAGES = BN >= 256 ? 6 : 8;
   const size_t smem = 1024 + (size_t)STAGES * (kTile * 128 + (BN / 2) * 128);
   static std::atomic<uint64_t> attr{0};
   if (const cudaError_t e = smem_attr_once(tc_gemm_pair_kernel<BN, STAGES, OUT>, smem, attr); e != cudaSuccess) return e;
   return launch_pdl_cluster(tc_gemm_pair_kernel<BN, STAGES, OUT>, dim3(2 * pairs, n_out / BN), dim3(192),
                             dim3(2, 1, 1), smem, stream, A0, A1, B0, B1, nk0, nk1, row_begin, G, b_stride, b1_off,
-                            out, out_ld, scatter, st, dense_rows, b0s);
+                            out, out_ld, scatter, st, dense_rows, b0s, band);
 }
 
 template <int KRP, int KE>
@@ -2415,13 +2426,15 @@ cudaError_t launch_ffn_tc(const LayerArgs& a, const void* x, const void* wg, con
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   // 6. Y = [hsum | V~] [Wd | Bdn]^T, rows to their token slot
+  // the pair form runs its tiles in bands of kDownBand pair tiles across all d_model tiles
+  constexpr int kDownBand = 8;
   // many waves of single-CTA tiles: the persistent form overlaps each tile's epilogue with the
   // next tile's K loop
   const bool down_persist = !down_pair && BN2 == 256 && tiles * (d / 256) > 2 * 148;
   SlotMap wd_slots;                              // W_down rows of group g start at wslot[g] * d
   for (int i = 0; i < kMaxE; ++i) wd_slots.s[i] = a.tab.wslot[i];
   e = down_pair ? launch_gemm_pair<256, kOutBf16>(mH, mVt, mWd, mBd, f / 64, 2 * KRP / 64, row_begin, G, d, d, 0,
-                                                  pairs, y_rows, d, row_asg, status, st, wd_slots)
+                                                  pairs, y_rows, d, row_asg, status, st, wd_slots, 0, kDownBand)
       : down_persist ? launch_gemm_persist<256, kOutBf16>(mH, mVt, mWd, mBd, f / 64, 2 * KRP / 64, row_begin, G, d,
                                                           d, 0, tiles, y_rows, d, row_asg, status, st, wd_slots)
                 : (BN2 == 256 ? launch_gemm<256, kOutBf16>(mH, mVt, mWd, mBd, f / 64, 2 * KRP / 64, row_begin, G, d,
