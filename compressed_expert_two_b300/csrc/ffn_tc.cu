@@ -1653,16 +1653,18 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up4p_kernel(
   __shared__ int abort_flag;
 
   const uint32_t rank = tc::cluster_rank();
-  // work items w = chunk * n_row_tiles + pair tile, chunk-major so that the clusters running at
-  // once share a chunk's W tiles and keep re-reading the same X rows; cluster c takes items
-  // c, c + clusters, ...  Both CTAs of a cluster walk the same items (a pair tile is empty for
-  // both or for neither), every role skips the empty ones alike, and the stage ring, accumulator
-  // parity and slot phases run on across items (glt: tiles, sig: slots over the cluster's items).
+  // work items w = pair tile * n_chunks + chunk, taken by cluster c as c, c + clusters, ...: the
+  // clusters running at once cover a band of consecutive pair tiles across every chunk, so the
+  // band's X rows stay in L2 while they are re-read for each d_ff tile, and each W tile is read
+  // from DRAM about once per round of items.  Both CTAs of a cluster walk the same items (a pair
+  // tile is empty for both or for neither), every role skips the empty ones alike, and the stage
+  // ring, accumulator parity and slot phases run on across items (glt: tiles, sig: slots over the
+  // cluster's items).
   const int cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
   const int n_items = p.n_row_tiles * p.n_chunks;
   auto item = [&](int w, int& g, int& r0, int& r1, int& ft0, int& nft) -> bool {
-    if (!pair_tile_of(p.row_begin, p.G, w % p.n_row_tiles, (int)rank, g, r0, r1)) return false;
-    ft0 = (w / p.n_row_tiles) * p.ftiles_per_chunk;
+    if (!pair_tile_of(p.row_begin, p.G, w / p.n_chunks, (int)rank, g, r0, r1)) return false;
+    ft0 = (w % p.n_chunks) * p.ftiles_per_chunk;
     nft = min(ft0 + p.ftiles_per_chunk, p.n_ftiles) - ft0;
     return nft > 0;
   };
@@ -1865,7 +1867,7 @@ __global__ void __launch_bounds__(kUpWarps * 32, 1) ffn_up4p_kernel(
     for (int w = cluster; w < n_items && ok; w += clusters) {
       int g, r0, r1, ft0, nft;
       if (!item(w, g, r0, r1, ft0, nft)) continue;
-      const int i = r0 + row, chunk = w / p.n_row_tiles;
+      const int i = r0 + row, chunk = w % p.n_chunks;
       const bool valid = i < r1;
       int le[KE];
       float gt[KE];
@@ -2136,16 +2138,27 @@ int tc_up_chunks(const LayerArgs& a) {
   if (pair) units = a.R >= 2 * kTile * a.G ? (a.R + 2 * kTile - 1) / (2 * kTile) + (a.G + 1) / 2 : units;
   if (units < 1) units = 1;
   const int slots = pair ? 148 / 2 : 148;
-  int best = 1;
+  // The pair kernel's clusters running at once cover slots / c consecutive pair tiles: enough
+  // chunks that their X rows (256 rows of d_model each) take at most about 40 MB, so that they
+  // stay in L2 while W streams past (on the Mixtral shape 4 chunks read 1.05 GB from DRAM per
+  // launch, 2 chunks with all 33 pair tiles live 2.87 GB)
+  int min_c = 1;
+  if (pair) {
+    const double band_bytes = 40.0 * (1 << 20), tile_bytes = 2.0 * kTile * a.d * 2;
+    const int band = (int)(band_bytes / tile_bytes) > 1 ? (int)(band_bytes / tile_bytes) : 1;
+    min_c = (slots + band - 1) / band;
+  }
+  int best = 0;
   double best_cost = 1e30;
   for (int c = 1; c <= n_ft; ++c) {
     const int per = (n_ft + c - 1) / c;
     if (c > 1 && (n_ft + per - 1) / per != c) continue;     // same split as a smaller count
+    if (c < min_c && c < n_ft) continue;
     const double rounds = (double)((units * c + slots - 1) / slots);
     const double cost = rounds * (per + item_cost);
     if (cost < best_cost - 1e-9) { best_cost = cost; best = c; }
   }
-  return best;
+  return best > 0 ? best : n_ft;
 }
 
 template <int BN, int OUT>
