@@ -334,6 +334,16 @@ def test_wide_residual_many_rows_sampled(T, kg, ke, seed):
     full_size_check("wide_residual", 48, cfg)
 
 
+@pytest.mark.parametrize("T,ke,seed", [(6100, 2, 71), (6100, 1, 72)])
+def test_pair_gate_up_many_items_sampled(T, ke, seed):
+    """d_model = 4096 with about 6000 rows in two groups: the persistent CTA-pair gate/up kernel
+    walks more (pair tile, chunk) items than there are clusters, so clusters take several items
+    each (the stage ring, accumulator parity and slot phases carried across items), with ragged
+    pair tiles; sampled tokens against the oracle."""
+    cfg = small(T=T, d=4096, f=1024, E=8, G=2, kg=1, ke=ke, seed=seed, resid_std=0.2)
+    full_size_check("pair_items", 48, cfg)
+
+
 def test_persistent_down_gemm_sampled():
     """Many waves of down-projection tiles with a short K loop (d_ff = 256): the persistent grouped
     GEMM with double-buffered accumulators; sampled tokens against the oracle, ragged groups."""
