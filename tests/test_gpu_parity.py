@@ -344,6 +344,15 @@ def test_pair_gate_up_many_items_sampled(T, ke, seed):
     full_size_check("pair_items", 48, cfg)
 
 
+def test_pair_gate_up_skewed_groups_sampled():
+    """The persistent CTA-pair gate/up kernel (d_model = 4096) under a Zipf(2.5) group load: one
+    group holds most rows, the others a few ragged pair tiles or none; sampled tokens against
+    the oracle."""
+    cfg = small(T=4096, d=4096, f=1024, E=16, G=4, kg=1, ke=2, seed=75, resid_std=0.2, zipf_s=2.5,
+                group_map="contiguous")
+    full_size_check("pair_skewed", 48, cfg)
+
+
 def test_persistent_down_gemm_sampled():
     """Many waves of down-projection tiles with a short K loop (d_ff = 256): the persistent grouped
     GEMM with double-buffered accumulators; sampled tokens against the oracle, ragged groups."""
