@@ -2308,7 +2308,12 @@ static PrepArgs prep_args(const LayerArgs& a, const ResidPtrs& rp, const TcBufs&
 }
 
 bool tc_u_dense(const LayerArgs& a) {
-  return tc_path_ok(a) && a.R > kUSimtMaxRows && a.G * 2 * tc_krp(a) <= 512;
+  // the dense U runs beside the routing on the side stream: it pays while it is short next to
+  // the routing (small workload, 8.6 GFLOP: 0.145 -> 0.137 ms per step); as long as the routing
+  // (Mixtral shape, 34 GFLOP) it only competes with it for SMs, and the routed U after the
+  // gather is 0.6% faster per step
+  const double flops = 4.0 * a.T * a.G * 2 * tc_krp(a) * a.d;   // hi + lo stacks
+  return tc_path_ok(a) && a.R > kUSimtMaxRows && a.G * 2 * tc_krp(a) <= 512 && flops <= 16e9;
 }
 
 // 1. residual stacks (weights only: may run on another stream, concurrently with the routing),
