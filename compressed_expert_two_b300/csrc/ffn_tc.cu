@@ -2127,9 +2127,9 @@ int tc_up_chunks(const LayerArgs& a) {
   const bool pair = up4_ok(a);
   // The 128-column kernel is persistent: an item boundary costs about a tenth of a tile (the next
   // item's K loop runs under the previous item's slots).  The 256-column kernel pays half a tile
-  // per CTA; so, in effect, does the pair kernel: it walks items as well, but every SM it adds
-  // draws power from the same cap (measured on the Mixtral shape: 2 chunks on 132 SMs beat 56
-  // chunks on all 148 by 3%), so more, smaller items do not pay.
+  // per CTA.  The pair kernel walks items too, but on the Mixtral shape finer items that balance
+  // its two rounds gained under 1% and added V-partial traffic (28 chunks: 1.377 vs 1.389 ms, V
+  // reduction 20 vs 9 us), so it is costed like the 256-column kernel.
   const double item_cost = up3_ok(a) || pair ? 0.5 : 0.1;
   const int full = (a.R + kTile - 1) / kTile;
   // units per chunk that find rows (a group's last tile is ragged: about half of them add one),
